@@ -1,0 +1,549 @@
+#!/usr/bin/env python
+"""Benchmark of the quantized routed-expert MoE layer on GB300.
+
+One JSON line on rank 0.  A step is one pass of the whole layer path (route ->
+dispatch -> expert FFN -> combine) over one batch of synthetic tokens; for the
+42-layer workloads a step is a pass through all 42 layers.  ``value`` is
+MoE-layer tokens/s (tokens x layers per second) with inputs resident in HBM,
+timed with CUDA events over exactly K graph-replayed steps.  Weights rotate over
+enough distinct layer weight sets that every step streams its experts from HBM
+(more than L2 between reuses).
+
+Workloads (``--workload``):
+  decode1           H4096 I2048 E288 top-8 + shared, T = 1, all 289 experts in HBM
+  decode8_zipf_x42  T = 8, Zipf(1.1) routing bias, 42 distinct layers
+  cache4_x42        T = 4, Zipf(1.1), 42 layers, 100 experts/layer in pinned host memory
+  tiny              H256 I128 E16 top-4 + shared, T = 4
+``--impl reference`` times the fp64 CPU oracle (the only reference this build
+has) on a bounded sample of the same workload.
+"""
+
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import synthetic  # noqa: E402
+
+METRIC = "MoE-layer tokens/s at 1 GB300 and achieved HBM GB/s vs roofline (decode); prefill TFLOP/s"
+UNIT = "tokens/s"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+# ------------------------------------------------------------------ helpers
+
+def dist_env():
+    return (int(os.environ.get("RANK", 0)), int(os.environ.get("LOCAL_RANK", 0)),
+            int(os.environ.get("WORLD_SIZE", 1)))
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return d, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi clocks/throttle reasons sampled every 200 ms in the background."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.samples = []
+        self.proc = None
+        self.gpu = gpu_index
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "200"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except (FileNotFoundError, OSError):
+            self.proc = None
+            return
+        threading.Thread(target=self._read, daemon=True).start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.samples.append((time.time(), [c.strip() for c in line.split(",")]))
+
+    def stop(self):
+        if self.proc:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self, t0, t1):
+        rows = [r for (t, r) in self.samples if t0 <= t <= t1 and len(r) >= 9]
+        if not rows:
+            rows = [r for (_, r) in self.samples if len(r) >= 9][-3:]
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0}
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i].lower() == "active"})
+        return {"sm_mhz": float(np.median(sm)) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(rows)}
+
+
+# ------------------------------------------------------------------ our arm
+
+class Workload:
+    """Device weights for the timed steps: ``n_sets`` distinct layers that steps rotate over."""
+
+    def __init__(self, name, device, n_sets=None, log=print):
+        import torch
+        from quantized_routed_expert_03_gb300.layer import ExpertArena, MoELayer
+        self.cfg = cfg = synthetic.CONFIGS[name]
+        self.name = name
+        H, I, E, k, G, T = cfg.hidden, cfg.inter, cfg.n_experts, cfg.top_k, cfg.group, cfg.tokens
+        self.T = T
+        self.layers_per_step = cfg.layers
+        if n_sets is None:
+            n_sets = cfg.layers if cfg.layers > 1 else (8 if H >= 4096 else 2)
+        self.n_sets = n_sets
+        t0 = time.time()
+        self.sets = []
+        staging = None
+        for r in range(n_sets):
+            host = np.append(synthetic.host_resident(cfg, r), False)
+            n_host = int(host.sum())
+            dev = ExpertArena(H, I, G, E + 1 - n_host, device=device)
+            harena = ExpertArena(H, I, G, n_host, host=True) if n_host else None
+            if harena is not None and staging is None:
+                staging = torch.empty(dev.layout["stride"], dtype=torch.uint8, device=device)
+            entries, di, hi = [], 0, 0
+            for e in range(E + 1):
+                wg, wu, wd = synthetic.expert_fp32_torch(H, I, cfg.seed, r, e, device)
+                if host[e]:
+                    harena.quantize_into(hi, wg, wu, wd, staging=staging)
+                    entries.append(harena.addresses(hi) + (1,))
+                    hi += 1
+                else:
+                    dev.quantize_into(di, wg, wu, wd)
+                    entries.append(dev.addresses(di) + (0,))
+                    di += 1
+                del wg, wu, wd
+            L = MoELayer(H, I, E, k, G, T, device=device)
+            L.set_slots(entries)
+            wr = torch.from_numpy(synthetic.router_weights(E, H, cfg.seed, r)).to(device)
+            bias = (torch.from_numpy(synthetic.zipf_bias(E, cfg.seed, r)).to(device) if cfg.zipf else None)
+            self.sets.append({"layer": L, "dev": dev, "host": harena, "wr": wr, "bias": bias, "n_host": n_host})
+            if (r + 1) % 8 == 0:
+                log(f"[bench] built {r + 1}/{n_sets} layers ({time.time() - t0:.0f} s)")
+        torch.cuda.synchronize()
+        self.expert_payload = self.sets[0]["dev"].layout["payload"]
+        self.host_ranks = None
+        log(f"[bench] weights ready: {n_sets} layer(s), {time.time() - t0:.1f} s")
+
+    def x_pool(self, n, device):
+        """n distinct activation batches per layer set, [n_sets][n][T,H] bf16 on device."""
+        import torch
+        cfg = self.cfg
+        out = []
+        for r in range(self.n_sets):
+            xs = np.stack([synthetic.activations_bits(self.T, cfg.hidden, cfg.seed, r, 1000 + i) for i in range(n)])
+            out.append(torch.from_numpy(xs.view(np.int16)).to(device).view(torch.bfloat16))
+        return out
+
+
+def run_ours(args, rank, local_rank, world):
+    import torch
+    device = torch.device(f"cuda:{local_rank}")
+    torch.cuda.set_device(device)
+    from quantized_routed_expert_03_gb300 import build as qbuild
+    qbuild.build()
+    import quantized_routed_expert_03_gb300 as qre
+    qre.load_library()
+
+    log = (lambda *a: print(*a, file=sys.stderr, flush=True)) if rank == 0 else (lambda *a: None)
+    wl = Workload(args.workload, device, log=log)
+    cfg, T, H, k = wl.cfg, wl.T, wl.cfg.hidden, wl.cfg.top_k
+    stream = torch.cuda.Stream(device)
+
+    # one captured unit = `per_graph` steps; each step covers one layer set
+    # (single-layer workloads) or all layer sets (42-layer stacks)
+    stack = wl.layers_per_step > 1
+    per_graph = 1 if stack else wl.n_sets * 4
+    n_x = 4 if stack else per_graph // wl.n_sets
+    xs = wl.x_pool(n_x, device)
+    K, W = args.steps, args.warmup
+
+    ev_kw = {"enable_timing": True}
+    try:
+        torch.cuda.Event(enable_timing=True, external=True)
+        ev_kw["external"] = True
+    except TypeError:
+        pass
+    ffn_events = []           # (start, end) per FFN call in the instrumented graph
+    nact_log = torch.zeros(4096, dtype=torch.int32, device=device)
+    ffn_slots = []            # nact_log index per FFN call
+
+    def one_layer(s, x, instrument):
+        L = s["layer"]
+        L.route(x, s["wr"], s["bias"], T)
+        L.dispatch(T)
+        if instrument:
+            e0, e1 = torch.cuda.Event(**ev_kw), torch.cuda.Event(**ev_kw)
+            e0.record()
+            L.expert_ffn(x, T)
+            e1.record()
+            ffn_events.append((e0, e1))
+            i = len(ffn_slots)
+            nact_log[i:i + 1].copy_(L.n_active[:1])
+            ffn_slots.append(i)
+        else:
+            L.expert_ffn(x, T)
+        L.combine(T)
+
+    def step_fn(j, instrument):
+        if stack:
+            for r, s in enumerate(wl.sets):
+                one_layer(s, xs[r][j % n_x], instrument)
+        else:
+            r = j % wl.n_sets
+            one_layer(wl.sets[r], xs[r][(j // wl.n_sets) % n_x], instrument)
+
+    # eager warm-up (sets kernel attributes, loads modules) then capture
+    with torch.cuda.stream(stream):
+        for j in range(min(W, per_graph) if W else 1):
+            step_fn(j, False)
+    stream.synchronize()
+
+    def capture(nsteps, instrument):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            for j in range(nsteps):
+                step_fn(j, instrument and ev_kw.get("external", False))
+        return g
+
+    g_full = capture(per_graph, True)
+    rem = K % per_graph
+    g_rem = capture(rem, False) if rem else None
+    n_full = K // per_graph
+
+    # warm-up replays
+    for _ in range(max(1, math.ceil(W / per_graph))):
+        g_full.replay()
+    torch.cuda.synchronize()
+
+    sampler = ClockSampler(local_rank)
+    if not args.no_clocks:
+        sampler.start()
+        time.sleep(0.6)
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    t_wall0 = time.time()
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    start.record()
+    for _ in range(n_full):
+        g_full.replay()
+    if g_rem is not None:
+        g_rem.replay()
+    end.record()
+    torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    t_wall1 = time.time()
+    ms = start.elapsed_time(end)
+    if world > 1:
+        t = torch.tensor([ms], device=device)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        ms = float(t.item())
+    sampler.stop()
+    clocks = sampler.summary(t_wall0, t_wall1)
+
+    # FFN stage: events from the last replay of the instrumented graph
+    ffn_ms, ffn_bytes, n_act = [], [], []
+    if ffn_events and n_full > 0:
+        nact = nact_log.cpu().numpy()
+        for (e0, e1), i in zip(ffn_events, ffn_slots):
+            ffn_ms.append(e0.elapsed_time(e1))
+            a = int(nact[i])
+            n_act.append(a)
+            ffn_bytes.append((a + 1) * wl.expert_payload + T * H * 2 + (T * k + T) * H * 4)
+
+    tokens_per_step = T * wl.layers_per_step
+    value = world * tokens_per_step * K / (ms / 1e3)
+    peaks, peak_src = load_peaks()
+    roofline = None
+    if ffn_ms:
+        achieved = float(np.mean(ffn_bytes)) / (float(np.mean(ffn_ms)) / 1e3) / 1e9
+        sustained = stack
+        peak = float(peaks["hbm_gbs"])
+        roofline = {"bound": "hbm", "kernel": "qre_expert_ffn (gate/up + down dequant-GEMV kernels)",
+                    "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
+                    "frac": round(achieved / peak, 4), "traffic": args.traffic,
+                    "peak_source": f"{peak_src} (MEASURED_PEAKS.json hbm_gbs)" if peak_src == "measured" else
+                    "fallback 6.8 TB/s",
+                    "ffn_us_mean": round(float(np.mean(ffn_ms)) * 1e3, 2),
+                    "ffn_bytes_mean": int(np.mean(ffn_bytes)),
+                    "unique_experts_mean": round(float(np.mean(n_act)) + 1, 2),
+                    "timed_region": "last replay of the captured steps"}
+    step_bytes = None
+    if ffn_bytes:
+        per_layer = float(np.mean(ffn_bytes)) + cfg.n_experts * H * 4
+        step_bytes = per_layer * wl.layers_per_step
+        roofline["step_hbm_gbs"] = round(step_bytes / (ms / K / 1e3) / 1e9, 1)
+        host_bytes = 0.0
+
+    # ---------------- end to end: pinned host input -> graph -> pinned host output, synced per step
+    e2e = None
+    if not args.no_e2e:
+        e2e = run_e2e(args, wl, xs, stream, device, tokens_per_step, world)
+
+    out = {
+        "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world, "steps": K, "warmup": W,
+        "ms_per_step": round(ms / K, 6), "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "u4 weights x bf16 activations, fp32 accumulate", "data": "synthetic (seeded generators; "
+        "random-init weights quantized to the library's 4-bit group format)",
+        "config": {"workload": args.workload, "note": cfg.note, "tokens_per_step": T,
+                   "layers_per_step": wl.layers_per_step, "hidden": H, "inter": cfg.inter,
+                   "experts": cfg.n_experts, "top_k": k, "group": cfg.group,
+                   "l2": f"inputs larger than L2: {wl.n_sets} distinct layer weight sets rotated "
+                         f"({wl.n_sets * (cfg.n_experts + 1) * wl.expert_payload / 1e9:.1f} GB)",
+                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+                   "launch": "CUDA graph of captured steps"},
+        "gpu_launches": None, "roofline": roofline, "clocks": clocks, "e2e": e2e,
+    }
+    launches_per_layer = 2 + (1 if T * k <= 1024 else 3) + 2 + 1
+    out["gpu_launches"] = launches_per_layer * wl.layers_per_step * K
+    if rank == 0 and not args.no_cpu_baseline:
+        out["cpu_baseline"] = cpu_baseline(args, wl, device)
+    return out
+
+
+def run_e2e(args, wl, xs, stream, device, tokens_per_step, world):
+    import torch
+    T, H = wl.T, wl.cfg.hidden
+    stack = wl.layers_per_step > 1
+    sets = wl.sets
+    xin_dev = [torch.empty((T, H), dtype=torch.bfloat16, device=device) for _ in sets]
+    graphs = []
+    # one graph per layer set (single-layer workloads) or one for the whole stack
+    def body(idx):
+        s = sets[idx]
+        L = s["layer"]
+        L.forward(xin_dev[idx], s["wr"], s["bias"], T)
+    with torch.cuda.stream(stream):
+        for i in range(len(sets)):
+            body(i)
+    stream.synchronize()
+    if stack:
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            for i in range(len(sets)):
+                body(i)
+        graphs = [g]
+    else:
+        for i in range(len(sets)):
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=stream):
+                body(i)
+            graphs.append(g)
+    n_x = xs[0].shape[0]
+    host_x = [xs[r].cpu().pin_memory() for r in range(len(sets))]
+    host_y = [torch.empty((T, H), dtype=torch.bfloat16).pin_memory() for _ in sets]
+    K = min(args.steps, args.e2e_steps)
+    h2d = (len(sets) if stack else 1) * T * H * 2
+    d2h = h2d
+
+    def one(j):
+        if stack:
+            for r in range(len(sets)):
+                xin_dev[r].copy_(host_x[r][j % n_x], non_blocking=True)
+            graphs[0].replay()
+            for r in range(len(sets)):
+                host_y[r].copy_(sets[r]["layer"].y_bf16[:T], non_blocking=True)
+        else:
+            r = j % len(sets)
+            xin_dev[r].copy_(host_x[r][(j // len(sets)) % n_x], non_blocking=True)
+            graphs[r].replay()
+            host_y[r].copy_(sets[r]["layer"].y_bf16[:T], non_blocking=True)
+        stream.synchronize()
+
+    with torch.cuda.stream(stream):
+        for j in range(3):
+            one(j)
+        torch.cuda.synchronize()
+        if world > 1:
+            torch.distributed.barrier()
+        s0, s1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        s0.record(stream)
+        for j in range(K):
+            one(j)
+        s1.record(stream)
+        torch.cuda.synchronize()
+    ms = s0.elapsed_time(s1)
+    return {"value": round(world * tokens_per_step * K / (ms / 1e3), 2), "unit": UNIT, "steps": K,
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+            "api": "MoELayer.forward captured in a CUDA graph; per step: pinned H2D input copy, replay, "
+                   "pinned D2H of the bf16 output, stream synchronize"}
+
+
+# ------------------------------------------------------------------ oracle (CPU) legs
+
+def _oracle_expert_source(cfg, layer, device):
+    """Oracle-quantized experts of one layer, from the same generator the GPU side used."""
+    from oracle import quant as oquant
+    cache = {}
+
+    def get(e):
+        e = int(e)
+        if e not in cache:
+            if device is not None:
+                import torch  # noqa: F401
+                w = [t.cpu().numpy() for t in synthetic.expert_fp32_torch(cfg.hidden, cfg.inter, cfg.seed, layer,
+                                                                           e, device)]
+            else:
+                w = synthetic.expert_fp32(cfg.hidden, cfg.inter, cfg.seed, layer, e)
+            cache[e] = oquant.quantize_expert(*w, cfg.group)
+        return cache[e]
+    return get
+
+
+def cpu_baseline(args, wl, device):
+    """The oracle timed on this host's cores for one full layer-token of the workload."""
+    from oracle import moe as omoe
+    cfg = wl.cfg
+    get = _oracle_expert_source(cfg, 0, device)
+    x_bits = synthetic.activations_bits(1, cfg.hidden, cfg.seed, 0, 1000)
+    wr = synthetic.router_weights(cfg.n_experts, cfg.hidden, cfg.seed, 0)
+    bias = synthetic.zipf_bias(cfg.n_experts, cfg.seed, 0) if cfg.zipf else None
+    r = omoe.route(omoe.bf16_bits_to_f64(x_bits), wr, bias, cfg.top_k)
+    need = list(r["idx"][0]) + [cfg.n_experts]
+    for e in need:                       # quantization is weight preparation, not timed
+        get(e)
+
+    class View:
+        def __getitem__(self, e):
+            return get(e)
+    t0 = time.perf_counter()
+    omoe.moe_layer(x_bits, wr, bias, View(), get(cfg.n_experts), cfg.hidden, cfg.inter, cfg.n_experts,
+                   cfg.top_k, cfg.group)
+    dt = time.perf_counter() - t0
+    return {"value": round(1.0 / dt, 5), "unit": UNIT, "cores": len(os.sched_getaffinity(0)), "kind": "oracle",
+            "sample": f"1 token through 1 layer of {args.workload} (route + {len(need)} experts dequantized "
+                      f"and applied in fp64 numpy); {dt:.1f} s"}
+
+
+def run_reference(args):
+    """--impl reference: the oracle, on a per-step sample sized to end in a few minutes."""
+    from oracle import moe as omoe
+    from oracle import quant as oquant
+    cfg = synthetic.CONFIGS[args.workload]
+    H, I, E, k, G = cfg.hidden, cfg.inter, cfg.n_experts, cfg.top_k, cfg.group
+    device = None
+    try:
+        import torch
+        if torch.cuda.is_available():
+            device = torch.device("cuda:0")
+    except Exception:
+        pass
+    get = _oracle_expert_source(cfg, 0, device)
+    wr = synthetic.router_weights(E, H, cfg.seed, 0)
+    bias = synthetic.zipf_bias(E, cfg.seed, 0) if cfg.zipf else None
+    # The FFN of one expert splits exactly into I/16 blocks of 16 intermediate
+    # features (16 gate rows + 16 up rows of the interleaved matrix, 16 down
+    # columns).  A layer-token is (k + 1) experts x I/16 blocks.  A step is the
+    # route of one token plus m blocks of its experts.
+    pool = [get(e) for e in range(2)] + [get(E)]
+    blocks_per_token = (k + 1) * (I // 16)
+
+    def block(ex, x, i):
+        comb = oquant.dequantize_matrix(ex["w_gate_up"][32 * i:32 * i + 32], ex["s_gate_up"][32 * i:32 * i + 32], H, G)
+        g, u = comb[:16], comb[16:]
+        c0 = 16 * i
+        wd = oquant.dequantize_matrix(ex["w_down"][:, c0 // 2:c0 // 2 + 8],
+                                      ex["s_down"][:, c0 // G:c0 // G + 1], 16, 16)
+        return wd @ (omoe.silu(g @ x) * (u @ x))
+
+    def step(j, m):
+        x_bits = synthetic.activations_bits(1, H, cfg.seed, 0, 1000 + j)
+        x = omoe.bf16_bits_to_f64(x_bits)
+        omoe.route(x, wr, bias, k)
+        acc = np.zeros(H)
+        for b in range(m):
+            ex = pool[(j + b) % len(pool)]
+            acc += block(ex, x[0], (j * m + b) % (I // 16))
+        return acc
+
+    t0 = time.perf_counter()
+    step(0, 4)
+    t_block = (time.perf_counter() - t0) / 4
+    budget = 150.0 / max(1, args.steps + args.warmup)
+    m = int(max(1, min(blocks_per_token, budget / max(t_block, 1e-6))))
+    for j in range(args.warmup):
+        step(j, m)
+    t0 = time.perf_counter()
+    for j in range(args.steps):
+        step(args.warmup + j, m)
+    dt = time.perf_counter() - t0
+    tokens = args.steps * m / blocks_per_token * (cfg.tokens if cfg.layers == 1 else 1)
+    value = tokens / dt
+    sample = (f"per step: route 1 token + {m} of the {blocks_per_token} 16-feature FFN blocks of a "
+              f"{args.workload} layer-token (fp64 numpy oracle); scaled to layer-tokens")
+    return {"metric": METRIC, "value": round(value, 6), "unit": UNIT, "n_gpus": 1, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": round(dt / args.steps * 1e3, 3), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": args.workload, "note": cfg.note}, "impl": "reference",
+            "cpu_baseline": {"value": round(value, 6), "unit": UNIT, "cores": len(os.sched_getaffinity(0)),
+                             "kind": "oracle", "sample": sample},
+            "e2e": {"value": round(value, 6), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20000)
+    ap.add_argument("--warmup", type=int, default=64)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="decode1", choices=sorted(synthetic.CONFIGS))
+    ap.add_argument("--e2e-steps", type=int, default=5000)
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-clocks", action="store_true")
+    ap.add_argument("--traffic", type=float, default=None,
+                    help="ncu dram bytes per FFN launch, when a capture of the current kernels exists")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    rank, local_rank, world = dist_env()
+    if args.impl == "reference":
+        if rank == 0:
+            print(json.dumps(run_reference(args)), flush=True)
+        return
+    if world > 1:
+        import torch
+        torch.cuda.set_device(local_rank)
+        torch.distributed.init_process_group("nccl")
+    out = run_ours(args, rank, local_rank, world)
+    if rank == 0:
+        print(json.dumps(out), flush=True)
+    if world > 1:
+        import torch
+        torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,255 @@
+/*
+ * qre.h -- C ABI of the quantized routed-expert MoE layer for GB300 (sm_103a).
+ *
+ * One routed mixture-of-experts layer: a sigmoid top-k router, a token->expert
+ * dispatch through an expert slot (pointer) table, a fused dequant + SwiGLU
+ * expert FFN over 4-bit group-quantized weights that live either in device
+ * memory (HBM cache slots) or in pinned host memory read zero-copy, a shared
+ * expert, and the routing-weighted combine.
+ *
+ * Sources.  The pages this library follows are serving recipes for
+ * GLM-5.3-Flash with expert offload: "GLM-5.3-Flash EXL3 3.05bpw on 1x RTX PRO
+ * 6000" (GPU expert cache, host-RAM streaming), "... on 1x RTX 3090" (RAM/NVMe
+ * expert tiering), "... 2.05bpw on 2x RTX 5090" and the glm53-flash-offload
+ * README.  They fix 288 routed experts, top-8 routing, a shared expert, expert
+ * pointer tables rewritten in place, zero-copy reads of host-resident experts and
+ * a ~1e-3 relative RMS error class per expert kernel.  They do not define the
+ * router function, the weight codebook or any kernel; those are this library's.
+ *
+ * Conventions (all entry points)
+ *   - Every pointer argument is a DEVICE pointer unless its comment says "host".
+ *     Pinned host memory mapped into the device address space (cudaHostAlloc with
+ *     cudaHostAllocMapped, or cudaHostRegister + device pointer) counts as a
+ *     device pointer where a comment says "device or host-mapped".
+ *   - The caller owns and allocates every buffer, including the workspace.  The
+ *     library allocates no memory on any call and keeps no state apart from a
+ *     per-device status word and a thread-local error message.
+ *   - Calls are asynchronous on the given stream (NULL = the legacy default
+ *     stream) and never synchronize with the host, except the two functions
+ *     that read the device status word.  Dependent calls must share a stream.
+ *   - Argument, shape and alignment errors are detected on the host before any
+ *     launch and returned synchronously; nothing is launched then.  Launch
+ *     failures return QRE_ERR_CUDA.  Conditions only visible on the device (a
+ *     null slot pointer, a non-finite scale, a wait that ran out of time) are
+ *     recorded in the device status word, and the kernel skips the affected
+ *     work instead of faulting; read it with qre_read_device_status.
+ *   - qre_last_error() returns the message of the last failing call made by
+ *     the calling host thread.
+ *   - Supported shapes: hidden and inter multiples of 128 and at most 4096;
+ *     group in {32, 64, 128} dividing both; 1 <= n_experts <= 1024;
+ *     1 <= top_k <= min(16, n_experts); 0 <= T <= 65536 / top_k.  T == 0 is a
+ *     valid empty call that launches nothing.
+ *   - Alignment: every array base must be 16-byte aligned.
+ */
+#ifndef QRE_H
+#define QRE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define QRE_API __attribute__((visibility("default")))
+#else
+#define QRE_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* A CUDA stream handle (cudaStream_t / CUstream). */
+typedef struct CUstream_st* qre_stream_t;
+
+typedef enum {
+  QRE_OK = 0,
+  QRE_ERR_INVALID_ARG = 1,   /* null pointer, negative size, k > E, ...            */
+  QRE_ERR_UNSUPPORTED = 2,   /* shape outside the supported set                    */
+  QRE_ERR_MISALIGNED = 3,    /* an array base is not 16-byte aligned               */
+  QRE_ERR_WORKSPACE = 4,     /* workspace smaller than qre_workspace_size()        */
+  QRE_ERR_CUDA = 5,          /* a CUDA runtime call or launch failed               */
+  QRE_ERR_TIMEOUT = 6,       /* device status: a bounded wait ran out of time      */
+  QRE_ERR_DEVICE_CHECK = 7   /* device status: a device-side check failed          */
+} qre_status;
+
+/* Device status word bits (qre_read_device_status). */
+#define QRE_DEV_TIMEOUT       0x1   /* a pipeline wait gave up; results are invalid  */
+#define QRE_DEV_NULL_SLOT     0x2   /* an active expert's slot has a null pointer    */
+#define QRE_DEV_BAD_SCALE     0x4   /* quantize: a group scale was not finite        */
+#define QRE_DEV_BAD_INDEX     0x8   /* an expert id outside [0, n_experts)           */
+
+/* Layer shape.  H = hidden, I = expert intermediate, E = routed experts,
+ * k = experts per token, G = quantization group along the reduction axis. */
+typedef struct {
+  int32_t hidden;
+  int32_t inter;
+  int32_t n_experts;
+  int32_t top_k;
+  int32_t group;
+} qre_layer_shape;
+
+/*
+ * One expert slot: where an expert's packed weights are.  The slot table is a
+ * DEVICE array of n_experts + 1 entries; entry n_experts is the shared expert.
+ * It plays the role of the per-expert pointer tables that the RTX PRO 6000
+ * recipe rewrites in place (config.expert_cache.mechanism): retargeting an
+ * expert from a cache slot to host memory is a write of this struct.
+ *
+ * Weight format (packed 4-bit symmetric groups, fp16 scales), for a matrix
+ * W [N, K] with K contiguous and groups of G along K:
+ *   s = fp16_RNE(max|w| / 7) (fp64 quotient), q = clamp(rint_half_even(w / s),
+ *   -8, 7) (q = 0 when s == 0), nibble u = q + 8 at byte (n*K + k)/2, even k in
+ *   the low nibble; dequantized value (u - 8) * s.
+ * The gate and up projections ([I, H] each) are stored as one [2I, H] matrix
+ * whose rows alternate in blocks of 16 (16 gate rows, 16 up rows, ...).
+ */
+typedef struct {
+  const uint8_t*  w_gate_up;  /* [2I][H/2] packed, device or host-mapped        */
+  const uint16_t* s_gate_up;  /* fp16 [2I][H/G], device or host-mapped          */
+  const uint8_t*  w_down;     /* [H][I/2] packed, device or host-mapped         */
+  const uint16_t* s_down;     /* fp16 [H][I/G], device or host-mapped           */
+  uint32_t tier;              /* 0 = device memory (read through shared-memory
+                                 bulk copies), 1 = host-mapped (read with direct
+                                 loads over the host link)                      */
+  uint32_t reserved;          /* must be 0                                      */
+} qre_slot;
+
+/* Message of the last failing call on this host thread ("" if none). */
+QRE_API const char* qre_last_error(void);
+
+/* Short name of a status code. */
+QRE_API const char* qre_status_string(qre_status status);
+
+/* Library version as MAJOR*10000 + MINOR*100 + PATCH. */
+QRE_API int32_t qre_version(void);
+
+/*
+ * Bytes of workspace that qre_route, qre_dispatch and qre_expert_ffn need for a
+ * call with T tokens (the maximum over the three; one buffer serves all).
+ * bytes: host pointer, written on success.  The workspace content need not be
+ * initialised and is not preserved between calls.
+ */
+QRE_API qre_status qre_workspace_size(const qre_layer_shape* shape, int32_t T, size_t* bytes);
+
+/*
+ * Quantize an fp32 matrix into the packed format above (the same rule as the
+ * slot table's comment).  This is the offline step that produces expert
+ * weights; it is not part of the per-token path.
+ *   w       [n_rows][k_dim] fp32, device
+ *   packed  [n_rows][k_dim/2] uint8, device (written)
+ *   scales  [n_rows][k_dim/group] fp16 bits, device (written)
+ * group in {32, 64, 128}; k_dim a positive multiple of group; n_rows >= 0.
+ * A non-finite scale sets QRE_DEV_BAD_SCALE in the device status word.
+ */
+QRE_API qre_status qre_quantize(int32_t n_rows, int32_t k_dim, int32_t group, const float* w,
+                        uint8_t* packed, uint16_t* scales, qre_stream_t stream);
+
+/*
+ * Quantize one expert's gate and up projections (w_gate, w_up: [inter][hidden]
+ * fp32, device) into the interleaved [2*inter][hidden] layout described at
+ * qre_slot: packed [2*inter][hidden/2] uint8 and scales [2*inter][hidden/group]
+ * fp16 bits (device, written).  inter a positive multiple of 16, hidden a
+ * positive multiple of group, group in {32, 64, 128}.  A non-finite scale sets
+ * QRE_DEV_BAD_SCALE.
+ */
+QRE_API qre_status qre_quantize_gate_up(int32_t inter, int32_t hidden, int32_t group, const float* w_gate,
+                                        const float* w_up, uint8_t* packed, uint16_t* scales,
+                                        qre_stream_t stream);
+
+/*
+ * Router: logits l = x W_r^T (fp32 accumulation), scores s = sigmoid(l),
+ * selection score s + bias (bias is selection-only; NULL = 0), the top_k experts
+ * by selection score with ties to the lower id, written in ascending id order,
+ * and weights w = s / sum(s over the selection).  Top-8 of 288: GLM-5.3-Flash
+ * EXL3 3.05bpw on 1x RTX 3090 recipe, summary (each token takes 8 of the 288
+ * experts of every layer);
+ * the sigmoid/renormalise rule is this library's reading (the pages are silent).
+ *   x_bf16    [T][H] bf16 bits, device
+ *   w_router  [E][H] fp32, device
+ *   bias      [E] fp32 or NULL, device
+ *   topk_idx  [T][k] int32, device (written)
+ *   topk_w    [T][k] fp32, device (written)
+ *   workspace device, >= qre_workspace_size bytes
+ */
+QRE_API qre_status qre_route(const qre_layer_shape* shape, int32_t T, const uint16_t* x_bf16,
+                     const float* w_router, const float* bias, int32_t* topk_idx,
+                     float* topk_w, void* workspace, size_t workspace_bytes,
+                     qre_stream_t stream);
+
+/*
+ * Dispatch: deduplicate the picks into the expert union that all tokens share
+ * (glm53-flash-offload README, "Elastic CLOCK expert cache": a one-block kernel
+ * dedups the router picks; "Batched decode": streams share the per-layer expert
+ * union).  For the T*k picks p = t*k + j:
+ *   counts   [E] int32     picks per expert
+ *   offsets  [E+1] int32   exclusive prefix sum of counts
+ *   perm     [T*k] int32   pick ids sorted stably by (expert, p)
+ *   inv_perm [T*k] int32   inv_perm[perm[q]] = q
+ *   active   [E] int32     experts with counts > 0, ascending (first n_active valid)
+ *   n_active [1] int32     number of active experts (stays on the device)
+ * All outputs device, written.  topk_idx [T][k] int32 device: each row must hold
+ * distinct ids in [0, E); an id outside that range sets QRE_DEV_BAD_INDEX and is
+ * dropped.  Results are deterministic.
+ */
+QRE_API qre_status qre_dispatch(const qre_layer_shape* shape, int32_t T, const int32_t* topk_idx,
+                        int32_t* counts, int32_t* offsets, int32_t* perm, int32_t* inv_perm,
+                        int32_t* active, int32_t* n_active, void* workspace,
+                        size_t workspace_bytes, qre_stream_t stream);
+
+/*
+ * Expert FFN: for every active expert e and each of its picks, and for the
+ * shared expert (slot n_experts) over all T tokens,
+ *   o = W_down (silu(W_gate x) * (W_up x)),
+ * with weights dequantized on the fly from the slot table (the fused MoE kernel
+ * of the glm53-flash-offload README, "Quality" section: ~1e-3 relative RMS per
+ * expert is the error class; host-resident experts are read zero-copy as in the
+ * README's "Zero-copy home").
+ *   x_bf16      [T][H] bf16 bits, device
+ *   slots       [E+1] qre_slot, device
+ *   offsets, perm, active, n_active: from qre_dispatch, device
+ *   expert_out  [T*k + T][H] fp32, device (written): row q < T*k is the output
+ *               of pick perm[q] (unweighted), row T*k + t the shared expert's
+ *               output for token t.
+ * T <= 8 runs the bandwidth-bound decode kernels (fp32-exact products, fp32
+ * accumulation); larger T runs the grouped-GEMM path (fp16 operands, fp32
+ * accumulation).
+ */
+QRE_API qre_status qre_expert_ffn(const qre_layer_shape* shape, int32_t T, const uint16_t* x_bf16,
+                          const qre_slot* slots, const int32_t* offsets, const int32_t* perm,
+                          const int32_t* active, const int32_t* n_active, float* expert_out,
+                          void* workspace, size_t workspace_bytes, qre_stream_t stream);
+
+/*
+ * Combine: y[t] = sum_j topk_w[t][j] * expert_out[inv_perm[t*k + j]] +
+ * expert_out[T*k + t], accumulated in fp32 in ascending j (ascending expert
+ * id), the shared term last.  The fp32 partial sums are added after the
+ * experts, as the glm53-flash-offload README's "CPU tier" bullet does.
+ *   expert_out [T*k + T][H] fp32, topk_w [T][k] fp32, inv_perm [T*k] int32: device
+ *   y_f32  [T][H] fp32, device (written)
+ *   y_bf16 [T][H] bf16 bits or NULL, device (written): round-to-nearest-even
+ *          of y_f32.
+ */
+QRE_API qre_status qre_combine(const qre_layer_shape* shape, int32_t T, const float* expert_out,
+                       const float* topk_w, const int32_t* inv_perm, float* y_f32,
+                       uint16_t* y_bf16, qre_stream_t stream);
+
+/*
+ * Checks a HOST copy of a slot table before it is uploaded: every pointer
+ * non-null and 16-byte aligned, reserved == 0, tier in {0, 1}, tier-0
+ * pointers in device memory and tier-1 pointers in host memory that the
+ * device can read.  host_slots: host array of n_experts + 1 entries.
+ */
+QRE_API qre_status qre_validate_slots(const qre_layer_shape* shape, const qre_slot* host_slots);
+
+/*
+ * Synchronizes the stream, then writes the current device's status word
+ * (QRE_DEV_* bits, 0 = clean) to *status (host).  qre_clear_device_status
+ * resets it to 0 (also synchronizing the stream).
+ */
+QRE_API qre_status qre_read_device_status(qre_stream_t stream, int32_t* status);
+QRE_API qre_status qre_clear_device_status(qre_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* QRE_H */

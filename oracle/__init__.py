@@ -10,9 +10,9 @@ Modules
 -------
 ``oracle.quant``
     The packed 4-bit group-quantized weight format: quantize, dequantize, and the
-    gate/up row interleave.  The pages do not define the EXL3 codebook (glm53-flash-
-    offload README, "CPU tier" and "Credits" bullets name only "MUL1/K=3 trellis"),
-    so the format is this library's own.
+    gate/up row interleave.  The pages name the EXL3 trellis codebook but do not
+    define it (glm53-flash-offload README, "CPU tier" bullet), so the format is
+    this library's own.
 ``oracle.moe``
     Router (sigmoid scores, top-k, renormalise), dispatch (histogram, stable
     permutation, active list), the SwiGLU expert FFN on dequantized weights, the

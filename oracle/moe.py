@@ -4,7 +4,7 @@ TEST INFRASTRUCTURE ONLY (see ``oracle/__init__``).
 
 What the pages fix, and what this module reads into them
     * 288 routed experts, top-8 per token per layer (GLM-5.3-Flash EXL3 3.05bpw on
-      1x RTX 3090 recipe, ``summary``: "8 picked per token per layer"); a shared
+      1x RTX 3090 recipe, ``summary``: each token takes 8 experts per layer); a shared
       expert that runs beside the routed ones (glm53-flash-offload README,
       "Decode kernels" bullet: the shared expert moved to a side stream).
     * Picks are deduplicated per layer into one expert union that all tokens of

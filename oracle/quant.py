@@ -4,10 +4,10 @@ TEST INFRASTRUCTURE ONLY (see ``oracle/__init__``).
 
 Why a format of our own
     The pages store experts as EXL3 trellis codes (GLM-5.3-Flash EXL3 3.05bpw on
-    1x RTX PRO 6000 recipe, ``summary`` and ``config.expert_cache.layout``:
-    "~9 MiB/expert at 3.05bpw"), but they never define the codebook (the
-    glm53-flash-offload README, "CPU tier" bullet, only names a "MUL1/K=3 trellis
-    kernel").  This library therefore defines a plain symmetric 4-bit group format
+    1x RTX PRO 6000 recipe, ``summary`` and ``config.expert_cache.layout``: about
+    9 MiB per expert at 3.05 bits per weight), but they never define the codebook
+    (the glm53-flash-offload README, "CPU tier" bullet, names the trellis variant
+    and nothing more).  This library therefore defines a plain symmetric 4-bit group format
     with fp16 scales.  It is a weight-only quantization, as on the pages.
 
 Definition (for a weight matrix ``W`` of shape ``[N, K]``, fp32, K contiguous)

@@ -1,0 +1,149 @@
+// common.cuh -- device helpers shared by the library's kernels (sm_103a).
+//
+// Inline PTX for mbarriers, bulk (TMA) copies, the warp-level f16 tensor-core
+// MMA, the global timer used to bound every wait, and the device status word.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <cuda_fp16.h>
+#include <cuda_bf16.h>
+#include <stdint.h>
+
+#include "../../include/qre.h"
+
+namespace qre {
+
+// Every spin-wait in this library gives up after this many nanoseconds, records
+// QRE_DEV_TIMEOUT in the status word and lets the kernel finish.
+constexpr uint64_t kWaitLimitNs = 1000000000ull;
+
+__device__ __forceinline__ uint64_t global_timer_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+__device__ __forceinline__ void set_status(int* status, int bits) {
+  if (status) atomicOr(status, bits);
+}
+
+__device__ __forceinline__ uint32_t smem_addr(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+// ---------------------------------------------------------------- mbarrier
+
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(bar)), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void fence_barrier_init() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_addr(bar)), "r"(bytes)
+               : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(bar)) : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+  uint32_t done;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(done)
+      : "r"(smem_addr(bar)), "r"(parity)
+      : "memory");
+  return done != 0;
+}
+
+// Waits for the phase of `bar` with the given parity.  Gives up when *abort is
+// set by another warp, or when the global timer passes `deadline` (then it sets
+// *abort and the status bit).  Returns true when the phase completed.
+__device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity, volatile int* abort,
+                                                  uint64_t deadline, int* status) {
+  uint32_t spins = 0;
+  while (!mbar_try_wait(bar, parity)) {
+    if (abort && *abort) return false;
+    if ((++spins & 63u) == 0 && global_timer_ns() > deadline) {
+      if (abort) *abort = 1;
+      set_status(status, QRE_DEV_TIMEOUT);
+      return false;
+    }
+  }
+  return true;
+}
+
+// ---------------------------------------------------------------- bulk copy
+
+// 1-D bulk copy global -> shared, completing `bytes` transaction bytes on `bar`.
+// dst, src 16-byte aligned; bytes a multiple of 16.
+__device__ __forceinline__ void bulk_copy_g2s(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+          smem_addr(dst)),
+      "l"(src), "r"(bytes), "r"(smem_addr(bar))
+      : "memory");
+}
+
+// ---------------------------------------------------------------- named barrier
+
+__device__ __forceinline__ void named_barrier_sync(int id, int nthreads) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
+}
+
+// ---------------------------------------------------------------- PDL
+
+__device__ __forceinline__ void grid_dependency_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void grid_dependents_launch() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+// ---------------------------------------------------------------- tensor-core MMA
+
+// D[16x8] += A[16x16] * B[16x8]; f16 operands, f32 accumulators.
+__device__ __forceinline__ void mma_f16_16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                              uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+      "{%0,%1,%2,%3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+// ---------------------------------------------------------------- 4-bit decode
+
+__device__ __forceinline__ uint32_t h2_as_u32(__half2 v) { return *reinterpret_cast<uint32_t*>(&v); }
+__device__ __forceinline__ __half2 u32_as_h2(uint32_t v) { return *reinterpret_cast<__half2*>(&v); }
+
+// Decodes the eight nibbles u0..u7 of one 32-bit word (u_i at bits 4i..4i+3)
+// into four fp16 pairs holding the signed codes q = u - 8, exactly:
+//   p[0] = (q0, q4), p[1] = (q1, q5), p[2] = (q2, q6), p[3] = (q3, q7)
+// (low half first).  OR-ing a nibble into the mantissa of fp16 1024 gives
+// 1024 + u (low nibble) or 1024 + 16u (high nibble of a byte); one subtract or
+// one fused multiply-add removes the offset.  All steps are exact in fp16.
+__device__ __forceinline__ void decode_nibbles(uint32_t w, uint32_t (&p)[4]) {
+  const uint32_t lo_mask = 0x000F000Fu, hi_mask = 0x00F000F0u, magic = 0x64006400u;
+  const __half2 k1032 = u32_as_h2(0x64086408u);   // 1032 = 1024 + 8
+  const __half2 k1_16 = u32_as_h2(0x2C002C00u);   // 1/16
+  const __half2 km72 = u32_as_h2(0xD480D480u);    // -72 = -(64 + 8)
+  const uint32_t w8 = w >> 8;
+  p[0] = h2_as_u32(__hsub2(u32_as_h2((w & lo_mask) | magic), k1032));
+  p[1] = h2_as_u32(__hfma2(u32_as_h2((w & hi_mask) | magic), k1_16, km72));
+  p[2] = h2_as_u32(__hsub2(u32_as_h2((w8 & lo_mask) | magic), k1032));
+  p[3] = h2_as_u32(__hfma2(u32_as_h2((w8 & hi_mask) | magic), k1_16, km72));
+}
+
+__device__ __forceinline__ float bf16_bits_to_float(uint32_t b) { return __uint_as_float(b << 16); }
+
+__device__ __forceinline__ uint32_t pack_half2(float lo, float hi) {
+  return h2_as_u32(__floats2half2_rn(lo, hi));
+}
+
+}  // namespace qre

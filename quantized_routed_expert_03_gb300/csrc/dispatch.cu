@@ -1,0 +1,192 @@
+// dispatch.cu -- per-expert histogram, offsets, stable permutation, active list.
+//
+// The glm53-flash-offload README ("Elastic CLOCK expert cache") dedups the
+// router picks of a layer in one block; batched streams share the resulting
+// expert union ("Batched decode").  Here the T*k picks p = t*k + j are ordered
+// stably by (expert, p): perm[q] is the pick at sorted position q, inv_perm its
+// inverse, offsets the exclusive prefix sum of the per-expert counts, and
+// active the ascending list of experts with at least one pick.
+//
+// Every step is integer-exact and order-fixed, so the result is deterministic.
+// Picks are cut into chunks of kChunk; each expert's thread walks a chunk in
+// pick order, which makes the placement stable without any sort:
+//   * one chunk (decode): a single CTA does count, scan and placement;
+//   * several chunks (prefill): count per chunk, one scan CTA over (chunk,
+//     expert), then placement per chunk from the chunk's base offsets.
+#include "common.cuh"
+#include "internal.h"
+
+namespace qre {
+namespace {
+
+constexpr int kChunk = 1024;
+
+// Block-wide exclusive scan of one value per thread (blockDim.x <= 1024).
+__device__ int block_exclusive_scan(int v, int* warp_tot, int* total) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = (blockDim.x + 31) >> 5;
+  int inc = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int y = __shfl_up_sync(0xffffffffu, inc, o);
+    if (lane >= o) inc += y;
+  }
+  if (lane == 31) warp_tot[warp] = inc;
+  __syncthreads();
+  if (warp == 0) {
+    int w = lane < nw ? warp_tot[lane] : 0;
+    int wi = w;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, wi, o);
+      if (lane >= o) wi += y;
+    }
+    if (lane < nw) warp_tot[lane] = wi - w;
+    if (lane == nw - 1) *total = wi;
+  }
+  __syncthreads();
+  const int r = warp_tot[warp] + inc - v;
+  __syncthreads();
+  return r;
+}
+
+__device__ __forceinline__ int load_pick(const int32_t* idx, int p, int E, int* status) {
+  const int e = idx[p];
+  if (e < 0 || e >= E) {
+    set_status(status, QRE_DEV_BAD_INDEX);
+    return -1;
+  }
+  return e;
+}
+
+// Places the picks of one chunk: thread e walks the chunk in pick order.
+__device__ void place_chunk(const int* s_idx, int p0, int n, int E, int base_e, int32_t* perm, int32_t* inv_perm) {
+  const int e = threadIdx.x;
+  if (e >= E) return;
+  int pos = base_e;
+  for (int i = 0; i < n; ++i) {
+    if (s_idx[i] == e) {
+      perm[pos] = p0 + i;
+      inv_perm[p0 + i] = pos;
+      ++pos;
+    }
+  }
+}
+
+// Single CTA: the whole pick list is one chunk.  blockDim.x = max(E, 32) rounded up to a warp.
+__global__ void __launch_bounds__(1024) dispatch_single(int P, int E, const int32_t* __restrict__ idx,
+                                                         int32_t* counts, int32_t* offsets, int32_t* perm,
+                                                         int32_t* inv_perm, int32_t* active, int32_t* n_active,
+                                                         int* status) {
+  __shared__ int s_idx[kChunk];
+  __shared__ int s_cnt[1024];
+  __shared__ int warp_tot[32];
+  __shared__ int total;
+  for (int e = threadIdx.x; e < E; e += blockDim.x) s_cnt[e] = 0;
+  __syncthreads();
+  for (int p = threadIdx.x; p < P; p += blockDim.x) {
+    const int e = load_pick(idx, p, E, status);
+    s_idx[p] = e;
+    if (e >= 0) atomicAdd(&s_cnt[e], 1);
+  }
+  __syncthreads();
+  const int e = threadIdx.x;
+  const int c = e < E ? s_cnt[e] : 0;
+  const int off = block_exclusive_scan(c, warp_tot, &total);
+  const int flag = c > 0 ? 1 : 0;
+  const int apos = block_exclusive_scan(flag, warp_tot, &total);
+  if (e < E) {
+    counts[e] = c;
+    offsets[e] = off;
+    if (flag) active[apos] = e;
+  }
+  if (threadIdx.x == 0) n_active[0] = total;
+  if (e == E - 1) offsets[E] = off + c;
+  place_chunk(s_idx, 0, P, E, off, perm, inv_perm);
+}
+
+// Multi-chunk, step 1: per-chunk counts -> ccount[chunk][E].
+__global__ void __launch_bounds__(1024) dispatch_count(int P, int E, const int32_t* __restrict__ idx, int* ccount,
+                                                        int* status) {
+  __shared__ int s_cnt[1024];
+  for (int e = threadIdx.x; e < E; e += blockDim.x) s_cnt[e] = 0;
+  __syncthreads();
+  const int p0 = blockIdx.x * kChunk;
+  const int n = min(kChunk, P - p0);
+  for (int i = threadIdx.x; i < n; i += blockDim.x) {
+    const int e = load_pick(idx, p0 + i, E, status);
+    if (e >= 0) atomicAdd(&s_cnt[e], 1);
+  }
+  __syncthreads();
+  for (int e = threadIdx.x; e < E; e += blockDim.x) ccount[(size_t)blockIdx.x * E + e] = s_cnt[e];
+}
+
+// Multi-chunk, step 2 (one CTA): totals, offsets, active list; ccount becomes
+// each chunk's base position per expert.
+__global__ void __launch_bounds__(1024) dispatch_scan(int nchunk, int E, int* ccount, int32_t* counts,
+                                                       int32_t* offsets, int32_t* active, int32_t* n_active) {
+  __shared__ int warp_tot[32];
+  __shared__ int total;
+  const int e = threadIdx.x;
+  int run = 0;
+  if (e < E)
+    for (int c = 0; c < nchunk; ++c) {
+      const int v = ccount[(size_t)c * E + e];
+      ccount[(size_t)c * E + e] = run;
+      run += v;
+    }
+  const int off = block_exclusive_scan(run, warp_tot, &total);
+  const int flag = run > 0 ? 1 : 0;
+  const int apos = block_exclusive_scan(flag, warp_tot, &total);
+  if (e < E) {
+    counts[e] = run;
+    offsets[e] = off;
+    if (flag) active[apos] = e;
+    for (int c = 0; c < nchunk; ++c) ccount[(size_t)c * E + e] += off;
+  }
+  if (threadIdx.x == 0) n_active[0] = total;
+  if (e == E - 1) offsets[E] = off + run;
+}
+
+// Multi-chunk, step 3: placement per chunk.
+__global__ void __launch_bounds__(1024) dispatch_place(int P, int E, const int32_t* __restrict__ idx,
+                                                        const int* ccount, int32_t* perm, int32_t* inv_perm) {
+  __shared__ int s_idx[kChunk];
+  const int p0 = blockIdx.x * kChunk;
+  const int n = min(kChunk, P - p0);
+  for (int i = threadIdx.x; i < n; i += blockDim.x) {
+    const int e = idx[p0 + i];
+    s_idx[i] = (e >= 0 && e < E) ? e : -1;
+  }
+  __syncthreads();
+  const int e = threadIdx.x;
+  const int base = e < E ? ccount[(size_t)blockIdx.x * E + e] : 0;
+  place_chunk(s_idx, p0, n, E, base, perm, inv_perm);
+}
+
+}  // namespace
+
+size_t dispatch_ws_bytes(const qre_layer_shape& s, int T) {
+  const long long P = (long long)T * s.top_k;
+  const long long nchunk = (P + kChunk - 1) / kChunk;
+  return nchunk > 1 ? (size_t)nchunk * s.n_experts * sizeof(int) : 0;
+}
+
+cudaError_t launch_dispatch(const qre_layer_shape& s, int T, const int32_t* topk_idx, int32_t* counts,
+                            int32_t* offsets, int32_t* perm, int32_t* inv_perm, int32_t* active,
+                            int32_t* n_active, void* ws, int* status, cudaStream_t stream) {
+  const int P = T * s.top_k, E = s.n_experts;
+  const int threads = ((E + 31) / 32) * 32;
+  if (P <= kChunk) {
+    dispatch_single<<<1, threads, 0, stream>>>(P, E, topk_idx, counts, offsets, perm, inv_perm, active, n_active,
+                                               status);
+    return cudaGetLastError();
+  }
+  const int nchunk = (P + kChunk - 1) / kChunk;
+  int* ccount = static_cast<int*>(ws);
+  dispatch_count<<<nchunk, 1024, 0, stream>>>(P, E, topk_idx, ccount, status);
+  dispatch_scan<<<1, threads, 0, stream>>>(nchunk, E, ccount, counts, offsets, active, n_active);
+  dispatch_place<<<nchunk, threads, 0, stream>>>(P, E, topk_idx, ccount, perm, inv_perm);
+  return cudaGetLastError();
+}
+
+}  // namespace qre

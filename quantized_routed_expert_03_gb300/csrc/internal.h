@@ -1,0 +1,55 @@
+// internal.h -- host-side declarations shared by the library's translation units.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "../../include/qre.h"
+
+namespace qre {
+
+// Largest token count the bandwidth-bound decode FFN handles in one pass: the
+// tokens are the N = 8 side of the m16n8k16 tensor-core tile.
+constexpr int kDecodeMaxTokens = 8;
+
+// Bytes of each workspace region for a call with T tokens (each call uses its
+// own region from offset 0; calls on one stream run one after the other).
+size_t route_ws_bytes(const qre_layer_shape& s, int T);
+size_t dispatch_ws_bytes(const qre_layer_shape& s, int T);
+size_t ffn_ws_bytes(const qre_layer_shape& s, int T);
+
+// Device properties, cached per device.
+int device_sm_count();
+int device_max_smem_optin();
+int* device_status_word();   // address of the current device's status word
+
+// Raises a kernel's dynamic shared-memory limit to at least `bytes` on the
+// current device (cached, so repeated launches and graph captures skip it).
+cudaError_t ensure_smem_limit(const void* kernel, int bytes);
+
+// Kernel launchers (return the launch error, cudaSuccess otherwise).
+// w2 == nullptr: plain matrix of n_rows rows.  Otherwise the gate/up pair:
+// n_rows = 2I output rows interleaved in blocks of 16 from w (gate) and w2 (up).
+cudaError_t launch_quantize(int n_rows, int k_dim, int group, const float* w, const float* w2, uint8_t* packed,
+                            uint16_t* scales, int* status, cudaStream_t stream);
+
+cudaError_t launch_route(const qre_layer_shape& s, int T, const uint16_t* x, const float* w_router,
+                         const float* bias, int32_t* topk_idx, float* topk_w, void* ws,
+                         cudaStream_t stream);
+
+cudaError_t launch_dispatch(const qre_layer_shape& s, int T, const int32_t* topk_idx, int32_t* counts,
+                            int32_t* offsets, int32_t* perm, int32_t* inv_perm, int32_t* active,
+                            int32_t* n_active, void* ws, int* status, cudaStream_t stream);
+
+// Returns cudaErrorInvalidValue when the shape has no decode kernel instance.
+cudaError_t launch_ffn_decode(const qre_layer_shape& s, int T, const uint16_t* x, const qre_slot* slots,
+                              const int32_t* offsets, const int32_t* perm, const int32_t* active,
+                              const int32_t* n_active, float* expert_out, void* ws, int* status,
+                              cudaStream_t stream);
+bool ffn_decode_supported(const qre_layer_shape& s);
+
+cudaError_t launch_combine(const qre_layer_shape& s, int T, const float* expert_out, const float* topk_w,
+                           const int32_t* inv_perm, float* y_f32, uint16_t* y_bf16, cudaStream_t stream);
+
+}  // namespace qre

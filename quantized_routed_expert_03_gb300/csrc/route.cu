@@ -1,0 +1,247 @@
+// route.cu -- router: fp32 logits, sigmoid scores, top-k, renormalised weights.
+//
+// Each token picks top_k of n_experts (8 of 288 in the GLM-5.3-Flash recipes:
+// the RTX 3090 recipe's summary).  The scoring function is not on the pages;
+// this library reads it as sigmoid scores with an optional selection-only bias,
+// ties to the lower expert id, and weights s / sum(s) over the selection.
+//
+// Two logits kernels:
+//   * T <= 16 (decode): a GEMV that streams W_r once; each CTA owns two expert
+//     rows and keeps all T tokens' partial sums in registers.
+//   * T > 16 (prefill): a tiled fp32 GEMM (64 tokens x 64 experts per CTA).
+// Both accumulate in a fixed order, so results are deterministic.  A warp per
+// token then does the selection.
+#include "common.cuh"
+#include "internal.h"
+
+namespace qre {
+namespace {
+
+constexpr int kGemvTMax = 16;
+
+template <int TMAX>
+__global__ void __launch_bounds__(256) route_logits_gemv(int T, int H, int E, const uint16_t* __restrict__ x,
+                                                         const float* __restrict__ W, float* __restrict__ logits) {
+  __shared__ float part[2][4][TMAX];
+  const int row = threadIdx.x >> 7;        // expert row within the CTA
+  const int c = threadIdx.x & 127;         // column slot
+  const int warp_in_row = (threadIdx.x >> 5) & 3, lane = threadIdx.x & 31;
+  const int e = blockIdx.x * 2 + row;
+  float acc[TMAX];
+#pragma unroll
+  for (int t = 0; t < TMAX; ++t) acc[t] = 0.f;
+  if (e < E) {
+    const float* w = W + (size_t)e * H;
+#pragma unroll 4
+    for (int j = c * 4; j < H; j += 512) {
+      const float4 wv = __ldg(reinterpret_cast<const float4*>(w + j));
+#pragma unroll
+      for (int t = 0; t < TMAX; ++t) {
+        if (t < T) {
+          const uint2 xv = __ldg(reinterpret_cast<const uint2*>(x + (size_t)t * H + j));
+          float a = acc[t];
+          a = fmaf(bf16_bits_to_float(xv.x & 0xFFFFu), wv.x, a);
+          a = fmaf(bf16_bits_to_float(xv.x >> 16), wv.y, a);
+          a = fmaf(bf16_bits_to_float(xv.y & 0xFFFFu), wv.z, a);
+          a = fmaf(bf16_bits_to_float(xv.y >> 16), wv.w, a);
+          acc[t] = a;
+        }
+      }
+    }
+  }
+#pragma unroll
+  for (int t = 0; t < TMAX; ++t) {
+    float v = acc[t];
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    if (lane == 0) part[row][warp_in_row][t] = v;
+  }
+  __syncthreads();
+  if (threadIdx.x < 2 * TMAX) {
+    const int r = threadIdx.x / TMAX, t = threadIdx.x % TMAX;
+    const int ee = blockIdx.x * 2 + r;
+    if (ee < E && t < T) {
+      const float v = ((part[r][0][t] + part[r][1][t]) + part[r][2][t]) + part[r][3][t];
+      logits[(size_t)t * E + ee] = v;
+    }
+  }
+}
+
+// logits[T][E] = X[T][H] (bf16) * W[E][H]^T (fp32), fp32 CUDA-core GEMM.
+constexpr int BM = 64, BN = 64, BK = 32;
+__global__ void __launch_bounds__(256) route_logits_gemm(int T, int H, int E, const uint16_t* __restrict__ x,
+                                                         const float* __restrict__ W, float* __restrict__ logits) {
+  __shared__ float xs[BK][BM + 4];
+  __shared__ float ws[BK][BN + 4];
+  const int tm = blockIdx.y * BM, en = blockIdx.x * BN;
+  const int tx = threadIdx.x & 15, ty = threadIdx.x >> 4;   // 16 x 16 threads, 4 x 4 outputs each
+  float acc[4][4] = {};
+  for (int k0 = 0; k0 < H; k0 += BK) {
+    // load 64 x 32 of X and of W; 256 threads, 8 elements each
+    for (int i = threadIdx.x; i < BM * BK / 4; i += 256) {
+      const int r = i / (BK / 4), cc = (i % (BK / 4)) * 4;
+      const int tok = tm + r;
+      if (tok < T) {
+        const uint2 v = __ldg(reinterpret_cast<const uint2*>(x + (size_t)tok * H + k0 + cc));
+        xs[cc + 0][r] = bf16_bits_to_float(v.x & 0xFFFFu);
+        xs[cc + 1][r] = bf16_bits_to_float(v.x >> 16);
+        xs[cc + 2][r] = bf16_bits_to_float(v.y & 0xFFFFu);
+        xs[cc + 3][r] = bf16_bits_to_float(v.y >> 16);
+      } else {
+        xs[cc + 0][r] = xs[cc + 1][r] = xs[cc + 2][r] = xs[cc + 3][r] = 0.f;
+      }
+      const int ex = en + r;
+      if (ex < E) {
+        const float4 v = __ldg(reinterpret_cast<const float4*>(W + (size_t)ex * H + k0 + cc));
+        ws[cc + 0][r] = v.x;
+        ws[cc + 1][r] = v.y;
+        ws[cc + 2][r] = v.z;
+        ws[cc + 3][r] = v.w;
+      } else {
+        ws[cc + 0][r] = ws[cc + 1][r] = ws[cc + 2][r] = ws[cc + 3][r] = 0.f;
+      }
+    }
+    __syncthreads();
+#pragma unroll 8
+    for (int kk = 0; kk < BK; ++kk) {
+      float a[4], b[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) a[i] = xs[kk][ty * 4 + i];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) b[j] = ws[kk][tx * 4 + j];
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+#pragma unroll
+        for (int j = 0; j < 4; ++j) acc[i][j] = fmaf(a[i], b[j], acc[i][j]);
+    }
+    __syncthreads();
+  }
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const int tok = tm + ty * 4 + i;
+    if (tok >= T) continue;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const int ex = en + tx * 4 + j;
+      if (ex < E) logits[(size_t)tok * E + ex] = acc[i][j];
+    }
+  }
+}
+
+struct Cand {
+  float v;
+  int id;
+};
+__device__ __forceinline__ bool better(const Cand& a, const Cand& b) {
+  return a.v > b.v || (a.v == b.v && a.id < b.id);
+}
+
+// One warp per token: sigmoid, selection score, k rounds of warp arg-max (ties
+// to the lower id), ascending-id output, weights s / sum(s) summed in ascending
+// id order.
+constexpr int kSelWarps = 8;
+__global__ void __launch_bounds__(kSelWarps * 32) route_select(int T, int E, int k, const float* __restrict__ logits,
+                                                               const float* __restrict__ bias, int32_t* __restrict__ idx,
+                                                               float* __restrict__ wout) {
+  __shared__ int sid[kSelWarps][16];
+  __shared__ float ssc[kSelWarps][16];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int t = blockIdx.x * kSelWarps + warp;
+  if (t >= T) return;
+  const float* lg = logits + (size_t)t * E;
+  float s[32], sel[32];
+  uint32_t taken = 0;
+#pragma unroll
+  for (int i = 0; i < 32; ++i) {
+    const int e = i * 32 + lane;
+    if (e < E) {
+      const float sc = 1.0f / (1.0f + expf(-lg[e]));
+      s[i] = sc;
+      sel[i] = bias ? sc + bias[e] : sc;
+    } else {
+      s[i] = 0.f;
+      sel[i] = -INFINITY;
+      taken |= 1u << i;
+    }
+  }
+  int my_id = -1;
+  float my_s = 0.f;
+  for (int r = 0; r < k; ++r) {
+    Cand best{-INFINITY, 0x7fffffff};
+    int best_i = -1;
+#pragma unroll
+    for (int i = 0; i < 32; ++i) {
+      if (!(taken >> i & 1u)) {
+        const Cand c{sel[i], i * 32 + lane};
+        if (best_i < 0 || better(c, best)) {
+          best = c;
+          best_i = i;
+        }
+      }
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      Cand other{__shfl_xor_sync(0xffffffffu, best.v, o), __shfl_xor_sync(0xffffffffu, best.id, o)};
+      if (better(other, best)) best = other;
+    }
+    const int owner = best.id & 31, slot = best.id >> 5;
+    float sw = 0.f;
+    if (lane == owner) {
+#pragma unroll
+      for (int i = 0; i < 32; ++i)
+        if (i == slot) {
+          taken |= 1u << i;
+          sw = s[i];
+        }
+    }
+    sw = __shfl_sync(0xffffffffu, sw, owner);
+    if (lane == r) {
+      my_id = best.id;
+      my_s = sw;
+    }
+  }
+  // rank = number of picks with a smaller id
+  int rank = 0;
+  for (int j = 0; j < k; ++j) {
+    const int other = __shfl_sync(0xffffffffu, my_id, j);
+    if (lane < k && other < my_id) ++rank;
+  }
+  if (lane < k) {
+    sid[warp][rank] = my_id;
+    ssc[warp][rank] = my_s;
+  }
+  __syncwarp();
+  if (lane == 0) {
+    float tot = 0.f;
+    for (int j = 0; j < k; ++j) tot += ssc[warp][j];
+    for (int j = 0; j < k; ++j) {
+      idx[(size_t)t * k + j] = sid[warp][j];
+      wout[(size_t)t * k + j] = ssc[warp][j] / tot;
+    }
+  }
+}
+
+}  // namespace
+
+size_t route_ws_bytes(const qre_layer_shape& s, int T) { return (size_t)T * s.n_experts * sizeof(float); }
+
+cudaError_t launch_route(const qre_layer_shape& s, int T, const uint16_t* x, const float* w_router,
+                         const float* bias, int32_t* topk_idx, float* topk_w, void* ws, cudaStream_t stream) {
+  float* logits = static_cast<float*>(ws);
+  const int H = s.hidden, E = s.n_experts;
+  if (T <= 8) {
+    route_logits_gemv<8><<<(E + 1) / 2, 256, 0, stream>>>(T, H, E, x, w_router, logits);
+  } else if (T <= kGemvTMax) {
+    route_logits_gemv<kGemvTMax><<<(E + 1) / 2, 256, 0, stream>>>(T, H, E, x, w_router, logits);
+  } else {
+    dim3 grid((E + BN - 1) / BN, (T + BM - 1) / BM);
+    route_logits_gemm<<<grid, 256, 0, stream>>>(T, H, E, x, w_router, logits);
+  }
+  cudaError_t err = cudaGetLastError();
+  if (err != cudaSuccess) return err;
+  route_select<<<(T + kSelWarps - 1) / kSelWarps, kSelWarps * 32, 0, stream>>>(T, E, s.top_k, logits, bias,
+                                                                              topk_idx, topk_w);
+  return cudaGetLastError();
+}
+
+}  // namespace qre

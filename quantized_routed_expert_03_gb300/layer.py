@@ -1,0 +1,152 @@
+"""Device plumbing for one routed MoE layer: buffers, expert arenas, slot table.
+
+PyTorch only allocates memory and supplies streams here; every computation is a
+call into libqre.so through the binding in ``__init__``.
+
+* :class:`ExpertArena` keeps the packed experts of a layer in one allocation,
+  either device memory (HBM cache slots) or pinned host memory that the GPU
+  reads zero-copy (the glm53-flash-offload README, "Zero-copy home": one
+  exact-size pinned arena per layer).
+* :class:`MoELayer` owns the per-call buffers and the device slot table, and
+  runs route -> dispatch -> expert FFN -> combine on one stream.
+"""
+
+from __future__ import annotations
+
+import ctypes
+
+import torch
+
+from . import (make_shape, qre_combine, qre_dispatch, qre_expert_ffn, qre_quantize, qre_quantize_gate_up,
+               qre_route, qre_slot, qre_validate_slots, qre_workspace_size, slot_array)
+
+_ALIGN = 256
+
+
+def _a(n: int) -> int:
+    return (n + _ALIGN - 1) // _ALIGN * _ALIGN
+
+
+def expert_layout(H: int, I: int, G: int) -> dict:
+    """Byte offsets of the four arrays of one packed expert, and its stride."""
+    wgu, sgu = 2 * I * H // 2, 2 * I * (H // G) * 2
+    wd, sd = H * I // 2, H * (I // G) * 2
+    o_sgu = _a(wgu)
+    o_wd = o_sgu + _a(sgu)
+    o_sd = o_wd + _a(wd)
+    return {"w_gate_up": (0, wgu), "s_gate_up": (o_sgu, sgu), "w_down": (o_wd, wd), "s_down": (o_sd, sd),
+            "stride": o_sd + _a(sd), "payload": wgu + sgu + wd + sd}
+
+
+class ExpertArena:
+    """``n`` packed experts in one contiguous allocation (device, or pinned host)."""
+
+    def __init__(self, H: int, I: int, G: int, n: int, device="cuda", host: bool = False):
+        self.H, self.I, self.G, self.n, self.host = H, I, G, n, host
+        self.layout = expert_layout(H, I, G)
+        nbytes = self.layout["stride"] * n
+        if host:
+            self.buf = torch.empty(nbytes, dtype=torch.uint8, pin_memory=True)
+        else:
+            self.buf = torch.empty(nbytes, dtype=torch.uint8, device=device)
+
+    def view(self, e: int, name: str) -> torch.Tensor:
+        off, size = self.layout[name]
+        base = e * self.layout["stride"] + off
+        return self.buf[base:base + size]
+
+    def addresses(self, e: int) -> tuple:
+        return tuple(self.view(e, n).data_ptr() for n in ("w_gate_up", "s_gate_up", "w_down", "s_down"))
+
+    def quantize_into(self, e: int, w_gate, w_up, w_down, stream=None, staging=None) -> None:
+        """Quantizes fp32 device weights (gate/up [I,H], down [H,I]) into slot e.
+
+        For a host arena the kernels write a device staging buffer (``staging``,
+        at least one expert stride) that is then copied into pinned memory.
+        """
+        H, I, G = self.H, self.I, self.G
+        if self.host:
+            if staging is None:
+                staging = torch.empty(self.layout["stride"], dtype=torch.uint8, device=w_gate.device)
+            dst = {n: staging[off:off + size] for n, (off, size) in self.layout.items()
+                   if n in ("w_gate_up", "s_gate_up", "w_down", "s_down")}
+        else:
+            dst = {n: self.view(e, n) for n in ("w_gate_up", "s_gate_up", "w_down", "s_down")}
+        qre_quantize_gate_up(I, H, G, w_gate, w_up, dst["w_gate_up"], dst["s_gate_up"], stream)
+        qre_quantize(H, I, G, w_down, dst["w_down"], dst["s_down"], stream)
+        if self.host:
+            for n, t in dst.items():
+                self.view(e, n).copy_(t, non_blocking=False)
+
+    def to_numpy(self, e: int) -> dict:
+        """The packed arrays of slot e on the host (for checks)."""
+        H, I, G = self.H, self.I, self.G
+        import numpy as np
+        out = {}
+        shapes = {"w_gate_up": ((2 * I, H // 2), np.uint8), "s_gate_up": ((2 * I, H // G), np.float16),
+                  "w_down": ((H, I // 2), np.uint8), "s_down": ((H, I // G), np.float16)}
+        for n, (shape, dt) in shapes.items():
+            raw = self.view(e, n).cpu().numpy()
+            out[n] = raw.view(dt).reshape(shape)
+        return out
+
+
+class MoELayer:
+    """Buffers and slot table for calls with up to ``t_max`` tokens."""
+
+    def __init__(self, H: int, I: int, E: int, k: int, G: int, t_max: int, device="cuda"):
+        self.H, self.I, self.E, self.k, self.G, self.t_max = H, I, E, k, G, t_max
+        self.shape = make_shape(H, I, E, k, G)
+        self.device = torch.device(device)
+        dev = self.device
+        P = t_max * k
+        i32 = dict(dtype=torch.int32, device=dev)
+        self.topk_idx = torch.empty((t_max, k), **i32)
+        self.topk_w = torch.empty((t_max, k), dtype=torch.float32, device=dev)
+        self.counts = torch.empty(E, **i32)
+        self.offsets = torch.empty(E + 1, **i32)
+        self.perm = torch.empty(P, **i32)
+        self.inv_perm = torch.empty(P, **i32)
+        self.active = torch.empty(E, **i32)
+        self.n_active = torch.zeros(4, **i32)
+        self.expert_out = torch.empty((P + t_max, H), dtype=torch.float32, device=dev)
+        self.y = torch.empty((t_max, H), dtype=torch.float32, device=dev)
+        self.y_bf16 = torch.empty((t_max, H), dtype=torch.bfloat16, device=dev)
+        self.ws_bytes = qre_workspace_size(self.shape, t_max)
+        self.workspace = torch.empty(max(self.ws_bytes, 256), dtype=torch.uint8, device=dev)
+        self.slots = torch.zeros((E + 1) * ctypes.sizeof(qre_slot), dtype=torch.uint8, device=dev)
+        self.host_slots = None
+
+    def set_slots(self, entries, validate: bool = True) -> None:
+        """entries: E + 1 tuples (w_gate_up, s_gate_up, w_down, s_down, tier); entry E is the shared expert."""
+        assert len(entries) == self.E + 1
+        arr = slot_array(entries)
+        if validate:
+            qre_validate_slots(self.shape, arr)
+        raw = bytes(memoryview(arr).cast("B"))
+        self.slots.copy_(torch.frombuffer(bytearray(raw), dtype=torch.uint8))
+        self.host_slots = arr
+
+    def route(self, x, w_router, bias, T, stream=None):
+        qre_route(self.shape, T, x, w_router, bias, self.topk_idx, self.topk_w, self.workspace, self.ws_bytes, stream)
+
+    def dispatch(self, T, stream=None):
+        qre_dispatch(self.shape, T, self.topk_idx, self.counts, self.offsets, self.perm, self.inv_perm, self.active,
+                     self.n_active, self.workspace, self.ws_bytes, stream)
+
+    def expert_ffn(self, x, T, stream=None):
+        qre_expert_ffn(self.shape, T, x, self.slots, self.offsets, self.perm, self.active, self.n_active,
+                       self.expert_out, self.workspace, self.ws_bytes, stream)
+
+    def combine(self, T, stream=None, bf16: bool = True):
+        qre_combine(self.shape, T, self.expert_out, self.topk_w, self.inv_perm, self.y,
+                    self.y_bf16 if bf16 else None, stream)
+
+    def forward(self, x, w_router, bias, T=None, stream=None):
+        """Runs the whole layer on ``x`` ([T, H] bf16, device); results stay in the buffers."""
+        T = x.shape[0] if T is None else T
+        self.route(x, w_router, bias, T, stream)
+        self.dispatch(T, stream)
+        self.expert_ffn(x, T, stream)
+        self.combine(T, stream)
+        return self.y[:T]

@@ -1,0 +1,225 @@
+"""GPU expert FFN, combine and the whole layer vs the oracle, plus invariances.
+
+Tolerances (derived from the arithmetic; the layer-level bar of the pages is
+1e-3 relative RMS, the error class of their own expert kernels):
+  * decode path (T <= 8): products of exact 4-bit codes and fp16 activations are
+    exact, accumulation is fp32, h enters the down projection as an fp16 pair
+    (high + remainder, ~2^-22 relative).  Expected error is a few 1e-7; the test
+    bound is 1e-5 relative RMS per output row and per layer output.
+  * the bf16 output must equal round-to-nearest-even of the fp32 output exactly.
+"""
+
+import numpy as np
+import pytest
+import torch
+
+import synthetic
+import quantized_routed_expert_03_gb300 as qre
+from oracle import moe as omoe
+
+from gpu_support import (BuiltLayer, bf16_tensor_to_bits, bits_to_bf16_tensor, check_routing, numpy_source,
+                         rel_rms, torch_sources)
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda:0"
+DECODE_TOL = 1e-5
+LAYER_BAR = 1e-3
+
+MID = synthetic.LayerConfig("mid", 512, 256, 32, 4, 128, 8)
+ODD = synthetic.LayerConfig("odd", 640, 384, 24, 3, 64, 8)
+
+
+def _inputs(cfg, T, layer=0, step=0, bias=None):
+    x_bits = synthetic.activations_bits(T, cfg.hidden, cfg.seed, layer, step)
+    wr = synthetic.router_weights(cfg.n_experts, cfg.hidden, cfg.seed, layer)
+    return x_bits, wr, bias
+
+
+def _run(built, x_bits, wr, bias):
+    L = built.layer
+    T = x_bits.shape[0]
+    x = bits_to_bf16_tensor(x_bits, DEV)
+    b = None if bias is None else torch.from_numpy(np.asarray(bias, np.float32)).to(DEV)
+    L.forward(x, torch.from_numpy(wr).to(DEV), b, T)
+    torch.cuda.synchronize()
+    P = T * built.k
+    return {
+        "idx": L.topk_idx[:T].cpu().numpy(), "w": L.topk_w[:T].cpu().numpy(),
+        "counts": L.counts.cpu().numpy(), "offsets": L.offsets.cpu().numpy(),
+        "perm": L.perm[:P].cpu().numpy(), "inv_perm": L.inv_perm[:P].cpu().numpy(),
+        "n_active": int(L.n_active[0].item()), "active": L.active.cpu().numpy(),
+        "expert_out": L.expert_out[:P + T].cpu().numpy(), "y": L.y[:T].cpu().numpy(),
+        "y_bf16": bf16_tensor_to_bits(L.y_bf16[:T]),
+    }
+
+
+def _check_layer(built, got, ref, tol=DECODE_TOL, check_bytes=True, tokens=None):
+    """Routing and dispatch over all tokens; FFN outputs and y for ``tokens`` (default all)."""
+    T = got["y"].shape[0]
+    k = built.k
+    near = check_routing(got["idx"], got["w"], ref)
+    assert near == 0, "near-tie token in a fixed test case"
+    for name in ("counts", "offsets", "perm", "inv_perm"):
+        np.testing.assert_array_equal(got[name], ref[name], err_msg=name)
+    assert got["n_active"] == ref["n_active"]
+    np.testing.assert_array_equal(got["active"][:ref["n_active"]], ref["active"])
+    toks = np.arange(T) if tokens is None else np.asarray(sorted(tokens))
+    used = sorted(set(int(e) for e in got["idx"][toks].reshape(-1)) | {built.E})
+    if check_bytes:
+        for e in used:
+            mine, theirs = built.packed_numpy(e), built.oracle_experts[e]
+            for n in ("w_gate_up", "w_down"):
+                np.testing.assert_array_equal(mine[n], theirs[n], err_msg=f"expert {e} {n}")
+            for n in ("s_gate_up", "s_down"):
+                np.testing.assert_array_equal(mine[n].view(np.uint16), theirs[n].view(np.uint16))
+    rows = np.concatenate([got["inv_perm"][t * k:(t + 1) * k] for t in toks] + [T * k + toks])
+    eo, reo = got["expert_out"][rows], ref["expert_out"][rows]
+    row_err = np.linalg.norm(eo - reo, axis=1) / np.maximum(np.linalg.norm(reo, axis=1), 1e-30)
+    assert row_err.max() <= tol, f"worst expert_out row {row_err.max():.3e}"
+    err = rel_rms(got["y"][toks], ref["y"][toks])
+    assert err <= tol and err <= LAYER_BAR, f"layer rel RMS {err:.3e}"
+    np.testing.assert_array_equal(got["y_bf16"], omoe.f32_to_bf16_bits(got["y"]))
+    return err
+
+
+@pytest.mark.parametrize("T", [1, 2, 3, 4, 5, 8])
+def test_tiny_layer_matches_oracle(T):
+    cfg = synthetic.CONFIGS["tiny"]
+    built = BuiltLayer(cfg.hidden, cfg.inter, cfg.n_experts, cfg.top_k, cfg.group, 8, DEV, numpy_source(cfg))
+    x_bits, wr, _ = _inputs(cfg, T)
+    got = _run(built, x_bits, wr, None)
+    ref = built.oracle_layer(x_bits, wr, None)
+    _check_layer(built, got, ref)
+
+
+@pytest.mark.parametrize("cfg", [MID, ODD], ids=["mid_G128", "odd_G64"])
+@pytest.mark.parametrize("T", [1, 7, 8])
+def test_mid_layers_match_oracle(cfg, T):
+    built = BuiltLayer(cfg.hidden, cfg.inter, cfg.n_experts, cfg.top_k, cfg.group, 8, DEV, numpy_source(cfg))
+    x_bits, wr, _ = _inputs(cfg, T, step=T)
+    got = _run(built, x_bits, wr, None)
+    ref = built.oracle_layer(x_bits, wr, None)
+    _check_layer(built, got, ref)
+
+
+def test_host_resident_experts_match_and_are_bit_identical_to_hbm():
+    """Slot placement invariance: experts read zero-copy from pinned host memory
+    give the same bits as the same experts in device memory."""
+    cfg = MID
+    src = numpy_source(cfg)
+    a = BuiltLayer(cfg.hidden, cfg.inter, cfg.n_experts, cfg.top_k, cfg.group, 8, DEV, src)
+    rng = np.random.default_rng(5)
+    host = rng.random(cfg.n_experts + 1) < 0.5
+    order = rng.permutation(cfg.n_experts + 1)
+    b = BuiltLayer(cfg.hidden, cfg.inter, cfg.n_experts, cfg.top_k, cfg.group, 8, DEV, src, host_mask=host,
+                   arena_order=order)
+    x_bits, wr, _ = _inputs(cfg, 8, step=99)
+    ga = _run(a, x_bits, wr, None)
+    gb = _run(b, x_bits, wr, None)
+    np.testing.assert_array_equal(ga["y"], gb["y"])
+    np.testing.assert_array_equal(ga["expert_out"], gb["expert_out"])
+    _check_layer(b, gb, b.oracle_layer(x_bits, wr, None))
+
+
+def test_token_order_invariance_bit_exact():
+    cfg = MID
+    built = BuiltLayer(cfg.hidden, cfg.inter, cfg.n_experts, cfg.top_k, cfg.group, 8, DEV, numpy_source(cfg))
+    x_bits, wr, _ = _inputs(cfg, 8, step=5)
+    g1 = _run(built, x_bits, wr, None)
+    order = np.array([5, 2, 7, 0, 3, 6, 1, 4])
+    g2 = _run(built, x_bits[order], wr, None)
+    np.testing.assert_array_equal(g2["idx"], g1["idx"][order])
+    np.testing.assert_array_equal(g2["w"], g1["w"][order])
+    np.testing.assert_array_equal(g2["y"], g1["y"][order])
+
+
+def test_zero_weight_expert_contributes_nothing():
+    cfg = synthetic.CONFIGS["tiny"]
+    built = BuiltLayer(cfg.hidden, cfg.inter, cfg.n_experts, cfg.top_k, cfg.group, 8, DEV, numpy_source(cfg))
+    x_bits, wr, _ = _inputs(cfg, 4)
+    base = _run(built, x_bits, wr, None)
+    e0 = int(base["idx"][0, 0])
+    # point e0's down scales at a zero buffer: its outputs must vanish exactly
+    entries = [tuple(built.layer.host_slots[e].__getattribute__(f) for f in
+                     ("w_gate_up", "s_gate_up", "w_down", "s_down", "tier")) for e in range(cfg.n_experts + 1)]
+    zeros = torch.zeros(cfg.hidden * (cfg.inter // cfg.group) * 2 + 256, dtype=torch.uint8, device=DEV)
+    wg, sg, wd, sd, tier = entries[e0]
+    entries[e0] = (wg, sg, wd, zeros.data_ptr(), tier)
+    built.layer.set_slots(entries)
+    got = _run(built, x_bits, wr, None)
+    rows = base["inv_perm"][np.nonzero(base["idx"].reshape(-1) == e0)[0]]
+    assert np.all(got["expert_out"][rows] == 0)
+    others = np.setdiff1d(np.arange(base["expert_out"].shape[0]), rows)
+    np.testing.assert_array_equal(got["expert_out"][others], base["expert_out"][others])
+
+
+def test_null_slot_pointer_is_reported_not_faulted():
+    cfg = synthetic.CONFIGS["tiny"]
+    built = BuiltLayer(cfg.hidden, cfg.inter, cfg.n_experts, cfg.top_k, cfg.group, 8, DEV, numpy_source(cfg))
+    x_bits, wr, _ = _inputs(cfg, 4)
+    base = _run(built, x_bits, wr, None)
+    e0 = int(base["idx"][0, 0])
+    entries = [tuple(getattr(built.layer.host_slots[e], f) for f in
+                     ("w_gate_up", "s_gate_up", "w_down", "s_down", "tier")) for e in range(cfg.n_experts + 1)]
+    entries[e0] = (None,) + entries[e0][1:]
+    with pytest.raises(qre.QreError):
+        built.layer.set_slots(entries)                       # the host-side check refuses it
+    built.layer.set_slots(entries, validate=False)          # the device-side check skips it
+    qre.qre_clear_device_status()
+    _run(built, x_bits, wr, None)
+    st = qre.qre_read_device_status()
+    qre.qre_clear_device_status()
+    assert st & qre.QRE_DEV_NULL_SLOT
+
+
+@pytest.mark.slow
+def test_full_size_decode_one_token():
+    """One full-size decode layer: H 4096, I 2048, 288 experts top-8 + shared, T = 1."""
+    cfg = synthetic.CONFIGS["decode1"]
+    host_src, dev_src = torch_sources(cfg, 0, DEV)
+    built = BuiltLayer(cfg.hidden, cfg.inter, cfg.n_experts, cfg.top_k, cfg.group, 8, DEV, host_src,
+                       device_source=dev_src)
+    x_bits, wr, _ = _inputs(cfg, 1, step=1)
+    got = _run(built, x_bits, wr, None)
+    _check_layer(built, got, built.oracle_layer(x_bits, wr, None))
+
+
+@pytest.mark.slow
+def test_full_size_decode_eight_tokens_zipf():
+    """One layer of the 42-layer skewed-routing stack: T = 8, Zipf(1.1) bias.
+
+    Routing and dispatch are checked for all 8 tokens; the FFN outputs for two
+    tokens (the oracle dequantizes every expert it touches, ~3 s each)."""
+    cfg = synthetic.CONFIGS["decode8_zipf_x42"]
+    layer = 17
+    host_src, dev_src = torch_sources(cfg, layer, DEV)
+    built = BuiltLayer(cfg.hidden, cfg.inter, cfg.n_experts, cfg.top_k, cfg.group, 8, DEV, host_src,
+                       device_source=dev_src)
+    bias = synthetic.zipf_bias(cfg.n_experts, cfg.seed, layer)
+    x_bits, wr, _ = _inputs(cfg, 8, layer=layer)
+    got = _run(built, x_bits, wr, bias)
+    toks = [0, 5]
+    _check_layer(built, got, built.oracle_layer(x_bits, wr, bias, tokens=toks), tokens=toks)
+
+
+@pytest.mark.slow
+def test_full_size_expert_cache_host_tier():
+    """Expert-cache placement: popularity ranks > 188 read zero-copy from pinned host memory.
+
+    The FFN outputs are checked for the tokens that picked a host-resident expert
+    (at most two), plus routing and dispatch for all four."""
+    cfg = synthetic.CONFIGS["cache4_x42"]
+    layer = 3
+    host_src, dev_src = torch_sources(cfg, layer, DEV)
+    host = np.append(synthetic.host_resident(cfg, layer), False)
+    built = BuiltLayer(cfg.hidden, cfg.inter, cfg.n_experts, cfg.top_k, cfg.group, 8, DEV, host_src,
+                       host_mask=host, device_source=dev_src)
+    bias = synthetic.zipf_bias(cfg.n_experts, cfg.seed, layer)
+    for step in range(8):
+        x_bits, wr, _ = _inputs(cfg, 4, layer=layer, step=step)
+        got = _run(built, x_bits, wr, bias)
+        toks = [t for t in range(4) if host[got["idx"][t]].any()][:2]
+        if toks:
+            break
+    assert toks, "no token picked a host-resident expert in 8 steps"
+    _check_layer(built, got, built.oracle_layer(x_bits, wr, bias, tokens=toks), tokens=toks)

@@ -1,0 +1,121 @@
+"""GPU router and dispatch vs the oracle: indices and permutations bit-exact."""
+
+import numpy as np
+import pytest
+import torch
+
+import synthetic
+import quantized_routed_expert_03_gb300 as qre
+from oracle import moe as omoe
+
+from gpu_support import bits_to_bf16_tensor, check_routing
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda:0"
+
+
+def _route(H, E, k, T, seed, bias=None, layer=0):
+    x_bits = synthetic.activations_bits(T, H, seed=seed, layer=layer)
+    wr = synthetic.router_weights(E, H, seed=seed, layer=layer)
+    shape = qre.make_shape(H, 128, E, k, 32)
+    ws = torch.empty(max(qre.qre_workspace_size(shape, T), 256), dtype=torch.uint8, device=DEV)
+    idx = torch.empty((T, k), dtype=torch.int32, device=DEV)
+    w = torch.empty((T, k), dtype=torch.float32, device=DEV)
+    b = None if bias is None else torch.from_numpy(bias).to(DEV)
+    qre.qre_route(shape, T, bits_to_bf16_tensor(x_bits, DEV), torch.from_numpy(wr).to(DEV), b, idx, w, ws)
+    torch.cuda.synchronize()
+    ref = omoe.route(omoe.bf16_bits_to_f64(x_bits), wr, bias, k)
+    return idx.cpu().numpy(), w.cpu().numpy(), ref
+
+
+@pytest.mark.parametrize("H,E,k,T", [(256, 16, 4, 4), (4096, 288, 8, 1), (4096, 288, 8, 8), (512, 64, 6, 13),
+                                     (1024, 288, 8, 16), (4096, 288, 8, 300), (768, 1024, 16, 40)])
+def test_route_matches_oracle(H, E, k, T):
+    idx, w, ref = _route(H, E, k, T, seed=3)
+    near = check_routing(idx, w, ref)
+    assert near <= max(1, T // 500)
+    np.testing.assert_allclose(w.sum(1), 1.0, rtol=0, atol=1e-6)
+
+
+def test_route_zipf_bias_matches_oracle():
+    H, E, k, T = 4096, 288, 8, 64
+    bias = synthetic.zipf_bias(E, seed=0, layer=2)
+    idx, w, ref = _route(H, E, k, T, seed=0, bias=bias, layer=2)
+    check_routing(idx, w, ref)
+
+
+@pytest.mark.slow
+def test_route_prefill_8192_matches_oracle():
+    idx, w, ref = _route(4096, 288, 8, 8192, seed=0)
+    near = check_routing(idx, w, ref)
+    assert near < 40
+
+
+def test_route_exact_ties_go_to_lower_id():
+    H, E, k, T = 256, 16, 4, 3
+    x_bits = synthetic.activations_bits(T, H, seed=1)
+    wr = np.tile(np.linspace(-0.1, 0.1, H, dtype=np.float32), (E, 1))
+    shape = qre.make_shape(H, 128, E, k, 32)
+    ws = torch.empty(max(qre.qre_workspace_size(shape, T), 256), dtype=torch.uint8, device=DEV)
+    idx = torch.empty((T, k), dtype=torch.int32, device=DEV)
+    w = torch.empty((T, k), dtype=torch.float32, device=DEV)
+    qre.qre_route(shape, T, bits_to_bf16_tensor(x_bits, DEV), torch.from_numpy(wr).to(DEV), None, idx, w, ws)
+    torch.cuda.synchronize()
+    np.testing.assert_array_equal(idx.cpu().numpy(), np.tile(np.arange(k), (T, 1)))
+    np.testing.assert_allclose(w.cpu().numpy(), 0.25, rtol=0, atol=1e-7)
+
+
+def _dispatch(idx_np, E, k):
+    T = idx_np.shape[0]
+    shape = qre.make_shape(256, 128, E, k, 32)
+    P = T * k
+    i32 = dict(dtype=torch.int32, device=DEV)
+    out = {n: torch.full((m,), -7, **i32) for n, m in
+           (("counts", E), ("offsets", E + 1), ("perm", P), ("inv_perm", P), ("active", E), ("n_active", 4))}
+    ws = torch.empty(max(qre.qre_workspace_size(shape, T), 256), dtype=torch.uint8, device=DEV)
+    qre.qre_dispatch(shape, T, torch.from_numpy(idx_np.astype(np.int32)).to(DEV), out["counts"], out["offsets"],
+                     out["perm"], out["inv_perm"], out["active"], out["n_active"], ws)
+    torch.cuda.synchronize()
+    return {n: t.cpu().numpy() for n, t in out.items()}
+
+
+@pytest.mark.parametrize("T,E,k", [(1, 288, 8), (4, 16, 4), (8, 288, 8), (128, 288, 8), (129, 288, 8),
+                                   (1000, 64, 2), (8192, 288, 8), (4096, 1024, 16), (3, 5, 5)])
+def test_dispatch_matches_oracle(T, E, k):
+    rng = np.random.default_rng(T * 31 + E)
+    idx = np.sort(np.stack([rng.choice(E, size=k, replace=False) for _ in range(T)]), axis=1)
+    got = _dispatch(idx, E, k)
+    ref = omoe.dispatch(idx, E)
+    n = ref["n_active"]
+    for name in ("counts", "offsets", "perm", "inv_perm"):
+        np.testing.assert_array_equal(got[name], ref[name], err_msg=name)
+    assert got["n_active"][0] == n
+    np.testing.assert_array_equal(got["active"][:n], ref["active"])
+
+
+def test_dispatch_skewed_all_tokens_one_expert_set():
+    T, E, k = 2000, 288, 8
+    idx = np.tile(np.arange(100, 108), (T, 1))
+    got = _dispatch(idx, E, k)
+    ref = omoe.dispatch(idx, E)
+    for name in ("counts", "offsets", "perm", "inv_perm"):
+        np.testing.assert_array_equal(got[name], ref[name], err_msg=name)
+    assert got["n_active"][0] == 8
+
+
+def test_dispatch_bad_index_sets_status_without_fault():
+    qre.qre_clear_device_status()
+    idx = np.array([[0, 3], [1, 99]], dtype=np.int32)   # 99 >= E
+    got = _dispatch(idx, 16, 2)
+    st = qre.qre_read_device_status()
+    qre.qre_clear_device_status()
+    assert st & qre.QRE_DEV_BAD_INDEX
+    assert got["counts"].sum() == 3
+
+
+def test_empty_call_is_a_no_op():
+    shape = qre.make_shape(256, 128, 16, 4, 32)
+    qre.qre_route(shape, 0, None, None, None, None, None, None, 0)
+    qre.qre_dispatch(shape, 0, None, None, None, None, None, None, None, None, 0)
+    qre.qre_expert_ffn(shape, 0, None, None, None, None, None, None, None, None, 0)
+    qre.qre_combine(shape, 0, None, None, None, None, None)

@@ -119,7 +119,12 @@ class Workload:
         self.T = T
         self.layers_per_step = cfg.layers
         if n_sets is None:
-            n_sets = cfg.layers if cfg.layers > 1 else (8 if H >= 4096 else 2)
+            if cfg.layers > 1:
+                n_sets = cfg.layers
+            elif T > 8:
+                n_sets = 1          # a prefill step streams far more than L2 on its own
+            else:
+                n_sets = 8 if H >= 4096 else 2
         self.n_sets = n_sets
         t0 = time.time()
         self.sets = []
@@ -176,15 +181,16 @@ def run_ours(args, rank, local_rank, world):
     qre.load_library()
 
     log = (lambda *a: print(*a, file=sys.stderr, flush=True)) if rank == 0 else (lambda *a: None)
-    wl = Workload(args.workload, device, log=log)
+    wl = Workload(args.workload, device, n_sets=args.sets, log=log)
     cfg, T, H, k = wl.cfg, wl.T, wl.cfg.hidden, wl.cfg.top_k
     stream = torch.cuda.Stream(device)
 
     # one captured unit = `per_graph` steps; each step covers one layer set
     # (single-layer workloads) or all layer sets (42-layer stacks)
     stack = wl.layers_per_step > 1
-    per_graph = 1 if stack else wl.n_sets * 4
-    n_x = 4 if stack else per_graph // wl.n_sets
+    prefill = T > 8
+    per_graph = 1 if (stack or prefill) else wl.n_sets * 4
+    n_x = 4 if stack else (2 if prefill else per_graph // wl.n_sets)
     xs = wl.x_pool(n_x, device)
     K, W = args.steps, args.warmup
 
@@ -275,6 +281,8 @@ def run_ours(args, rank, local_rank, world):
 
     # FFN stage: events from the last replay of the instrumented graph
     ffn_ms, ffn_bytes, n_act = [], [], []
+    I = cfg.inter
+    ffn_flops = 2.0 * 3 * H * I * (T * k + T)        # gate, up, down for every pick and the shared expert
     if ffn_events and n_full > 0:
         nact = nact_log.cpu().numpy()
         for (e0, e1), i in zip(ffn_events, ffn_slots):
@@ -287,25 +295,32 @@ def run_ours(args, rank, local_rank, world):
     value = world * tokens_per_step * K / (ms / 1e3)
     peaks, peak_src = load_peaks()
     roofline = None
-    if ffn_ms:
+    if ffn_ms and not prefill:
         achieved = float(np.mean(ffn_bytes)) / (float(np.mean(ffn_ms)) / 1e3) / 1e9
-        sustained = stack
         peak = float(peaks["hbm_gbs"])
         roofline = {"bound": "hbm", "kernel": "qre_expert_ffn (gate/up + down dequant-GEMV kernels)",
                     "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                     "frac": round(achieved / peak, 4), "traffic": args.traffic,
-                    "peak_source": f"{peak_src} (MEASURED_PEAKS.json hbm_gbs)" if peak_src == "measured" else
-                    "fallback 6.8 TB/s",
+                    "peak_source": "of measured (MEASURED_PEAKS.json hbm_gbs)" if peak_src == "measured" else
+                    "of fallback 6.8 TB/s",
                     "ffn_us_mean": round(float(np.mean(ffn_ms)) * 1e3, 2),
                     "ffn_bytes_mean": int(np.mean(ffn_bytes)),
                     "unique_experts_mean": round(float(np.mean(n_act)) + 1, 2),
-                    "timed_region": "last replay of the captured steps"}
-    step_bytes = None
-    if ffn_bytes:
+                    "timed_region": "per-launch CUDA events captured in the replayed graph (last replay)"}
         per_layer = float(np.mean(ffn_bytes)) + cfg.n_experts * H * 4
-        step_bytes = per_layer * wl.layers_per_step
-        roofline["step_hbm_gbs"] = round(step_bytes / (ms / K / 1e3) / 1e9, 1)
-        host_bytes = 0.0
+        roofline["step_hbm_gbs"] = round(per_layer * wl.layers_per_step / (ms / K / 1e3) / 1e9, 1)
+    elif ffn_ms:
+        achieved = ffn_flops / (float(np.mean(ffn_ms)) / 1e3) / 1e12
+        peak = float(peaks.get("bf16_tflops_sustained", peaks["bf16_tflops"]))
+        roofline = {"bound": "tensor", "kernel": "qre_expert_ffn (gather + two tcgen05 grouped GEMMs)",
+                    "achieved": round(achieved, 1), "peak": peak, "unit": "TFLOP/s",
+                    "frac": round(achieved / peak, 4), "traffic": args.traffic,
+                    "peak_source": ("of measured (MEASURED_PEAKS.json bf16_tflops_sustained; fp16 has the "
+                                    "same nominal dense rate)") if peak_src == "measured" else
+                                   "of fallback 1.7 PFLOP/s sustained",
+                    "ffn_ms_mean": round(float(np.mean(ffn_ms)), 4), "ffn_tflop": round(ffn_flops / 1e12, 4),
+                    "unique_experts_mean": round(float(np.mean(n_act)) + 1, 2),
+                    "timed_region": "per-launch CUDA events captured in the replayed graph (last replay)"}
 
     # ---------------- end to end: pinned host input -> graph -> pinned host output, synced per step
     e2e = None
@@ -326,7 +341,7 @@ def run_ours(args, rank, local_rank, world):
                    "launch": "CUDA graph of captured steps"},
         "gpu_launches": None, "roofline": roofline, "clocks": clocks, "e2e": e2e,
     }
-    launches_per_layer = 2 + (1 if T * k <= 1024 else 3) + 2 + 1
+    launches_per_layer = 2 + (1 if T * k <= 1024 else 3) + (3 if prefill else 2) + 1
     out["gpu_launches"] = launches_per_layer * wl.layers_per_step * K
     if rank == 0 and not args.no_cpu_baseline:
         out["cpu_baseline"] = cpu_baseline(args, wl, device)
@@ -520,6 +535,8 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="decode1", choices=sorted(synthetic.CONFIGS))
     ap.add_argument("--e2e-steps", type=int, default=5000)
+    ap.add_argument("--sets", type=int, default=None,
+                    help="distinct layer weight sets to rotate over (default: enough to exceed L2)")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-clocks", action="store_true")

@@ -76,6 +76,7 @@ typedef enum {
 #define QRE_DEV_NULL_SLOT     0x2   /* an active expert's slot has a null pointer    */
 #define QRE_DEV_BAD_SCALE     0x4   /* quantize: a group scale was not finite        */
 #define QRE_DEV_BAD_INDEX     0x8   /* an expert id outside [0, n_experts)           */
+#define QRE_DEV_FP16_RANGE    0x10  /* prefill: an activation or h exceeded fp16     */
 
 /* Layer shape.  H = hidden, I = expert intermediate, E = routed experts,
  * k = experts per token, G = quantization group along the reduction axis. */

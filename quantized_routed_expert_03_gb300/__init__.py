@@ -32,6 +32,7 @@ QRE_DEV_TIMEOUT = 0x1
 QRE_DEV_NULL_SLOT = 0x2
 QRE_DEV_BAD_SCALE = 0x4
 QRE_DEV_BAD_INDEX = 0x8
+QRE_DEV_FP16_RANGE = 0x10
 
 # Every symbol include/qre.h declares.
 EXPORTS = (

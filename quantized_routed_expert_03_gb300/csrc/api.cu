@@ -156,7 +156,7 @@ qre_status qre_workspace_size(const qre_layer_shape* shape, int32_t T, size_t* b
   if (!bytes) return fail(QRE_ERR_INVALID_ARG, "bytes is NULL");
   size_t b = qre::route_ws_bytes(*shape, T);
   const size_t d = qre::dispatch_ws_bytes(*shape, T);
-  const size_t f = T <= qre::kDecodeMaxTokens ? qre::ffn_ws_bytes(*shape, T) : 0;
+  const size_t f = T <= qre::kDecodeMaxTokens ? qre::ffn_ws_bytes(*shape, T) : qre::ffn_prefill_ws_bytes(*shape, T);
   if (d > b) b = d;
   if (f > b) b = f;
   *bytes = align256(b);
@@ -246,16 +246,24 @@ qre_status qre_expert_ffn(const qre_layer_shape* shape, int32_t T, const uint16_
   QRE_REQUIRE_PTR(active);
   QRE_REQUIRE_PTR(n_active);
   QRE_REQUIRE_PTR(expert_out);
-  if (T > qre::kDecodeMaxTokens)
-    return fail(QRE_ERR_UNSUPPORTED, "T = %d: the grouped-GEMM path for T > %d is not built yet", T,
-                qre::kDecodeMaxTokens);
+  cudaStream_t st_ = reinterpret_cast<cudaStream_t>(stream);
+  if (T > qre::kDecodeMaxTokens) {
+    if (!qre::ffn_prefill_supported(*shape))
+      return fail(QRE_ERR_UNSUPPORTED, "no grouped-GEMM plan for hidden %d, inter %d, %d experts", shape->hidden,
+                  shape->inter, shape->n_experts);
+    st = check_workspace(workspace, workspace_bytes, qre::ffn_prefill_ws_bytes(*shape, T));
+    if (st != QRE_OK) return st;
+    return launched(qre::launch_ffn_prefill(*shape, T, x_bf16, slots, offsets, perm, active, n_active, expert_out,
+                                            workspace, qre::device_status_word(), st_),
+                    "qre_expert_ffn (grouped GEMM) launch");
+  }
   if (!qre::ffn_decode_supported(*shape))
     return fail(QRE_ERR_UNSUPPORTED, "no decode kernel plan for hidden %d, inter %d, group %d", shape->hidden,
                 shape->inter, shape->group);
   st = check_workspace(workspace, workspace_bytes, qre::ffn_ws_bytes(*shape, T));
   if (st != QRE_OK) return st;
   return launched(qre::launch_ffn_decode(*shape, T, x_bf16, slots, offsets, perm, active, n_active, expert_out,
-                                         workspace, qre::device_status_word(), reinterpret_cast<cudaStream_t>(stream)),
+                                         workspace, qre::device_status_word(), st_),
                   "qre_expert_ffn launch");
 }
 

@@ -63,11 +63,13 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   return done != 0;
 }
 
-// Waits for the phase of `bar` with the given parity.  Gives up when *abort is
-// set by another warp, or when the global timer passes `deadline` (then it sets
-// *abort and the status bit).  Returns true when the phase completed.
-__device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity, volatile int* abort,
-                                                  uint64_t deadline, int* status) {
+// Waits for the phase of `bar` with the given parity, for at most kWaitLimitNs
+// from the first failed poll.  Gives up early when *abort is set by another
+// warp; on expiry sets *abort and QRE_DEV_TIMEOUT.  Returns true when the phase
+// completed.
+__device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity, volatile int* abort, int* status) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t deadline = global_timer_ns() + kWaitLimitNs;
   uint32_t spins = 0;
   while (!mbar_try_wait(bar, parity)) {
     if (abort && *abort) return false;

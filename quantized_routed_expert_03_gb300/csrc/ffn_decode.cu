@@ -257,7 +257,6 @@ __global__ void __launch_bounds__(kThreads, 1) ffn_decode_kernel(const FfnParams
     fence_barrier_init();
   }
   __syncthreads();
-  const uint64_t deadline = global_timer_ns() + kWaitLimitNs;
 
   if (warp == kNW) {
     // ---------------- producer: one thread issues the bulk copies
@@ -270,7 +269,7 @@ __global__ void __launch_bounds__(kThreads, 1) ffn_decode_kernel(const FfnParams
         if (!un.ok || un.host) continue;
         const int s = it % p.nstage;
         const uint32_t par = ((it / p.nstage) & 1) ^ 1;
-        if (!mbar_wait_bounded(&empty[s], par, abort_flag, deadline, p.status)) break;
+        if (!mbar_wait_bounded(&empty[s], par, abort_flag, p.status)) break;
         uint8_t* dst = stages + (size_t)s * p.stage_bytes;
         mbar_arrive_expect_tx(&full[s], kRows * row_bytes + scale_bytes);
         for (int r = 0; r < kRows; ++r) bulk_copy_g2s(dst + r * p.pitch, un.w + (size_t)r * row_bytes, row_bytes, &full[s]);
@@ -280,7 +279,7 @@ __global__ void __launch_bounds__(kThreads, 1) ffn_decode_kernel(const FfnParams
       // Every issued copy must land before the CTA exits (also after an abort).
       const int first = it > p.nstage ? it - p.nstage : 0;
       for (int j = first; j < it; ++j)
-        mbar_wait_bounded(&full[j % p.nstage], (j / p.nstage) & 1, nullptr, deadline + kWaitLimitNs, p.status);
+        mbar_wait_bounded(&full[j % p.nstage], (j / p.nstage) & 1, nullptr, p.status);
     }
     return;
   }
@@ -312,7 +311,7 @@ __global__ void __launch_bounds__(kThreads, 1) ffn_decode_kernel(const FfnParams
       float acc[4] = {0.f, 0.f, 0.f, 0.f};
       if (!un.host) {
         const int s = it % p.nstage;
-        const bool have = mbar_wait_bounded(&full[s], (it / p.nstage) & 1, abort_flag, deadline, p.status);
+        const bool have = mbar_wait_bounded(&full[s], (it / p.nstage) & 1, abort_flag, p.status);
         const uint32_t wb = smem_addr(stages + (size_t)s * p.stage_bytes);
         if (have) unit_dot<CPW, NB, true>(wb, p.pitch, wb + kRows * p.pitch, p.K / p.G, c0, p.gc, g, t, bfr, acc);
         __syncwarp();

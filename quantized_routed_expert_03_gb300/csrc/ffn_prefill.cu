@@ -1,0 +1,505 @@
+// ffn_prefill.cu -- the expert FFN for T > 8 as a grouped GEMM on tcgen05/TMEM.
+//
+// Prefill pushes thousands of tokens through one MoE layer (the RTX PRO 6000
+// recipe prefills in chunks of 4096 tokens, the glm53-flash-offload README in
+// chunks of 8192); each expert sees ~T*k/E tokens, enough to make its FFN a
+// dense contraction.  The weights are the M side of the MMA (128 output rows
+// per tile), the expert's tokens the N side (up to 256 per tile): D[feature,
+// token] += W[feature, k] * X[token, k].
+//
+// Three kernels:
+//   gather   Xg[q] = fp16(x[token of pick perm[q]]) for the T*k sorted picks,
+//            then Xg[T*k + t] = fp16(x[t]) for the shared expert.  Every
+//            expert's tokens become a contiguous row range of Xg.
+//   GEMM 1   per tile (expert, 128 rows of the interleaved gate/up matrix, <=256
+//            tokens); the epilogue pairs each gate row with its up row (they sit
+//            16 TMEM lanes apart) and writes h = silu(g) * u as fp16 to h16.
+//   GEMM 2   per tile (expert, 128 rows of W_down, <=256 tokens) from h16 rows;
+//            the epilogue writes fp32 rows of expert_out (row q = pick at sorted
+//            position q; row T*k + t = shared expert for token t).
+// Both GEMMs are one persistent warp-specialised kernel, one CTA per SM:
+//   warp 0      TMA loads of the token operand (128-byte swizzle) into a 4-stage ring
+//   warp 1      allocates 512 TMEM columns (two 128x256 fp32 accumulators) and
+//               issues tcgen05.mma (M=128, N<=256, K=16) from one thread
+//   warps 2-5   dequantize the weight operand: one thread per row decodes 64
+//               nibbles per stage, multiplies by the group scale in fp16 and
+//               stores the 128-byte swizzled rows the MMA expects
+//   warps 6-9   epilogue: tcgen05.ld of the finished accumulator while the MMA
+//               warp fills the other one
+// Operands are fp16 (x bf16 -> fp16 is exact in fp16's normal range; dequantized
+// weights and h are rounded to fp16), accumulation fp32.
+#include "common.cuh"
+#include "internal.h"
+#include "tc.cuh"
+
+namespace qre {
+namespace {
+
+constexpr int BM = 128;                 // weight rows per tile
+constexpr int BN = 256;                 // tokens per tile (max)
+constexpr int BK = 64;                  // reduction elements per stage: one 128-byte swizzle row
+constexpr int NSTAGE = 4;
+constexpr int A_STAGE = BM * BK * 2;    // 16 KB
+constexpr int B_STAGE = BN * BK * 2;    // 32 KB
+constexpr int kWarps = 10;
+constexpr int kThreads = kWarps * 32;
+constexpr int kTmemCols = 512;
+constexpr int kAccCols = 256;
+
+struct PrefillParams {
+  int H, I, E, k, G, T;
+  int K;        // reduction length: H (gate/up) or I (down)
+  int n_out;    // weight rows: 2I or H
+  int amax;     // largest possible number of active experts
+  const qre_slot* slots;
+  const int32_t* offsets;
+  const int32_t* active;
+  const int32_t* n_active;
+  __half* h16;         // [T*k + T][I]
+  float* expert_out;   // [T*k + T][H]
+  int* status;
+};
+
+struct SmemLayout {
+  static constexpr int a_off = 0;
+  static constexpr int b_off = NSTAGE * A_STAGE;
+  static constexpr int bar_off = b_off + NSTAGE * B_STAGE;
+  // full_a[NS], full_b[NS], empty[NS], acc_full[2], acc_empty[2]
+  static constexpr int nbars = 3 * NSTAGE + 4;
+  static constexpr int misc_off = bar_off + nbars * 8;   // tmem base, abort flag, group count, tile count
+  static constexpr int tab_off = misc_off + 16;
+  static size_t bytes(int E) { return (size_t)tab_off + 3 * (size_t)(E + 2) * 4 + 1024; }
+};
+
+// ---------------------------------------------------------------- gather
+
+__global__ void __launch_bounds__(256) gather_x_kernel(int T, int H, int k, const uint16_t* __restrict__ x,
+                                                       const int32_t* __restrict__ perm, __half* __restrict__ xg,
+                                                       int* status) {
+  const long long P = (long long)T * k;
+  const int per_row = H / 8;
+  const long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+  if (i >= (P + T) * per_row) return;
+  const long long q = i / per_row;
+  const int c = (int)(i - q * per_row) * 8;
+  const int t = q < P ? __ldg(perm + q) / k : (int)(q - P);
+  const uint4 v = __ldg(reinterpret_cast<const uint4*>(x + (size_t)t * H + c));
+  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+  uint32_t o[4];
+  bool bad = false;
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const float lo = bf16_bits_to_float(w[j] & 0xFFFFu), hi = bf16_bits_to_float(w[j] >> 16);
+    const __half2 h = __floats2half2_rn(lo, hi);
+    bad |= __hisinf(__low2half(h)) || __hisinf(__high2half(h));
+    o[j] = h2_as_u32(h);
+  }
+  if (bad) set_status(status, QRE_DEV_FP16_RANGE);
+  *reinterpret_cast<uint4*>(xg + (size_t)q * H + c) = make_uint4(o[0], o[1], o[2], o[3]);
+}
+
+// ---------------------------------------------------------------- GEMM
+
+struct Tile {
+  int g;       // group: active index, or n_act for the shared expert
+  int e;       // expert id (E = shared)
+  int row0;    // first row of the group in Xg / h16 / expert_out
+  int M;       // tokens in the group
+  int m0;      // first weight row
+  int n0;      // first token of the tile within the group
+  int n;       // tokens in this tile
+};
+
+__device__ __forceinline__ Tile decode_tile(int t, int ngroups, const int* tstart, const int* row0, const int* gm,
+                                            int mt_per, int n_act, const int32_t* active, int E) {
+  int lo = 0, hi = ngroups - 1;
+  while (lo < hi) {  // last g with tstart[g] <= t
+    const int mid = (lo + hi + 1) >> 1;
+    if (tstart[mid] <= t) lo = mid;
+    else hi = mid - 1;
+  }
+  Tile tl;
+  tl.g = lo;
+  tl.e = lo < n_act ? __ldg(active + lo) : E;
+  tl.row0 = row0[lo];
+  tl.M = gm[lo];
+  const int local = t - tstart[lo];
+  const int nt = local / mt_per, mt = local - nt * mt_per;
+  tl.m0 = mt * BM;
+  tl.n0 = nt * BN;
+  tl.n = min(BN, tl.M - tl.n0);
+  return tl;
+}
+
+// Eight nibbles (k, k+1, ..., k+7 from the low end of w) -> eight fp16 values
+// q*s in natural k order, as four half2.
+__device__ __forceinline__ uint4 dequant8(uint32_t w, __half2 s2) {
+  uint32_t p[4];
+  decode_nibbles(w, p);  // (q0,q4) (q1,q5) (q2,q6) (q3,q7)
+  const uint32_t n01 = __byte_perm(p[0], p[1], 0x5410);
+  const uint32_t n23 = __byte_perm(p[2], p[3], 0x5410);
+  const uint32_t n45 = __byte_perm(p[0], p[1], 0x7632);
+  const uint32_t n67 = __byte_perm(p[2], p[3], 0x7632);
+  uint4 r;
+  r.x = h2_as_u32(__hmul2(u32_as_h2(n01), s2));
+  r.y = h2_as_u32(__hmul2(u32_as_h2(n23), s2));
+  r.z = h2_as_u32(__hmul2(u32_as_h2(n45), s2));
+  r.w = h2_as_u32(__hmul2(u32_as_h2(n67), s2));
+  return r;
+}
+
+template <int MODE>
+__global__ void __launch_bounds__(kThreads, 1) prefill_gemm_kernel(const PrefillParams p,
+                                                                   const __grid_constant__ CUtensorMap tmap_b) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
+  uint8_t* As = smem + SmemLayout::a_off;
+  uint8_t* Bs = smem + SmemLayout::b_off;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + SmemLayout::bar_off);
+  uint64_t* full_a = bars;
+  uint64_t* full_b = bars + NSTAGE;
+  uint64_t* empty = bars + 2 * NSTAGE;
+  uint64_t* acc_full = bars + 3 * NSTAGE;
+  uint64_t* acc_empty = acc_full + 2;
+  uint32_t* tmem_base_p = reinterpret_cast<uint32_t*>(smem + SmemLayout::misc_off);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + SmemLayout::misc_off + 4);
+  int* counts_p = reinterpret_cast<int*>(smem + SmemLayout::misc_off + 8);  // ngroups, ntiles
+  int* tstart = reinterpret_cast<int*>(smem + SmemLayout::tab_off);
+  int* grow0 = tstart + (p.E + 2);
+  int* gM = grow0 + (p.E + 2);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int P = p.T * p.k;
+  const int mt_per = p.n_out / BM;
+  const int KB = p.K / BK;
+
+  int n_act = *p.n_active;
+  n_act = n_act < 0 ? 0 : (n_act > p.amax ? p.amax : n_act);
+  const int ngroups = n_act + 1;
+
+  // group table: rows, tokens and first tile of every group (one warp)
+  if (warp == 0) {
+    int carry = 0;
+    for (int base = 0; base < ngroups; base += 32) {
+      const int g = base + lane;
+      int tiles = 0;
+      if (g < ngroups) {
+        int r0, m;
+        if (g < n_act) {
+          const int e = __ldg(p.active + g);
+          r0 = __ldg(p.offsets + e);
+          m = __ldg(p.offsets + e + 1) - r0;
+        } else {
+          r0 = P;
+          m = p.T;
+        }
+        grow0[g] = r0;
+        gM[g] = m;
+        tiles = ((m + BN - 1) / BN) * mt_per;
+      }
+      int inc = tiles;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, inc, o);
+        if (lane >= o) inc += y;
+      }
+      if (g < ngroups) tstart[g] = carry + inc - tiles;
+      carry += __shfl_sync(0xffffffffu, inc, 31);
+    }
+    if (lane == 0) {
+      tstart[ngroups] = carry;
+      counts_p[0] = ngroups;
+      counts_p[1] = carry;
+    }
+  }
+  if (threadIdx.x == 32) {
+    for (int s = 0; s < NSTAGE; ++s) {
+      mbar_init(&full_a[s], 128);
+      mbar_init(&full_b[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&acc_full[b], 1);
+      mbar_init(&acc_empty[b], 128);
+    }
+    *abort_flag = 0;
+    fence_barrier_init();
+  }
+  if (warp == 1) {
+    __syncwarp();
+    tmem_alloc(tmem_base_p, kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_base_p;
+  const int ntiles = counts_p[1];
+
+  if (warp == 0) {
+    // ---------------- token operand: TMA
+    if (lane == 0) {
+      int it = 0;
+      for (int t = blockIdx.x; t < ntiles; t += gridDim.x) {
+        const Tile tl = decode_tile(t, ngroups, tstart, grow0, gM, mt_per, n_act, p.active, p.E);
+        for (int kb = 0; kb < KB; ++kb, ++it) {
+          const int s = it % NSTAGE;
+          if (!mbar_wait_bounded(&empty[s], ((it / NSTAGE) & 1) ^ 1, abort_flag, p.status)) goto b_done;
+          mbar_arrive_expect_tx(&full_b[s], B_STAGE);
+          tma_load_2d(Bs + (size_t)s * B_STAGE, &tmap_b, kb * BK, tl.row0 + tl.n0, &full_b[s]);
+        }
+      }
+    b_done:
+      const int first = it > NSTAGE ? it - NSTAGE : 0;
+      for (int j = first; j < it; ++j)
+        mbar_wait_bounded(&full_b[j % NSTAGE], (j / NSTAGE) & 1, nullptr, p.status);
+    }
+  } else if (warp == 1) {
+    // ---------------- MMA issue (one thread)
+    if (lane == 0) {
+      int it = 0, lt = 0, last = -1;
+      for (int t = blockIdx.x; t < ntiles; t += gridDim.x, ++lt) {
+        const Tile tl = decode_tile(t, ngroups, tstart, grow0, gM, mt_per, n_act, p.active, p.E);
+        const int buf = lt & 1;
+        if (!mbar_wait_bounded(&acc_empty[buf], ((lt >> 1) & 1) ^ 1, abort_flag, p.status)) break;
+        tc_fence_after();
+        const uint32_t d_tmem = tmem_base + buf * kAccCols;
+        const int n_mma = (tl.n + 15) & ~15;
+        const uint32_t idesc = umma_idesc_f16(BM, n_mma);
+        bool ok = true;
+        for (int kb = 0; kb < KB; ++kb, ++it) {
+          const int s = it % NSTAGE;
+          const uint32_t ph = (it / NSTAGE) & 1;
+          if (!mbar_wait_bounded(&full_a[s], ph, abort_flag, p.status) ||
+              !mbar_wait_bounded(&full_b[s], ph, abort_flag, p.status)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint64_t a0 = umma_desc_sw128(smem_addr(As + (size_t)s * A_STAGE));
+          const uint64_t b0 = umma_desc_sw128(smem_addr(Bs + (size_t)s * B_STAGE));
+#pragma unroll
+          for (int j = 0; j < BK / 16; ++j)  // advance 16 elements = 32 bytes inside the swizzle row
+            umma_f16(d_tmem, a0 + (uint64_t)(2 * j), b0 + (uint64_t)(2 * j), idesc, (kb | j) != 0);
+          umma_commit(&empty[s]);
+        }
+        umma_commit(&acc_full[buf]);
+        last = lt;
+        if (!ok) break;
+      }
+      // TMEM is freed below: every MMA issued here must have completed first
+      if (last >= 0) mbar_wait_bounded(&acc_full[last & 1], (last >> 1) & 1, nullptr, p.status);
+    }
+  } else if (warp < 6) {
+    // ---------------- weight operand: dequantize into the swizzled stage
+    const int r = threadIdx.x - 64;  // row within the tile, 0..127
+    const int sw = r & 7;
+    const uint32_t row_off = (uint32_t)(r >> 3) * 1024 + (uint32_t)sw * 128;
+    int it = 0;
+    const int KG = p.K / p.G;
+    for (int t = blockIdx.x; t < ntiles; t += gridDim.x) {
+      const Tile tl = decode_tile(t, ngroups, tstart, grow0, gM, mt_per, n_act, p.active, p.E);
+      const qre_slot* sl = p.slots + tl.e;
+      const uint8_t* wb = MODE == 0 ? sl->w_gate_up : sl->w_down;
+      const uint16_t* sb = MODE == 0 ? sl->s_gate_up : sl->s_down;
+      const bool valid = wb && sb && ((reinterpret_cast<uintptr_t>(wb) | reinterpret_cast<uintptr_t>(sb)) & 15) == 0;
+      if (!valid && r == 0) set_status(p.status, QRE_DEV_NULL_SLOT);
+      const uint4* wrow = valid ? reinterpret_cast<const uint4*>(wb + (size_t)(tl.m0 + r) * (p.K / 2)) : nullptr;
+      const uint16_t* srow = valid ? sb + (size_t)(tl.m0 + r) * KG : nullptr;
+      uint4 ring[4][2];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        if (valid && j < KB) {
+          ring[j][0] = __ldg(wrow + 2 * j);
+          ring[j][1] = __ldg(wrow + 2 * j + 1);
+        } else {
+          ring[j][0] = ring[j][1] = make_uint4(0x88888888u, 0x88888888u, 0x88888888u, 0x88888888u);
+        }
+      }
+      for (int kb0 = 0; kb0 < KB; kb0 += 4) {
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const int kb = kb0 + j;
+          if (kb < KB) {
+            const int s = it % NSTAGE;
+            const bool go = mbar_wait_bounded(&empty[s], ((it / NSTAGE) & 1) ^ 1, abort_flag, p.status);
+            if (go) {
+              float sa = 0.f, sbv = 0.f;
+              if (valid) {
+                sa = __half2float(__ushort_as_half(__ldg(srow + (kb * BK) / p.G)));
+                sbv = __half2float(__ushort_as_half(__ldg(srow + (kb * BK + 32) / p.G)));
+              }
+              const __half2 s2a = __float2half2_rn(sa), s2b = __float2half2_rn(sbv);
+              const uint32_t words[8] = {ring[j][0].x, ring[j][0].y, ring[j][0].z, ring[j][0].w,
+                                         ring[j][1].x, ring[j][1].y, ring[j][1].z, ring[j][1].w};
+              uint8_t* stage = As + (size_t)s * A_STAGE + row_off;
+#pragma unroll
+              for (int c = 0; c < 8; ++c) {
+                const uint4 v = dequant8(words[c], c < 4 ? s2a : s2b);
+                *reinterpret_cast<uint4*>(stage + ((c ^ sw) << 4)) = v;
+              }
+              fence_proxy_async_smem();
+            }
+            mbar_arrive(&full_a[s]);
+            ++it;
+            if (valid && kb + 4 < KB) {
+              ring[j][0] = __ldg(wrow + 2 * (kb + 4));
+              ring[j][1] = __ldg(wrow + 2 * (kb + 4) + 1);
+            }
+          }
+        }
+      }
+    }
+  } else {
+    // ---------------- epilogue
+    const int q = warp & 3;  // TMEM lane quarter this warp may access
+    int lt = 0;
+    for (int t = blockIdx.x; t < ntiles; t += gridDim.x, ++lt) {
+      const Tile tl = decode_tile(t, ngroups, tstart, grow0, gM, mt_per, n_act, p.active, p.E);
+      const int buf = lt & 1;
+      const bool have = mbar_wait_bounded(&acc_full[buf], (lt >> 1) & 1, abort_flag, p.status);
+      tc_fence_after();
+      if (have) {
+        const uint32_t tbase = tmem_base + ((uint32_t)(32 * q) << 16) + buf * kAccCols;
+        for (int c0 = 0; c0 < tl.n; c0 += 32) {
+          uint32_t v[32];
+          tmem_ld_32x32b_x32(tbase + c0, v);
+          tmem_ld_wait();
+          if constexpr (MODE == 0) {
+            // lanes 0-15 hold gate rows, lanes 16-31 the matching up rows
+            const int feat = tl.m0 / 2 + 16 * q + (lane & 15);
+#pragma unroll
+            for (int j = 0; j < 32; ++j) {
+              const float up = __shfl_down_sync(0xffffffffu, __uint_as_float(v[j]), 16);
+              const int n = c0 + j;
+              if (lane < 16 && n < tl.n) {
+                const float g = __uint_as_float(v[j]);
+                const float h = g / (1.0f + expf(-g)) * up;
+                const __half hh = __float2half_rn(h);
+                if (__hisinf(hh)) set_status(p.status, QRE_DEV_FP16_RANGE);
+                p.h16[(size_t)(tl.row0 + tl.n0 + n) * p.I + feat] = hh;
+              }
+            }
+          } else {
+            const int col = tl.m0 + 32 * q + lane;
+#pragma unroll
+            for (int j = 0; j < 32; ++j) {
+              const int n = c0 + j;
+              if (n < tl.n) p.expert_out[(size_t)(tl.row0 + tl.n0 + n) * p.H + col] = __uint_as_float(v[j]);
+            }
+          }
+        }
+      }
+      tc_fence_before();
+      mbar_arrive(&acc_empty[buf]);
+    }
+  }
+
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem_base, kTmemCols);
+  }
+}
+
+// ---------------------------------------------------------------- host
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static bool tried = false;
+  if (!tried) {
+    tried = true;
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  }
+  return fn;
+}
+
+// 2-D fp16 row-major [rows][cols] -> boxes of 64 columns x 256 rows, 128-byte swizzle.
+bool make_tmap(CUtensorMap* m, const void* base, long long rows, int cols) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+  cuuint64_t strides[1] = {(cuuint64_t)cols * 2};
+  cuuint32_t box[2] = {BK, BN};
+  cuuint32_t estr[2] = {1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+size_t align256(size_t b) { return (b + 255) & ~(size_t)255; }
+
+}  // namespace
+
+size_t ffn_prefill_ws_bytes(const qre_layer_shape& s, int T) {
+  const size_t rows = (size_t)T * s.top_k + T;
+  return align256(rows * s.hidden * 2) + align256(rows * s.inter * 2);
+}
+
+bool ffn_prefill_supported(const qre_layer_shape& s) {
+  return s.hidden % BK == 0 && s.inter % BK == 0 && (2 * s.inter) % BM == 0 && s.hidden % BM == 0 &&
+         SmemLayout::bytes(s.n_experts) <= (size_t)device_max_smem_optin();
+}
+
+cudaError_t launch_ffn_prefill(const qre_layer_shape& s, int T, const uint16_t* x, const qre_slot* slots,
+                               const int32_t* offsets, const int32_t* perm, const int32_t* active,
+                               const int32_t* n_active, float* expert_out, void* ws, int* status,
+                               cudaStream_t stream) {
+  const long long P = (long long)T * s.top_k;
+  const long long rows = P + T;
+  __half* xg = static_cast<__half*>(ws);
+  __half* h16 = reinterpret_cast<__half*>(static_cast<uint8_t*>(ws) + align256((size_t)rows * s.hidden * 2));
+
+  {
+    const long long n = rows * (s.hidden / 8);
+    gather_x_kernel<<<(unsigned)((n + 255) / 256), 256, 0, stream>>>(T, s.hidden, s.top_k, x, perm, xg, status);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+  }
+  CUtensorMap tx, th;
+  if (!make_tmap(&tx, xg, rows, s.hidden) || !make_tmap(&th, h16, rows, s.inter)) return cudaErrorInvalidValue;
+
+  PrefillParams p{};
+  p.H = s.hidden;
+  p.I = s.inter;
+  p.E = s.n_experts;
+  p.k = s.top_k;
+  p.G = s.group;
+  p.T = T;
+  p.amax = (int)(P < s.n_experts ? P : s.n_experts);
+  p.slots = slots;
+  p.offsets = offsets;
+  p.active = active;
+  p.n_active = n_active;
+  p.h16 = h16;
+  p.expert_out = expert_out;
+  p.status = status;
+  const size_t smem = SmemLayout::bytes(s.n_experts);
+  const int grid = device_sm_count();
+
+  p.K = s.hidden;
+  p.n_out = 2 * s.inter;
+  cudaError_t e = ensure_smem_limit(reinterpret_cast<const void*>(prefill_gemm_kernel<0>), (int)smem);
+  if (e != cudaSuccess) return e;
+  prefill_gemm_kernel<0><<<grid, kThreads, smem, stream>>>(p, tx);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+
+  p.K = s.inter;
+  p.n_out = s.hidden;
+  e = ensure_smem_limit(reinterpret_cast<const void*>(prefill_gemm_kernel<1>), (int)smem);
+  if (e != cudaSuccess) return e;
+  prefill_gemm_kernel<1><<<grid, kThreads, smem, stream>>>(p, th);
+  return cudaGetLastError();
+}
+
+}  // namespace qre

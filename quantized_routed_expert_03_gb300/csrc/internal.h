@@ -49,6 +49,14 @@ cudaError_t launch_ffn_decode(const qre_layer_shape& s, int T, const uint16_t* x
                               cudaStream_t stream);
 bool ffn_decode_supported(const qre_layer_shape& s);
 
+// Grouped-GEMM expert FFN for T > kDecodeMaxTokens (tcgen05, TMEM, TMA).
+size_t ffn_prefill_ws_bytes(const qre_layer_shape& s, int T);
+bool ffn_prefill_supported(const qre_layer_shape& s);
+cudaError_t launch_ffn_prefill(const qre_layer_shape& s, int T, const uint16_t* x, const qre_slot* slots,
+                               const int32_t* offsets, const int32_t* perm, const int32_t* active,
+                               const int32_t* n_active, float* expert_out, void* ws, int* status,
+                               cudaStream_t stream);
+
 cudaError_t launch_combine(const qre_layer_shape& s, int T, const float* expert_out, const float* topk_w,
                            const int32_t* inv_perm, float* y_f32, uint16_t* y_bf16, cudaStream_t stream);
 

@@ -68,8 +68,8 @@ class ExpertArena:
         if self.host:
             if staging is None:
                 staging = torch.empty(self.layout["stride"], dtype=torch.uint8, device=w_gate.device)
-            dst = {n: staging[off:off + size] for n, (off, size) in self.layout.items()
-                   if n in ("w_gate_up", "s_gate_up", "w_down", "s_down")}
+            dst = {n: staging[self.layout[n][0]:self.layout[n][0] + self.layout[n][1]]
+                   for n in ("w_gate_up", "s_gate_up", "w_down", "s_down")}
         else:
             dst = {n: self.view(e, n) for n in ("w_gate_up", "s_gate_up", "w_down", "s_down")}
         qre_quantize_gate_up(I, H, G, w_gate, w_up, dst["w_gate_up"], dst["s_gate_up"], stream)

@@ -54,7 +54,7 @@ def test_quantize_special_values_bit_exact():
 
 def test_quantize_gate_up_interleave_bit_exact():
     rng = np.random.default_rng(12)
-    I, H, G = 64, 512, 128
+    I, H, G = 128, 512, 128
     Wg = (rng.standard_normal((I, H)) * 0.02).astype(np.float32)
     Wu = (rng.standard_normal((I, H)) * 0.02).astype(np.float32)
     wg, wu = (torch.from_numpy(a).to(DEV) for a in (Wg, Wu))

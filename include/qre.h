@@ -234,6 +234,46 @@ QRE_API qre_status qre_combine(const qre_layer_shape* shape, int32_t T, const fl
                        uint16_t* y_bf16, qre_stream_t stream);
 
 /*
+ * Expert cache, manager step (one CTA, stream-ordered, no host sync).  Per layer
+ * and call, after qre_dispatch: the LFU scores decay, every miss takes the
+ * lowest-scoring cache slot that this call does not use, and `table` (the slot
+ * table qre_expert_ffn reads) is rewritten in place -- the RTX PRO 6000 recipe's
+ * config.expert_cache.mechanism (decay 0.995 there).
+ *   n_slots      number of cache slots S (1 <= S <= 1024)
+ *   decay        score decay per call, e.g. 0.995
+ *   active, n_active   this call's expert union, from qre_dispatch (device)
+ *   scores       [E] fp32 (device, read-write); scores[e] = fp32(fp32(scores[e] *
+ *                decay) + [e used by this call])
+ *   expert_slot  [E] int32 (device, read-write): slot of e, -1 not cached, -2 static
+ *   slot_expert  [S] int32 (device, read-write): expert in slot s, -1 empty
+ *   home         [E+1] qre_slot (device): where each expert lives when it is not
+ *                cached (pinned host memory, tier 1) -- never dereferenced here
+ *   slot_mem     [S] qre_slot (device): the HBM addresses of the slots (tier 0)
+ *   table        [E+1] qre_slot (device, rewritten): admitted experts -> their
+ *                slot, evicted experts -> home
+ *   copy_list    [2 * max_copies] int32 (device, written): (expert, slot) pairs
+ *   n_copies     [1] int32 (device, written): admissions of this call
+ * Misses are handled in ascending expert id; the victim is the candidate slot
+ * with the lowest score of its current expert (empty slots first), ties to the
+ * lowest slot index; a miss with no candidate stays host-resident this call.
+ */
+QRE_API qre_status qre_cache_update(const qre_layer_shape* shape, int32_t n_slots, float decay,
+                                    const int32_t* active, const int32_t* n_active, float* scores,
+                                    int32_t* expert_slot, int32_t* slot_expert, const qre_slot* home,
+                                    const qre_slot* slot_mem, qre_slot* table, int32_t* copy_list,
+                                    int32_t* n_copies, int32_t max_copies, qre_stream_t stream);
+
+/*
+ * Expert cache, miss copy: copies each admitted expert's four arrays from
+ * home[e] (pinned host memory, read over the host link) to slot_mem[s] (HBM),
+ * reading the number of copies on the device (no host sync).  Arguments as in
+ * qre_cache_update; all device.
+ */
+QRE_API qre_status qre_cache_copy(const qre_layer_shape* shape, const qre_slot* home, const qre_slot* slot_mem,
+                                  const int32_t* copy_list, const int32_t* n_copies, int32_t max_copies,
+                                  qre_stream_t stream);
+
+/*
  * Checks a HOST copy of a slot table before it is uploaded: every pointer
  * non-null and 16-byte aligned, reserved == 0, tier in {0, 1}, tier-0
  * pointers in device memory and tier-1 pointers in host memory that the

@@ -39,6 +39,7 @@ EXPORTS = (
     "qre_last_error", "qre_status_string", "qre_version", "qre_workspace_size", "qre_quantize",
     "qre_quantize_gate_up",
     "qre_route", "qre_dispatch", "qre_expert_ffn", "qre_combine", "qre_validate_slots",
+    "qre_cache_update", "qre_cache_copy",
     "qre_read_device_status", "qre_clear_device_status",
 )
 
@@ -78,6 +79,9 @@ _SIGS = {
     "qre_expert_ffn": ([_SHAPE, _I32, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _SZ, _VP], ctypes.c_int),
     "qre_combine": ([_SHAPE, _I32, _VP, _VP, _VP, _VP, _VP, _VP], ctypes.c_int),
     "qre_validate_slots": ([_SHAPE, ctypes.POINTER(qre_slot)], ctypes.c_int),
+    "qre_cache_update": ([_SHAPE, _I32, ctypes.c_float, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _I32, _VP],
+                         ctypes.c_int),
+    "qre_cache_copy": ([_SHAPE, _VP, _VP, _VP, _VP, _I32, _VP], ctypes.c_int),
     "qre_read_device_status": ([_VP, ctypes.POINTER(ctypes.c_int32)], ctypes.c_int),
     "qre_clear_device_status": ([_VP], ctypes.c_int),
 }
@@ -188,6 +192,19 @@ def qre_expert_ffn(shape, T, x_bf16, slots, offsets, perm, active, n_active, exp
 def qre_combine(shape, T, expert_out, topk_w, inv_perm, y_f32, y_bf16, stream=None) -> None:
     _check(load_library().qre_combine(ctypes.byref(shape), T, _ptr(expert_out), _ptr(topk_w), _ptr(inv_perm),
                                        _ptr(y_f32), _ptr(y_bf16), _stream(stream)), "qre_combine")
+
+
+def qre_cache_update(shape, n_slots, decay, active, n_active, scores, expert_slot, slot_expert, home, slot_mem,
+                     table, copy_list, n_copies, max_copies, stream=None) -> None:
+    _check(load_library().qre_cache_update(ctypes.byref(shape), n_slots, decay, _ptr(active), _ptr(n_active),
+                                           _ptr(scores), _ptr(expert_slot), _ptr(slot_expert), _ptr(home),
+                                           _ptr(slot_mem), _ptr(table), _ptr(copy_list), _ptr(n_copies),
+                                           max_copies, _stream(stream)), "qre_cache_update")
+
+
+def qre_cache_copy(shape, home, slot_mem, copy_list, n_copies, max_copies, stream=None) -> None:
+    _check(load_library().qre_cache_copy(ctypes.byref(shape), _ptr(home), _ptr(slot_mem), _ptr(copy_list),
+                                         _ptr(n_copies), max_copies, _stream(stream)), "qre_cache_copy")
 
 
 def qre_validate_slots(shape, host_slots) -> None:

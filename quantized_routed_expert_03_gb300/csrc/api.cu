@@ -282,6 +282,45 @@ qre_status qre_combine(const qre_layer_shape* shape, int32_t T, const float* exp
                   "qre_combine launch");
 }
 
+qre_status qre_cache_update(const qre_layer_shape* shape, int32_t n_slots, float decay, const int32_t* active,
+                            const int32_t* n_active, float* scores, int32_t* expert_slot, int32_t* slot_expert,
+                            const qre_slot* home, const qre_slot* slot_mem, qre_slot* table, int32_t* copy_list,
+                            int32_t* n_copies, int32_t max_copies, qre_stream_t stream) {
+  qre_status st = check_shape(shape, 0);
+  if (st != QRE_OK) return st;
+  if (n_slots < 1 || n_slots > 1024) return fail(QRE_ERR_UNSUPPORTED, "n_slots %d not in [1, 1024]", n_slots);
+  if (max_copies < 1) return fail(QRE_ERR_INVALID_ARG, "max_copies %d < 1", max_copies);
+  if (!(decay >= 0.0f && decay <= 1.0f)) return fail(QRE_ERR_INVALID_ARG, "decay must be in [0, 1]");
+  QRE_REQUIRE_PTR(active);
+  QRE_REQUIRE_PTR(n_active);
+  QRE_REQUIRE_PTR(scores);
+  QRE_REQUIRE_PTR(expert_slot);
+  QRE_REQUIRE_PTR(slot_expert);
+  QRE_REQUIRE_PTR(home);
+  QRE_REQUIRE_PTR(slot_mem);
+  QRE_REQUIRE_PTR(table);
+  QRE_REQUIRE_PTR(copy_list);
+  QRE_REQUIRE_PTR(n_copies);
+  return launched(qre::launch_cache_update(shape->n_experts, n_slots, decay, active, n_active, scores, slot_expert,
+                                           expert_slot, home, slot_mem, table, copy_list, n_copies, max_copies,
+                                           qre::device_status_word(), reinterpret_cast<cudaStream_t>(stream)),
+                  "qre_cache_update launch");
+}
+
+qre_status qre_cache_copy(const qre_layer_shape* shape, const qre_slot* home, const qre_slot* slot_mem,
+                          const int32_t* copy_list, const int32_t* n_copies, int32_t max_copies, qre_stream_t stream) {
+  qre_status st = check_shape(shape, 0);
+  if (st != QRE_OK) return st;
+  if (max_copies < 1) return fail(QRE_ERR_INVALID_ARG, "max_copies %d < 1", max_copies);
+  QRE_REQUIRE_PTR(home);
+  QRE_REQUIRE_PTR(slot_mem);
+  QRE_REQUIRE_PTR(copy_list);
+  QRE_REQUIRE_PTR(n_copies);
+  return launched(qre::launch_cache_copy(*shape, home, slot_mem, copy_list, n_copies, max_copies,
+                                         reinterpret_cast<cudaStream_t>(stream)),
+                  "qre_cache_copy launch");
+}
+
 qre_status qre_validate_slots(const qre_layer_shape* shape, const qre_slot* host_slots) {
   qre_status st = check_shape(shape, 0);
   if (st != QRE_OK) return st;

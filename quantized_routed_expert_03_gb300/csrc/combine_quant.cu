@@ -117,8 +117,9 @@ __global__ void __launch_bounds__(256) quantize_kernel(long long n_threads, int 
 cudaError_t launch_combine(const qre_layer_shape& s, int T, const float* expert_out, const float* topk_w,
                            const int32_t* inv_perm, float* y_f32, uint16_t* y_bf16, cudaStream_t stream) {
   const int H = s.hidden;
-  dim3 grid((H / 4 + 255) / 256, T);
-  combine_kernel<<<grid, 256, 0, stream>>>(T, H, s.top_k, expert_out, topk_w, inv_perm, y_f32, y_bf16);
+  const int threads = T <= 8 ? 64 : 256;   // small batches: spread over more SMs
+  dim3 grid((H / 4 + threads - 1) / threads, T);
+  combine_kernel<<<grid, threads, 0, stream>>>(T, H, s.top_k, expert_out, topk_w, inv_perm, y_f32, y_bf16);
   return cudaGetLastError();
 }
 

@@ -41,10 +41,23 @@ namespace {
 
 constexpr int kNW = 16;                    // consumer warps
 constexpr int kThreads = (kNW + 1) * 32;   // + one producer warp
-constexpr int kRows = 16;                  // output rows per unit (MMA M)
+constexpr int kTiles = 2;                  // MMA M tiles (16 rows each) per unit
+constexpr int kRows = 16 * kTiles;         // rows per unit: one gate block + one up block
 constexpr int kTok = kDecodeMaxTokens;     // MMA N
 constexpr int kRedStride = 20;             // floats between token columns of a partial
-constexpr int kRedWarp = kTok * kRedStride;
+constexpr int kRedTile = kTok * kRedStride;
+constexpr int kRedWarp = kTiles * kRedTile;
+constexpr int kMaxGroups = kDecodeMaxTokens * 16 + 1;   // T*k active experts + the shared one
+
+// One active expert (or the shared expert) as this kernel sees it; built once
+// per CTA in shared memory so that no unit waits on dependent global loads.
+struct Group {
+  const uint8_t* w;    // packed matrix of this kernel (gate/up or down)
+  const uint16_t* s;   // its scales
+  int e;               // expert id (E = shared)
+  int flags;           // bit 0: usable, bit 1: host-resident (read with direct loads)
+  int outq[kTok];      // down kernel: expert_out row of token n, or -1
+};
 
 struct FfnParams {
   int H, I, E, k, G, T;
@@ -52,8 +65,10 @@ struct FfnParams {
   int n_out;        // rows per expert: 2I (gate/up) or H (down)
   int gc;           // 32-element chunks per quantization group
   int aw;           // working consumer warps
-  int pitch;        // shared-memory row pitch in bytes
-  int stage_bytes;  // rows + scales of one unit
+  int nparts;       // K is staged in this many parts; warp w reads part w / (aw / nparts)
+  int pitch;        // shared-memory row pitch in bytes (16 mod 128)
+  int part_bytes;   // bytes of one row in one part
+  int stage_bytes;  // rows of one part + the unit's scales
   int nstage;
   int amax;         // largest possible number of active experts, min(E, T*k)
   const uint16_t* x;
@@ -62,54 +77,11 @@ struct FfnParams {
   const int32_t* perm;
   const int32_t* active;
   const int32_t* n_active;
-  float* gu;          // [(max active + 1)][8][2I] fp32: gate/up outputs
+  uint16_t* hfrag;    // [(amax+1)][I/32][32 lanes][16 halves]: h as MMA B fragments
   float* expert_out;  // [T*k + T][H]
   int* status;
 };
 
-struct Unit {
-  const uint8_t* w;
-  const uint16_t* s;
-  int a;      // index in the active list; n_active = shared expert
-  int e;      // expert id (E = shared)
-  int r0;     // first output row
-  bool host;  // read over the host link
-  bool ok;
-};
-
-template <int MODE>
-__device__ __forceinline__ Unit resolve_unit(const FfnParams& p, int u, int n_act, int units_per_exp) {
-  Unit un;
-  un.a = u / units_per_exp;
-  un.r0 = (u - un.a * units_per_exp) * kRows;
-  un.e = (un.a < n_act) ? __ldg(p.active + un.a) : p.E;
-  un.ok = (un.e >= 0 && un.e <= p.E);
-  if (!un.ok) {
-    un.w = nullptr;
-    un.s = nullptr;
-    un.host = false;
-    return un;
-  }
-  const qre_slot* sl = p.slots + un.e;
-  const uint8_t* w = MODE == 0 ? sl->w_gate_up : sl->w_down;
-  const uint16_t* s = MODE == 0 ? sl->s_gate_up : sl->s_down;
-  un.host = sl->tier != 0;
-  un.ok = w != nullptr && s != nullptr && ((reinterpret_cast<uintptr_t>(w) | reinterpret_cast<uintptr_t>(s)) & 15) == 0;
-  un.w = w + (size_t)un.r0 * (p.K / 2);
-  un.s = s + (size_t)un.r0 * (p.K / p.G);
-  return un;
-}
-
-__device__ __forceinline__ uint32_t lds_u32(uint32_t addr) {
-  uint32_t v;
-  asm volatile("ld.shared.u32 %0, [%1];" : "=r"(v) : "r"(addr));
-  return v;
-}
-__device__ __forceinline__ float lds_half_as_float(uint32_t addr) {
-  unsigned short v;
-  asm volatile("ld.shared.u16 %0, [%1];" : "=h"(v) : "r"(addr));
-  return __half2float(__ushort_as_half(v));
-}
 __device__ __forceinline__ uint32_t ldg_u32(const void* p) {
   return __ldg(reinterpret_cast<const unsigned int*>(p));
 }
@@ -117,48 +89,88 @@ __device__ __forceinline__ float ldg_half_as_float(const uint16_t* p) {
   return __half2float(__ushort_as_half(__ldg(reinterpret_cast<const unsigned short*>(p))));
 }
 
-// Dot products of one unit's 16 rows with the warp's K range.  SMEM selects
-// shared-memory stage reads (wbase/sbase are shared addresses) or direct global
-// reads (host-resident experts).  NB = 4 (one fp16 operand) or 8 (high + low).
+// Dot products of one unit's 32 rows (two 16-row MMA tiles) with the warp's K
+// range.  SMEM: wbase/sbase point into the shared-memory stage (the staged part
+// and the unit's scales); otherwise global addresses of row 0 and its scales.
+// cbase is subtracted from the global chunk index to address the staged part.
+// Each tile accumulates into kAcc independent fragments (chunk cl goes to
+// cl % kAcc) so consecutive MMAs do not wait on each other; they are summed
+// when a quantization group ends.
+constexpr int kAcc = 2;
 template <int CPW, int NB, bool SMEM>
-__device__ __forceinline__ void unit_dot(uintptr_t wbase, int wpitch, uintptr_t sbase, int s_stride, int c0,
-                                         int gc, int g, int t, const uint32_t (&bfr)[CPW][NB], float (&acc)[4]) {
-  float d[4] = {0.f, 0.f, 0.f, 0.f};
+__device__ __forceinline__ void unit_dot(const uint8_t* wbase, int wpitch, const uint16_t* sbase, int s_stride,
+                                         int c0, int cbase, int gc, int g, int t,
+                                         const uint32_t (&bfr)[CPW][NB], float (&acc)[kTiles][4]) {
+  float d[kTiles][kAcc][4];
+#pragma unroll
+  for (int i = 0; i < kTiles; ++i)
+#pragma unroll
+    for (int j = 0; j < kAcc; ++j) d[i][j][0] = d[i][j][1] = d[i][j][2] = d[i][j][3] = 0.f;
+  // Loads are issued one quantization group (GCMAX chunks at most) ahead of
+  // their use, so they overlap the previous group's MMAs.
+  constexpr int GCMAX = CPW < 4 ? CPW : 4;
+  uint32_t wv[GCMAX][kTiles][2];
 #pragma unroll
   for (int cl = 0; cl < CPW; ++cl) {
     const int c = c0 + cl;
-    const uintptr_t off_lo = (uintptr_t)g * wpitch + c * 16 + t * 4;
-    const uintptr_t off_hi = off_lo + (uintptr_t)8 * wpitch;
-    uint32_t wlo, whi;
-    if constexpr (SMEM) {
-      wlo = lds_u32((uint32_t)(wbase + off_lo));
-      whi = lds_u32((uint32_t)(wbase + off_hi));
-    } else {
-      wlo = ldg_u32(reinterpret_cast<const void*>(wbase + off_lo));
-      whi = ldg_u32(reinterpret_cast<const void*>(wbase + off_hi));
+    const int j = cl % kAcc;
+    if (cl % GCMAX == 0) {
+#pragma unroll
+      for (int u = 0; u < GCMAX; ++u) {
+        const int col = (c + u - cbase) * 16 + t * 4;
+#pragma unroll
+        for (int i = 0; i < kTiles; ++i) {
+          const uint8_t* r_lo = wbase + (size_t)(16 * i + g) * wpitch + col;
+          const uint8_t* r_hi = r_lo + (size_t)8 * wpitch;
+          if constexpr (SMEM) {
+            wv[u][i][0] = *reinterpret_cast<const uint32_t*>(r_lo);
+            wv[u][i][1] = *reinterpret_cast<const uint32_t*>(r_hi);
+          } else {
+            wv[u][i][0] = ldg_u32(r_lo);
+            wv[u][i][1] = ldg_u32(r_hi);
+          }
+        }
+      }
     }
-    uint32_t pl[4], ph[4];
-    decode_nibbles(wlo, pl);
-    decode_nibbles(whi, ph);
-    mma_f16_16816(d, pl[0], ph[0], pl[1], ph[1], bfr[cl][0], bfr[cl][1]);
-    if constexpr (NB == 8) mma_f16_16816(d, pl[0], ph[0], pl[1], ph[1], bfr[cl][4], bfr[cl][5]);
-    mma_f16_16816(d, pl[2], ph[2], pl[3], ph[3], bfr[cl][2], bfr[cl][3]);
-    if constexpr (NB == 8) mma_f16_16816(d, pl[2], ph[2], pl[3], ph[3], bfr[cl][6], bfr[cl][7]);
+    const int u = cl % GCMAX;
+#pragma unroll
+    for (int i = 0; i < kTiles; ++i) {
+      uint32_t pl[4], ph[4];
+      decode_nibbles(wv[u][i][0], pl);
+      decode_nibbles(wv[u][i][1], ph);
+      mma_f16_16816(d[i][j], pl[0], ph[0], pl[1], ph[1], bfr[cl][0], bfr[cl][1]);
+      if constexpr (NB == 8) mma_f16_16816(d[i][j], pl[0], ph[0], pl[1], ph[1], bfr[cl][4], bfr[cl][5]);
+      mma_f16_16816(d[i][j], pl[2], ph[2], pl[3], ph[3], bfr[cl][2], bfr[cl][3]);
+      if constexpr (NB == 8) mma_f16_16816(d[i][j], pl[2], ph[2], pl[3], ph[3], bfr[cl][6], bfr[cl][7]);
+    }
     if (((cl + 1) & (gc - 1)) == 0) {  // end of a quantization group
       const int grp = c / gc;
-      float slo, shi;
-      if constexpr (SMEM) {
-        slo = lds_half_as_float((uint32_t)(sbase + ((uintptr_t)g * s_stride + grp) * 2));
-        shi = lds_half_as_float((uint32_t)(sbase + ((uintptr_t)(g + 8) * s_stride + grp) * 2));
-      } else {
-        slo = ldg_half_as_float(reinterpret_cast<const uint16_t*>(sbase) + (size_t)g * s_stride + grp);
-        shi = ldg_half_as_float(reinterpret_cast<const uint16_t*>(sbase) + (size_t)(g + 8) * s_stride + grp);
+#pragma unroll
+      for (int i = 0; i < kTiles; ++i) {
+        const size_t e_lo = (size_t)(16 * i + g) * s_stride + grp;
+        const size_t e_hi = e_lo + (size_t)8 * s_stride;
+        float slo, shi;
+        if constexpr (SMEM) {
+          slo = __half2float(__ushort_as_half(sbase[e_lo]));
+          shi = __half2float(__ushort_as_half(sbase[e_hi]));
+        } else {
+          slo = ldg_half_as_float(sbase + e_lo);
+          shi = ldg_half_as_float(sbase + e_hi);
+        }
+        float v[4];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          v[q] = d[i][0][q];
+#pragma unroll
+          for (int jj = 1; jj < kAcc; ++jj) v[q] += d[i][jj][q];
+        }
+        acc[i][0] = fmaf(slo, v[0], acc[i][0]);
+        acc[i][1] = fmaf(slo, v[1], acc[i][1]);
+        acc[i][2] = fmaf(shi, v[2], acc[i][2]);
+        acc[i][3] = fmaf(shi, v[3], acc[i][3]);
+#pragma unroll
+        for (int jj = 0; jj < kAcc; ++jj) d[i][jj][0] = d[i][jj][1] = d[i][jj][2] = d[i][jj][3] = 0.f;
       }
-      acc[0] = fmaf(slo, d[0], acc[0]);
-      acc[1] = fmaf(slo, d[1], acc[1]);
-      acc[2] = fmaf(shi, d[2], acc[2]);
-      acc[3] = fmaf(shi, d[3], acc[3]);
-      d[0] = d[1] = d[2] = d[3] = 0.f;
     }
   }
 }
@@ -185,49 +197,20 @@ __device__ __forceinline__ void load_x_frags(const FfnParams& p, int c0, int g, 
   }
 }
 
-__device__ __forceinline__ float silu_f32(float z) { return z / (1.0f + expf(-z)); }
-
-// Activation operand for down: h = silu(g) * u for intermediate features
-// 32c + 8t .. +7 of token column g, from the gate/up workspace of active
-// index a, split into fp16 high parts (slots 0..3) and remainders (4..7).
+// Activation operand for down: the fragments the gate/up kernel stored.
 template <int CPW>
-__device__ __forceinline__ void load_h_frags(const FfnParams& p, int a, int c0, int g, int t, uint32_t (&bfr)[CPW][8]) {
-  const float* gb = p.gu + ((size_t)a * kTok + g) * (2 * p.I);
+__device__ __forceinline__ void load_h_frags(const FfnParams& p, int a, int c0, int lane, uint32_t (&bfr)[CPW][8]) {
+  const int nch = p.I / 32;
 #pragma unroll
   for (int cl = 0; cl < CPW; ++cl) {
-    const int f0 = (c0 + cl) * 32 + t * 8;
-    const int gate_row = 32 * (f0 / 16) + (f0 % 16);
-    const float4 ga = *reinterpret_cast<const float4*>(gb + gate_row);
-    const float4 gb4 = *reinterpret_cast<const float4*>(gb + gate_row + 4);
-    const float4 ua = *reinterpret_cast<const float4*>(gb + gate_row + 16);
-    const float4 ub4 = *reinterpret_cast<const float4*>(gb + gate_row + 20);
-    const float gv[8] = {ga.x, ga.y, ga.z, ga.w, gb4.x, gb4.y, gb4.z, gb4.w};
-    const float uv[8] = {ua.x, ua.y, ua.z, ua.w, ub4.x, ub4.y, ub4.z, ub4.w};
-    float hi[8], lo[8];
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      const float h = silu_f32(gv[i]) * uv[i];
-      const __half hh = __float2half_rn(h);
-      hi[i] = __half2float(hh);
-      lo[i] = h - hi[i];
-    }
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      bfr[cl][j] = pack_half2(hi[j], hi[j + 4]);
-      bfr[cl][4 + j] = pack_half2(lo[j], lo[j + 4]);
-    }
+    const uint4* src = reinterpret_cast<const uint4*>(p.hfrag + (((size_t)a * nch + c0 + cl) * 32 + lane) * 16);
+    const uint4 v0 = src[0], v1 = src[1];
+    bfr[cl][0] = v0.x; bfr[cl][1] = v0.y; bfr[cl][2] = v0.z; bfr[cl][3] = v0.w;
+    bfr[cl][4] = v1.x; bfr[cl][5] = v1.y; bfr[cl][6] = v1.z; bfr[cl][7] = v1.w;
   }
 }
 
-// Output row of expert_out for token n of the unit's expert, or -1.
-__device__ __forceinline__ int output_row(const FfnParams& p, const Unit& un, int n_act, int n) {
-  if (n >= p.T) return -1;
-  if (un.a >= n_act) return p.T * p.k + n;  // shared expert
-  const int lo = __ldg(p.offsets + un.e), hi = __ldg(p.offsets + un.e + 1);
-  for (int q = lo; q < hi; ++q)
-    if (__ldg(p.perm + q) / p.k == n) return q;
-  return -1;
-}
+__device__ __forceinline__ float silu_f32(float z) { return z / (1.0f + expf(-z)); }
 
 template <int MODE, int CPW>
 __global__ void __launch_bounds__(kThreads, 1) ffn_decode_kernel(const FfnParams p) {
@@ -235,8 +218,9 @@ __global__ void __launch_bounds__(kThreads, 1) ffn_decode_kernel(const FfnParams
   extern __shared__ __align__(128) uint8_t smem[];
   int n_act = *p.n_active;
   n_act = n_act < 0 ? 0 : (n_act > p.amax ? p.amax : n_act);
-  const int units_per_exp = p.n_out / kRows;
-  const int U = (n_act + 1) * units_per_exp;
+  const int ngroups = n_act + 1;
+  const int upe = p.n_out / kRows;                 // units per expert
+  const int U = ngroups * upe;
   const int ub = (int)((long long)blockIdx.x * U / gridDim.x);
   const int ue = (int)((long long)(blockIdx.x + 1) * U / gridDim.x);
   if (ub >= ue) return;
@@ -245,36 +229,77 @@ __global__ void __launch_bounds__(kThreads, 1) ffn_decode_kernel(const FfnParams
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + (size_t)p.nstage * p.stage_bytes);
   uint64_t* empty = full + p.nstage;
   float* red = reinterpret_cast<float*>(empty + p.nstage);
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(red + 2 * kNW * kRedWarp);
+  Group* groups = reinterpret_cast<Group*>(red + 2 * kNW * kRedWarp);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(groups + kMaxGroups);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  if (threadIdx.x == 0) {
+  const int tid = threadIdx.x;
+  // Only the groups this CTA's units touch are needed; filling all is cheap.
+  for (int a = tid; a < ngroups; a += blockDim.x) {
+    Group gr;
+    gr.e = a < n_act ? __ldg(p.active + a) : p.E;
+    gr.w = nullptr;
+    gr.s = nullptr;
+    gr.flags = 0;
+    if (gr.e >= 0 && gr.e <= p.E) {
+      const qre_slot* sl = p.slots + gr.e;
+      gr.w = MODE == 0 ? sl->w_gate_up : sl->w_down;
+      gr.s = MODE == 0 ? sl->s_gate_up : sl->s_down;
+      const bool ok = gr.w && gr.s &&
+                      ((reinterpret_cast<uintptr_t>(gr.w) | reinterpret_cast<uintptr_t>(gr.s)) & 15) == 0;
+      gr.flags = (ok ? 1 : 0) | (sl->tier != 0 ? 2 : 0);
+    }
+    Group& dst = groups[a];
+    dst.w = gr.w;
+    dst.s = gr.s;
+    dst.e = gr.e;
+    dst.flags = gr.flags;
+#pragma unroll
+    for (int n = 0; n < kTok; ++n) dst.outq[n] = (MODE == 1 && a == n_act && n < p.T) ? p.T * p.k + n : -1;
+    if (MODE == 1 && a < n_act && (gr.flags & 1)) {
+      const int lo = __ldg(p.offsets + gr.e), hi = __ldg(p.offsets + gr.e + 1);
+      for (int q = lo; q < hi && q < lo + kTok; ++q) {
+        const int tk = __ldg(p.perm + q) / p.k;
+        if (tk >= 0 && tk < kTok) dst.outq[tk] = q;
+      }
+    }
+  }
+  if (tid == 0) {
     for (int s = 0; s < p.nstage; ++s) {
       mbar_init(&full[s], 1);
-      mbar_init(&empty[s], p.aw);
+      mbar_init(&empty[s], p.aw / p.nparts);
     }
     *abort_flag = 0;
     fence_barrier_init();
   }
   __syncthreads();
 
+  const int part_chunks = (p.K / 32) / p.nparts;
+  const uint32_t scale_bytes = kRows * (p.K / p.G) * 2;
+
   if (warp == kNW) {
-    // ---------------- producer: one thread issues the bulk copies
+    // ---------------- producer: one thread issues the bulk copies, part by part
     if (lane == 0) {
-      const uint32_t row_bytes = p.K / 2;
-      const uint32_t scale_bytes = kRows * (p.K / p.G) * 2;
+      const size_t row_bytes = p.K / 2;
       int it = 0;
       for (int u = ub; u < ue; ++u) {
-        const Unit un = resolve_unit<MODE>(p, u, n_act, units_per_exp);
-        if (!un.ok || un.host) continue;
-        const int s = it % p.nstage;
-        const uint32_t par = ((it / p.nstage) & 1) ^ 1;
-        if (!mbar_wait_bounded(&empty[s], par, abort_flag, p.status)) break;
-        uint8_t* dst = stages + (size_t)s * p.stage_bytes;
-        mbar_arrive_expect_tx(&full[s], kRows * row_bytes + scale_bytes);
-        for (int r = 0; r < kRows; ++r) bulk_copy_g2s(dst + r * p.pitch, un.w + (size_t)r * row_bytes, row_bytes, &full[s]);
-        bulk_copy_g2s(dst + kRows * p.pitch, un.s, scale_bytes, &full[s]);
-        ++it;
+        const int a = u / upe, r0 = (u - a * upe) * kRows;
+        const Group& gr = groups[a];
+        if ((gr.flags & 3) != 1) continue;   // skipped or host-resident
+        bool stop = false;
+        for (int part = 0; part < p.nparts; ++part, ++it) {
+          const int s = it % p.nstage;
+          if (!mbar_wait_bounded(&empty[s], ((it / p.nstage) & 1) ^ 1, abort_flag, p.status)) {
+            stop = true;
+            break;
+          }
+          uint8_t* dst = stages + (size_t)s * p.stage_bytes;
+          const uint8_t* src = gr.w + (size_t)r0 * row_bytes + (size_t)part * p.part_bytes;
+          mbar_arrive_expect_tx(&full[s], kRows * p.part_bytes + scale_bytes);
+          for (int r = 0; r < kRows; ++r) bulk_copy_g2s(dst + r * p.pitch, src + r * row_bytes, p.part_bytes, &full[s]);
+          bulk_copy_g2s(dst + kRows * p.pitch, gr.s + (size_t)r0 * (p.K / p.G), scale_bytes, &full[s]);
+        }
+        if (stop) break;
       }
       // Every issued copy must land before the CTA exits (also after an abort).
       const int first = it > p.nstage ? it - p.nstage : 0;
@@ -286,56 +311,88 @@ __global__ void __launch_bounds__(kThreads, 1) ffn_decode_kernel(const FfnParams
 
   // ---------------- consumers
   const int g = lane >> 2, t = lane & 3;
-  const int tid = threadIdx.x;
   const bool working = warp < p.aw;
   const int c0 = warp * CPW;
+  const int wpart = working ? warp / (p.aw / p.nparts) : 0;
   uint32_t bfr[CPW][NB];
   if constexpr (MODE == 0) {
     if (working) load_x_frags<CPW>(p, c0, g, t, bfr);
   }
-  int cur_a = -1, myq = -1, it = 0, buf = 0;
+  int cur_a = -1, units0 = 0, buf = 0;
   for (int u = ub; u < ue; ++u) {
-    const Unit un = resolve_unit<MODE>(p, u, n_act, units_per_exp);
-    if (!un.ok) {
+    const int a = u / upe, r0 = (u - a * upe) * kRows;
+    const Group& gr = groups[a];
+    if (!(gr.flags & 1)) {
       if (tid == 0) set_status(p.status, QRE_DEV_NULL_SLOT);
       continue;
     }
-    if (un.a != cur_a) {
-      cur_a = un.a;
-      if constexpr (MODE == 1) {
-        if (working) load_h_frags<CPW>(p, un.a, c0, g, t, bfr);
-        if (tid < kRows * kTok) myq = output_row(p, un, n_act, tid / kRows);
-      }
+    const bool host = gr.flags & 2;
+    if constexpr (MODE == 1) {
+      if (a != cur_a && working) load_h_frags<CPW>(p, a, c0, lane, bfr);
     }
+    cur_a = a;
     if (working) {
-      float acc[4] = {0.f, 0.f, 0.f, 0.f};
-      if (!un.host) {
+      float acc[kTiles][4];
+#pragma unroll
+      for (int i = 0; i < kTiles; ++i) acc[i][0] = acc[i][1] = acc[i][2] = acc[i][3] = 0.f;
+      if (!host) {
+        const int it = units0 * p.nparts + wpart;
         const int s = it % p.nstage;
         const bool have = mbar_wait_bounded(&full[s], (it / p.nstage) & 1, abort_flag, p.status);
-        const uint32_t wb = smem_addr(stages + (size_t)s * p.stage_bytes);
-        if (have) unit_dot<CPW, NB, true>(wb, p.pitch, wb + kRows * p.pitch, p.K / p.G, c0, p.gc, g, t, bfr, acc);
+        const uint8_t* wb = stages + (size_t)s * p.stage_bytes;
+        if (have)
+          unit_dot<CPW, NB, true>(wb, p.pitch, reinterpret_cast<const uint16_t*>(wb + kRows * p.pitch), p.K / p.G,
+                                  c0, wpart * part_chunks, p.gc, g, t, bfr, acc);
         __syncwarp();
         if (lane == 0) mbar_arrive(&empty[s]);
       } else {
-        unit_dot<CPW, NB, false>(reinterpret_cast<uintptr_t>(un.w), p.K / 2, reinterpret_cast<uintptr_t>(un.s),
-                                 p.K / p.G, c0, p.gc, g, t, bfr, acc);
+        unit_dot<CPW, NB, false>(gr.w + (size_t)r0 * (p.K / 2), p.K / 2, gr.s + (size_t)r0 * (p.K / p.G), p.K / p.G,
+                                 c0, 0, p.gc, g, t, bfr, acc);
       }
       float* rw = red + (size_t)(buf * kNW + warp) * kRedWarp;
-      rw[(2 * t) * kRedStride + g] = acc[0];
-      rw[(2 * t + 1) * kRedStride + g] = acc[1];
-      rw[(2 * t) * kRedStride + g + 8] = acc[2];
-      rw[(2 * t + 1) * kRedStride + g + 8] = acc[3];
+#pragma unroll
+      for (int i = 0; i < kTiles; ++i) {
+        rw[i * kRedTile + (2 * t) * kRedStride + g] = acc[i][0];
+        rw[i * kRedTile + (2 * t + 1) * kRedStride + g] = acc[i][1];
+        rw[i * kRedTile + (2 * t) * kRedStride + g + 8] = acc[i][2];
+        rw[i * kRedTile + (2 * t + 1) * kRedStride + g + 8] = acc[i][3];
+      }
     }
-    if (!un.host) ++it;
+    if (!host) ++units0;
     named_barrier_sync(1, kNW * 32);
-    if (tid < kRows * kTok) {
-      const int n = tid / kRows, r = tid % kRows;
-      float v = 0.f;
-      for (int w = 0; w < p.aw; ++w) v += red[(size_t)(buf * kNW + w) * kRedWarp + n * kRedStride + r];
-      if (MODE == 0) {
-        p.gu[((size_t)un.a * kTok + n) * (2 * p.I) + un.r0 + r] = v;
-      } else if (myq >= 0) {
-        p.expert_out[(size_t)myq * p.H + un.r0 + r] = v;
+    const float* rb = red + (size_t)buf * kNW * kRedWarp;
+    if constexpr (MODE == 0) {
+      if (tid < 16 * kTok) {
+        // gate row r and up row r of token n -> h = silu(g) * u, stored as the
+        // down kernel's B fragment: feature f = r0/2 + r of chunk f/32, lane
+        // 4n + (f%32)/8, pair (f%8)%4, half (f%8)/4; high part then remainder.
+        const int n = tid >> 4, r = tid & 15;
+        float gs = 0.f, us = 0.f;
+#pragma unroll
+        for (int w = 0; w < kNW; ++w) {
+          if (w < p.aw) {
+            gs += rb[w * kRedWarp + n * kRedStride + r];
+            us += rb[w * kRedWarp + kRedTile + n * kRedStride + r];
+          }
+        }
+        const float h = silu_f32(gs) * us;
+        const __half hh = __float2half_rn(h);
+        const __half hl = __float2half_rn(h - __half2float(hh));
+        const int f = r0 / 2 + r;
+        const int c = f >> 5, tt = (f & 31) >> 3, i8 = f & 7;
+        const size_t base = (((size_t)a * (p.I / 32) + c) * 32 + (4 * n + tt)) * 16;
+        p.hfrag[base + (i8 & 3) * 2 + (i8 >> 2)] = __half_as_ushort(hh);
+        p.hfrag[base + (4 + (i8 & 3)) * 2 + (i8 >> 2)] = __half_as_ushort(hl);
+      }
+    } else {
+      if (tid < kTiles * 16 * kTok) {
+        const int i = tid >> 7, n = (tid >> 4) & 7, r = tid & 15;
+        float v = 0.f;
+#pragma unroll
+        for (int w = 0; w < kNW; ++w)
+          if (w < p.aw) v += rb[w * kRedWarp + i * kRedTile + n * kRedStride + r];
+        const int q = gr.outq[n];
+        if (q >= 0) p.expert_out[(size_t)q * p.H + r0 + 16 * i + r] = v;
       }
     }
     buf ^= 1;
@@ -343,7 +400,7 @@ __global__ void __launch_bounds__(kThreads, 1) ffn_decode_kernel(const FfnParams
 }
 
 struct Plan {
-  int cpw = 0, aw = 0, gc = 0, pitch = 0, stage_bytes = 0, nstage = 0;
+  int cpw = 0, aw = 0, gc = 0, nparts = 1, pitch = 0, part_bytes = 0, stage_bytes = 0, nstage = 0;
   size_t smem = 0;
   bool ok = false;
 };
@@ -359,10 +416,12 @@ Plan make_plan(int K, int G, int smem_budget) {
   }
   if (!pl.cpw) return pl;
   pl.aw = nchunks / pl.cpw;
-  pl.pitch = ((K / 2 + 127) / 128) * 128 + 16;
+  pl.nparts = (pl.aw % 2 == 0) ? 2 : 1;
+  pl.part_bytes = K / 2 / pl.nparts;
+  pl.pitch = ((pl.part_bytes + 127) / 128) * 128 + 16;
   pl.stage_bytes = kRows * pl.pitch + kRows * (K / G) * 2;
   pl.stage_bytes = (pl.stage_bytes + 127) / 128 * 128;
-  const int fixed = 2 * kNW * kRedWarp * 4 + 16;
+  const int fixed = 2 * kNW * kRedWarp * 4 + kMaxGroups * (int)sizeof(Group) + 16;
   int ns = (smem_budget - fixed) / (pl.stage_bytes + 16);
   if (ns > 8) ns = 8;
   if (ns < 2) return pl;
@@ -377,7 +436,9 @@ cudaError_t launch_mode(const FfnParams& base, const Plan& pl, int grid, cudaStr
   FfnParams p = base;
   p.gc = pl.gc;
   p.aw = pl.aw;
+  p.nparts = pl.nparts;
   p.pitch = pl.pitch;
+  p.part_bytes = pl.part_bytes;
   p.stage_bytes = pl.stage_bytes;
   p.nstage = pl.nstage;
   void (*kern)(const FfnParams) = nullptr;
@@ -404,7 +465,7 @@ bool ffn_decode_supported(const qre_layer_shape& s) {
 size_t ffn_ws_bytes(const qre_layer_shape& s, int T) {
   const long long pk = (long long)T * s.top_k;
   const long long amax = pk < s.n_experts ? pk : s.n_experts;
-  return (size_t)(amax + 1) * kTok * 2 * s.inter * sizeof(float);
+  return (size_t)(amax + 1) * (s.inter / 32) * 32 * 16 * sizeof(uint16_t);
 }
 
 cudaError_t launch_ffn_decode(const qre_layer_shape& s, int T, const uint16_t* x, const qre_slot* slots,
@@ -428,7 +489,7 @@ cudaError_t launch_ffn_decode(const qre_layer_shape& s, int T, const uint16_t* x
   p.perm = perm;
   p.active = active;
   p.n_active = n_active;
-  p.gu = static_cast<float*>(ws);
+  p.hfrag = static_cast<uint16_t*>(ws);
   p.expert_out = expert_out;
   p.status = status;
   const long long pk = (long long)T * s.top_k;

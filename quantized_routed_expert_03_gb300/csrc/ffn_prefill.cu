@@ -21,10 +21,11 @@
 //   warp 0      TMA loads of the token operand (128-byte swizzle) into a 4-stage ring
 //   warp 1      allocates 512 TMEM columns (two 128x256 fp32 accumulators) and
 //               issues tcgen05.mma (M=128, N<=256, K=16) from one thread
-//   warps 2-5   dequantize the weight operand: one thread per row decodes 64
-//               nibbles per stage, multiplies by the group scale in fp16 and
-//               stores the 128-byte swizzled rows the MMA expects
-//   warps 6-9   epilogue: tcgen05.ld of the finished accumulator while the MMA
+//   warps 2-9   dequantize the weight operand: two threads per row each decode
+//               32 nibbles per stage (words and scales prefetched four stages
+//               ahead), multiply by the group scale in fp16 and store the
+//               128-byte swizzled rows the MMA expects
+//   warps 10-13 epilogue: tcgen05.ld of the finished accumulator while the MMA
 //               warp fills the other one
 // Operands are fp16 (x bf16 -> fp16 is exact in fp16's normal range; dequantized
 // weights and h are rounded to fp16), accumulation fp32.
@@ -41,7 +42,8 @@ constexpr int BK = 64;                  // reduction elements per stage: one 128
 constexpr int NSTAGE = 4;
 constexpr int A_STAGE = BM * BK * 2;    // 16 KB
 constexpr int B_STAGE = BN * BK * 2;    // 32 KB
-constexpr int kWarps = 10;
+constexpr int kWarps = 14;          // 0 TMA, 1 MMA, 2-9 dequant, 10-13 epilogue
+constexpr int kDqThreads = 256;
 constexpr int kThreads = kWarps * 32;
 constexpr int kTmemCols = 512;
 constexpr int kAccCols = 256;
@@ -214,7 +216,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_gemm_kernel(const Prefill
   }
   if (threadIdx.x == 32) {
     for (int s = 0; s < NSTAGE; ++s) {
-      mbar_init(&full_a[s], 128);
+      mbar_init(&full_a[s], kDqThreads);
       mbar_init(&full_b[s], 1);
       mbar_init(&empty[s], 1);
     }
@@ -290,9 +292,11 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_gemm_kernel(const Prefill
       // TMEM is freed below: every MMA issued here must have completed first
       if (last >= 0) mbar_wait_bounded(&acc_full[last & 1], (last >> 1) & 1, nullptr, p.status);
     }
-  } else if (warp < 6) {
+  } else if (warp < 10) {
     // ---------------- weight operand: dequantize into the swizzled stage
-    const int r = threadIdx.x - 64;  // row within the tile, 0..127
+    const int dq = threadIdx.x - 64;        // 0..255
+    const int r = dq & 127;                 // row within the tile
+    const int hf = dq >> 7;                 // which 32 of the stage's 64 reduction elements
     const int sw = r & 7;
     const uint32_t row_off = (uint32_t)(r >> 3) * 1024 + (uint32_t)sw * 128;
     int it = 0;
@@ -303,17 +307,20 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_gemm_kernel(const Prefill
       const uint8_t* wb = MODE == 0 ? sl->w_gate_up : sl->w_down;
       const uint16_t* sb = MODE == 0 ? sl->s_gate_up : sl->s_down;
       const bool valid = wb && sb && ((reinterpret_cast<uintptr_t>(wb) | reinterpret_cast<uintptr_t>(sb)) & 15) == 0;
-      if (!valid && r == 0) set_status(p.status, QRE_DEV_NULL_SLOT);
-      const uint4* wrow = valid ? reinterpret_cast<const uint4*>(wb + (size_t)(tl.m0 + r) * (p.K / 2)) : nullptr;
+      if (!valid && dq == 0) set_status(p.status, QRE_DEV_NULL_SLOT);
+      // 16 bytes (32 nibbles) of row m0 + r per stage, and the scale of its group
+      const uint4* wrow = valid ? reinterpret_cast<const uint4*>(wb + (size_t)(tl.m0 + r) * (p.K / 2)) + hf : nullptr;
       const uint16_t* srow = valid ? sb + (size_t)(tl.m0 + r) * KG : nullptr;
-      uint4 ring[4][2];
+      uint4 ring[4];
+      unsigned short sring[4];
 #pragma unroll
       for (int j = 0; j < 4; ++j) {
         if (valid && j < KB) {
-          ring[j][0] = __ldg(wrow + 2 * j);
-          ring[j][1] = __ldg(wrow + 2 * j + 1);
+          ring[j] = __ldg(wrow + 2 * j);
+          sring[j] = __ldg(reinterpret_cast<const unsigned short*>(srow) + (j * BK + 32 * hf) / p.G);
         } else {
-          ring[j][0] = ring[j][1] = make_uint4(0x88888888u, 0x88888888u, 0x88888888u, 0x88888888u);
+          ring[j] = make_uint4(0x88888888u, 0x88888888u, 0x88888888u, 0x88888888u);
+          sring[j] = 0;
         }
       }
       for (int kb0 = 0; kb0 < KB; kb0 += 4) {
@@ -324,27 +331,21 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_gemm_kernel(const Prefill
             const int s = it % NSTAGE;
             const bool go = mbar_wait_bounded(&empty[s], ((it / NSTAGE) & 1) ^ 1, abort_flag, p.status);
             if (go) {
-              float sa = 0.f, sbv = 0.f;
-              if (valid) {
-                sa = __half2float(__ushort_as_half(__ldg(srow + (kb * BK) / p.G)));
-                sbv = __half2float(__ushort_as_half(__ldg(srow + (kb * BK + 32) / p.G)));
-              }
-              const __half2 s2a = __float2half2_rn(sa), s2b = __float2half2_rn(sbv);
-              const uint32_t words[8] = {ring[j][0].x, ring[j][0].y, ring[j][0].z, ring[j][0].w,
-                                         ring[j][1].x, ring[j][1].y, ring[j][1].z, ring[j][1].w};
+              const __half2 s2 = __half2half2(__ushort_as_half(sring[j]));
+              const uint32_t words[4] = {ring[j].x, ring[j].y, ring[j].z, ring[j].w};
               uint8_t* stage = As + (size_t)s * A_STAGE + row_off;
 #pragma unroll
-              for (int c = 0; c < 8; ++c) {
-                const uint4 v = dequant8(words[c], c < 4 ? s2a : s2b);
-                *reinterpret_cast<uint4*>(stage + ((c ^ sw) << 4)) = v;
+              for (int c = 0; c < 4; ++c) {
+                const uint4 v = dequant8(words[c], s2);
+                *reinterpret_cast<uint4*>(stage + (((4 * hf + c) ^ sw) << 4)) = v;
               }
               fence_proxy_async_smem();
             }
             mbar_arrive(&full_a[s]);
             ++it;
             if (valid && kb + 4 < KB) {
-              ring[j][0] = __ldg(wrow + 2 * (kb + 4));
-              ring[j][1] = __ldg(wrow + 2 * (kb + 4) + 1);
+              ring[j] = __ldg(wrow + 2 * (kb + 4));
+              sring[j] = __ldg(reinterpret_cast<const unsigned short*>(srow) + ((kb + 4) * BK + 32 * hf) / p.G);
             }
           }
         }

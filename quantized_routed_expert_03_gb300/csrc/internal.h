@@ -57,6 +57,14 @@ cudaError_t launch_ffn_prefill(const qre_layer_shape& s, int T, const uint16_t* 
                                const int32_t* n_active, float* expert_out, void* ws, int* status,
                                cudaStream_t stream);
 
+cudaError_t launch_cache_update(int E, int S, float decay, const int32_t* active, const int32_t* n_active,
+                                float* scores, int32_t* slot_expert, int32_t* expert_slot, const qre_slot* home,
+                                const qre_slot* slot_mem, qre_slot* table, int32_t* copy_list, int32_t* n_copies,
+                                int max_copies, int* status, cudaStream_t stream);
+cudaError_t launch_cache_copy(const qre_layer_shape& s, const qre_slot* home, const qre_slot* slot_mem,
+                              const int32_t* copy_list, const int32_t* n_copies, int max_copies,
+                              cudaStream_t stream);
+
 cudaError_t launch_combine(const qre_layer_shape& s, int T, const float* expert_out, const float* topk_w,
                            const int32_t* inv_perm, float* y_f32, uint16_t* y_bf16, cudaStream_t stream);
 

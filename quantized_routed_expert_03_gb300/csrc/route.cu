@@ -9,8 +9,10 @@
 //   * T <= 16 (decode): a GEMV that streams W_r once; each CTA owns two expert
 //     rows and keeps all T tokens' partial sums in registers.
 //   * T > 16 (prefill): a tiled fp32 GEMM (64 tokens x 64 experts per CTA).
-// Both accumulate in a fixed order, so results are deterministic.  A warp per
-// token then does the selection.
+// Both accumulate in a fixed order, so results are deterministic.  Selection:
+// for T <= 64 one CTA per token ranks every expert against all others in
+// parallel; for larger T one warp per token runs k rounds of arg-max.  Both
+// give the same bits (same fp32 scores, same exact order, same summation).
 #include "common.cuh"
 #include "internal.h"
 
@@ -32,9 +34,17 @@ __global__ void __launch_bounds__(256) route_logits_gemv(int T, int H, int E, co
   for (int t = 0; t < TMAX; ++t) acc[t] = 0.f;
   if (e < E) {
     const float* w = W + (size_t)e * H;
-#pragma unroll 4
-    for (int j = c * 4; j < H; j += 512) {
-      const float4 wv = __ldg(reinterpret_cast<const float4*>(w + j));
+    float4 wbuf[8];
+#pragma unroll
+    for (int m = 0; m < 8; ++m) {   // all of this thread's weights in flight at once
+      const int j = c * 4 + m * 512;
+      wbuf[m] = j < H ? __ldg(reinterpret_cast<const float4*>(w + j)) : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+#pragma unroll
+    for (int m = 0; m < 8; ++m) {
+      const int j = c * 4 + m * 512;
+      if (j >= H) break;
+      const float4 wv = wbuf[m];
 #pragma unroll
       for (int t = 0; t < TMAX; ++t) {
         if (t < T) {
@@ -221,6 +231,54 @@ __global__ void __launch_bounds__(kSelWarps * 32) route_select(int T, int E, int
   }
 }
 
+// One CTA per token (small T): every expert computes its rank in the order
+// (selection score descending, id ascending) against all others; the k experts
+// of rank < k are compacted in ascending id with a block-wide prefix count.
+__global__ void __launch_bounds__(1024) route_select_rank(int T, int E, int k, const float* __restrict__ logits,
+                                                          const float* __restrict__ bias, int32_t* __restrict__ idx,
+                                                          float* __restrict__ wout) {
+  __shared__ float sel_s[1024];
+  __shared__ int wcount[32];
+  __shared__ int chosen[16];
+  __shared__ float chosen_s[16];
+  const int t = blockIdx.x, e = threadIdx.x, lane = e & 31, warp = e >> 5;
+  float sc = 0.f, my = -INFINITY;
+  if (e < E) {
+    sc = 1.0f / (1.0f + expf(-logits[(size_t)t * E + e]));
+    my = bias ? sc + bias[e] : sc;
+    sel_s[e] = my;
+  }
+  __syncthreads();
+  int rank = 0;
+  if (e < E) {
+    for (int j = 0; j < E; ++j) {
+      const float v = sel_s[j];
+      rank += (v > my || (v == my && j < e)) ? 1 : 0;
+    }
+  }
+  const bool pick = e < E && rank < k;
+  const unsigned bal = __ballot_sync(0xffffffffu, pick);
+  if (lane == 0) wcount[warp] = __popc(bal);
+  __syncthreads();
+  if (pick) {
+    int pos = __popc(bal & ((1u << lane) - 1u));
+    for (int w = 0; w < warp; ++w) pos += wcount[w];
+    if (pos < 16) {
+      chosen[pos] = e;
+      chosen_s[pos] = sc;
+    }
+  }
+  __syncthreads();
+  if (e == 0) {
+    float tot = 0.f;
+    for (int j = 0; j < k; ++j) tot += chosen_s[j];
+    for (int j = 0; j < k; ++j) {
+      idx[(size_t)t * k + j] = chosen[j];
+      wout[(size_t)t * k + j] = chosen_s[j] / tot;
+    }
+  }
+}
+
 }  // namespace
 
 size_t route_ws_bytes(const qre_layer_shape& s, int T) { return (size_t)T * s.n_experts * sizeof(float); }
@@ -239,8 +297,12 @@ cudaError_t launch_route(const qre_layer_shape& s, int T, const uint16_t* x, con
   }
   cudaError_t err = cudaGetLastError();
   if (err != cudaSuccess) return err;
-  route_select<<<(T + kSelWarps - 1) / kSelWarps, kSelWarps * 32, 0, stream>>>(T, E, s.top_k, logits, bias,
-                                                                              topk_idx, topk_w);
+  if (T <= 64) {
+    route_select_rank<<<T, ((E + 31) / 32) * 32, 0, stream>>>(T, E, s.top_k, logits, bias, topk_idx, topk_w);
+  } else {
+    route_select<<<(T + kSelWarps - 1) / kSelWarps, kSelWarps * 32, 0, stream>>>(T, E, s.top_k, logits, bias,
+                                                                                topk_idx, topk_w);
+  }
   return cudaGetLastError();
 }
 

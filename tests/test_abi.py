@@ -134,3 +134,15 @@ def test_validate_slots_host_checks(lib):
     arr[1].reserved = 5
     st, msg = _status(lambda: qre.qre_validate_slots(s, arr))
     assert st == qre.QRE_ERR_INVALID_ARG and "reserved" in msg
+
+
+def test_cache_argument_errors(lib):
+    s = _shape()
+    st, msg = _status(lambda: qre.qre_cache_update(s, 0, 0.995, A, A, A, A, A, A, A, A, A, A, 8, stream=0))
+    assert st == qre.QRE_ERR_UNSUPPORTED and "n_slots" in msg
+    st, msg = _status(lambda: qre.qre_cache_update(s, 8, 1.5, A, A, A, A, A, A, A, A, A, A, 8, stream=0))
+    assert st == qre.QRE_ERR_INVALID_ARG and "decay" in msg
+    st, msg = _status(lambda: qre.qre_cache_update(s, 8, 0.995, A, A, A, A, MIS, A, A, A, A, A, 8, stream=0))
+    assert st == qre.QRE_ERR_MISALIGNED and "slot_expert" in msg
+    st, msg = _status(lambda: qre.qre_cache_copy(s, A, None, A, A, 8, stream=0))
+    assert st == qre.QRE_ERR_INVALID_ARG and "slot_mem" in msg

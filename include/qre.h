@@ -177,6 +177,28 @@ QRE_API qre_status qre_route(const qre_layer_shape* shape, int32_t T, const uint
                      qre_stream_t stream);
 
 /*
+ * qre_route without a workspace: the same router and the same results as
+ * qre_route, for callers that cannot allocate device memory -- code that runs
+ * inside a host framework which owns every device allocation, loops that must
+ * not allocate once they run, or callers that only hold the input and output
+ * buffers someone else gave them.  The pages have no counterpart; it is an
+ * interface choice of this library.
+ *   Scratch: a fixed array of 65,536 floats (256 KiB) inside the library, kept
+ *   by every GPU that loads it until the process exits; T * n_experts must be at
+ *   most 65,536 (QRE_ERR_UNSUPPORTED otherwise, nothing launched).
+ *   The first call on each device looks up the array's device address with that
+ *   device current; make that first call before any stream capture.
+ *   Every call shares the array: calls whose kernels may overlap on the GPU race
+ *   and give wrong results; keep them on one stream or otherwise ordered.
+ *   Nothing in the array has to start at zero.  No cudaMalloc, cudaFree or
+ *   allocating library routine is called.
+ * Arguments, layouts and errors are those of qre_route.
+ */
+QRE_API qre_status qre_route_noalloc(const qre_layer_shape* shape, int32_t T, const uint16_t* x_bf16,
+                                     const float* w_router, const float* bias, int32_t* topk_idx,
+                                     float* topk_w, qre_stream_t stream);
+
+/*
  * Dispatch: deduplicate the picks into the expert union that all tokens share
  * (glm53-flash-offload README, "Elastic CLOCK expert cache": a one-block kernel
  * dedups the router picks; "Batched decode": streams share the per-layer expert

@@ -40,7 +40,7 @@ EXPORTS = (
     "qre_quantize_gate_up",
     "qre_route", "qre_dispatch", "qre_expert_ffn", "qre_combine", "qre_validate_slots",
     "qre_cache_update", "qre_cache_copy",
-    "qre_read_device_status", "qre_clear_device_status",
+    "qre_read_device_status", "qre_clear_device_status", "qre_route_noalloc",
 )
 
 
@@ -84,6 +84,7 @@ _SIGS = {
     "qre_cache_copy": ([_SHAPE, _VP, _VP, _VP, _VP, _I32, _VP], ctypes.c_int),
     "qre_read_device_status": ([_VP, ctypes.POINTER(ctypes.c_int32)], ctypes.c_int),
     "qre_clear_device_status": ([_VP], ctypes.c_int),
+    "qre_route_noalloc": ([_SHAPE, _I32, _VP, _VP, _VP, _VP, _VP, _VP], ctypes.c_int),
 }
 
 
@@ -171,6 +172,13 @@ def qre_route(shape, T, x_bf16, w_router, bias, topk_idx, topk_w, workspace, wor
     _check(load_library().qre_route(ctypes.byref(shape), T, _ptr(x_bf16), _ptr(w_router), _ptr(bias),
                                     _ptr(topk_idx), _ptr(topk_w), _ptr(workspace),
                                     _nbytes(workspace, workspace_bytes), _stream(stream)), "qre_route")
+
+
+def qre_route_noalloc(shape, T, x_bf16, w_router, bias, topk_idx, topk_w, stream=None) -> None:
+    """qre_route for callers that cannot allocate device memory: the logits scratch
+    is a fixed array inside the library (T * n_experts <= 65,536)."""
+    _check(load_library().qre_route_noalloc(ctypes.byref(shape), T, _ptr(x_bf16), _ptr(w_router), _ptr(bias),
+                                            _ptr(topk_idx), _ptr(topk_w), _stream(stream)), "qre_route_noalloc")
 
 
 def qre_dispatch(shape, T, topk_idx, counts, offsets, perm, inv_perm, active, n_active, workspace,

@@ -37,6 +37,13 @@ __device__ int g_qre_device_status;
 
 namespace qre {
 
+void set_error_message(const char* fmt, ...) {
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(g_err, sizeof(g_err), fmt, ap);
+  va_end(ap);
+}
+
 namespace {
 struct DevCache {
   std::once_flag once;

@@ -19,6 +19,9 @@ size_t route_ws_bytes(const qre_layer_shape& s, int T);
 size_t dispatch_ws_bytes(const qre_layer_shape& s, int T);
 size_t ffn_ws_bytes(const qre_layer_shape& s, int T);
 
+// Sets the calling thread's qre_last_error() message (printf format).
+void set_error_message(const char* fmt, ...);
+
 // Device properties, cached per device.
 int device_sm_count();
 int device_max_smem_optin();

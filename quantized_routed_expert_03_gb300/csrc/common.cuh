@@ -94,6 +94,36 @@ __device__ __forceinline__ void bulk_copy_g2s(void* dst, const void* src, uint32
       : "memory");
 }
 
+// 16-byte asynchronous copy global -> shared (L2 only), and the arrival on an
+// mbarrier once all of this thread's earlier cp.async copies have completed
+// (the barrier's expected count must include this arrival).
+__device__ __forceinline__ void cp_async_16(void* dst, const void* src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_addr(dst)), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_arrive(uint64_t* bar) {
+  asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(smem_addr(bar)) : "memory");
+}
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
+
+// Returns its argument through a volatile instruction: shared-memory loads whose
+// address depends on the result stay after every earlier volatile asm (such as
+// an mbarrier wait) while remaining free to be reordered among themselves.
+__device__ __forceinline__ uint32_t after_wait(uint32_t v) {
+  uint32_t r;
+  asm volatile("mov.b32 %0, %1;" : "=r"(r) : "r"(v));
+  return r;
+}
+__device__ __forceinline__ uint32_t lds32(uint32_t addr) {
+  uint32_t v;
+  asm("ld.shared.u32 %0, [%1];" : "=r"(v) : "r"(addr));
+  return v;
+}
+__device__ __forceinline__ unsigned short lds16(uint32_t addr) {
+  unsigned short v;
+  asm("ld.shared.u16 %0, [%1];" : "=h"(v) : "r"(addr));
+  return v;
+}
+
 // ---------------------------------------------------------------- named barrier
 
 __device__ __forceinline__ void named_barrier_sync(int id, int nthreads) {

@@ -8,14 +8,16 @@
 // and keep every other cost under it.
 //
 // Layout of the work
-//   * A unit is 16 consecutive output rows of one expert's matrix over the full
-//     reduction length K (16 x K/2 bytes of packed weights plus their scales).
+//   * A unit is 32 consecutive output rows of one expert's matrix (for gate/up,
+//     one block of 16 gate rows and the matching 16 up rows) over the full
+//     reduction length K, staged in two K halves ("parts").
 //     Units of all active experts and the shared expert are split into equal
 //     contiguous ranges, one per CTA; one CTA per SM (persistent).
 //   * A producer warp streams each unit from HBM into a ring of shared-memory
-//     stages with one 1-D bulk (TMA) copy per row, completing on an mbarrier.
-//     Rows land at a pitch of 16 mod 128 bytes so the consumers' 32-bit loads are
-//     free of bank conflicts.  Units of host-resident experts (slot tier 1) skip
+//     stages with 1-D bulk (TMA) copies, one row per lane, so a stage's copies
+//     leave in one warp-wide instruction (one thread issuing them one by one was
+//     measured to cap the stream near 2 TB/s), completing on an mbarrier.  Rows land at a pitch of 16 mod 128 bytes so
+//     the consumers' 32-bit loads are free of bank conflicts.  Units of host-resident experts (slot tier 1) skip
 //     the ring: the consumers read them with direct loads over the host link,
 //     as the README's "Zero-copy home" does.
 //   * 16 consumer warps split K; each warp owns a fixed K range, so the
@@ -27,9 +29,10 @@
 //     fp32 per quantization group, and the group's fp16 scale is applied in fp32.
 //     The K order inside a 32-element chunk is permuted identically in weights
 //     and activations, which leaves every dot product unchanged.
-//   * Per unit, the 16 warps' partial sums are added in fixed warp order
-//     (deterministic), and the result goes to the gate/up workspace (gate/up
-//     kernel) or to the expert's output rows (down kernel).
+//   * Per unit, the 16 warps' partial sums go to one of two shared buffers and a
+//     reducer warp adds them in fixed warp order (deterministic) while the
+//     consumers continue with the next unit; the result goes to the gate/up
+//     workspace (gate/up kernel) or to the expert's output rows (down kernel).
 // The down kernel computes h = silu(g) * u from the gate/up workspace while it
 // loads its activation operand, and splits h into an fp16 high part and an fp16
 // remainder so that its products stay accurate to about fp32.
@@ -40,9 +43,12 @@ namespace qre {
 namespace {
 
 constexpr int kNW = 16;                    // consumer warps
-constexpr int kThreads = (kNW + 1) * 32;   // + one producer warp
+constexpr int kProducerWarp = kNW;
+constexpr int kReducerWarp = kNW + 1;
+constexpr int kThreads = (kNW + 2) * 32;   // + one producer warp + one reducer warp
 constexpr int kTiles = 2;                  // MMA M tiles (16 rows each) per unit
 constexpr int kRows = 16 * kTiles;         // rows per unit: one gate block + one up block
+static_assert(kRows == 32, "the producer issues one row copy per lane");
 constexpr int kTok = kDecodeMaxTokens;     // MMA N
 constexpr int kRedStride = 20;             // floats between token columns of a partial
 constexpr int kRedTile = kTok * kRedStride;
@@ -98,8 +104,8 @@ __device__ __forceinline__ float ldg_half_as_float(const uint16_t* p) {
 // when a quantization group ends.
 constexpr int kAcc = 2;
 template <int CPW, int NB, bool SMEM>
-__device__ __forceinline__ void unit_dot(const uint8_t* wbase, int wpitch, const uint16_t* sbase, int s_stride,
-                                         int c0, int cbase, int gc, int g, int t,
+__device__ __forceinline__ void unit_dot(const uint8_t* wbase, uint32_t wbase_s, int wpitch, const uint16_t* sbase,
+                                         uint32_t sbase_s, int s_stride, int c0, int cbase, int gc, int g, int t,
                                          const uint32_t (&bfr)[CPW][NB], float (&acc)[kTiles][4]) {
   float d[kTiles][kAcc][4];
 #pragma unroll
@@ -120,14 +126,14 @@ __device__ __forceinline__ void unit_dot(const uint8_t* wbase, int wpitch, const
         const int col = (c + u - cbase) * 16 + t * 4;
 #pragma unroll
         for (int i = 0; i < kTiles; ++i) {
-          const uint8_t* r_lo = wbase + (size_t)(16 * i + g) * wpitch + col;
-          const uint8_t* r_hi = r_lo + (size_t)8 * wpitch;
           if constexpr (SMEM) {
-            wv[u][i][0] = *reinterpret_cast<const uint32_t*>(r_lo);
-            wv[u][i][1] = *reinterpret_cast<const uint32_t*>(r_hi);
+            const uint32_t a_lo = wbase_s + (uint32_t)((16 * i + g) * wpitch + col);
+            wv[u][i][0] = lds32(a_lo);
+            wv[u][i][1] = lds32(a_lo + 8 * wpitch);
           } else {
+            const uint8_t* r_lo = wbase + (size_t)(16 * i + g) * wpitch + col;
             wv[u][i][0] = ldg_u32(r_lo);
-            wv[u][i][1] = ldg_u32(r_hi);
+            wv[u][i][1] = ldg_u32(r_lo + (size_t)8 * wpitch);
           }
         }
       }
@@ -151,8 +157,8 @@ __device__ __forceinline__ void unit_dot(const uint8_t* wbase, int wpitch, const
         const size_t e_hi = e_lo + (size_t)8 * s_stride;
         float slo, shi;
         if constexpr (SMEM) {
-          slo = __half2float(__ushort_as_half(sbase[e_lo]));
-          shi = __half2float(__ushort_as_half(sbase[e_hi]));
+          slo = __half2float(__ushort_as_half(lds16(sbase_s + (uint32_t)(e_lo * 2))));
+          shi = __half2float(__ushort_as_half(lds16(sbase_s + (uint32_t)(e_hi * 2))));
         } else {
           slo = ldg_half_as_float(sbase + e_lo);
           shi = ldg_half_as_float(sbase + e_hi);
@@ -228,7 +234,9 @@ __global__ void __launch_bounds__(kThreads, 1) ffn_decode_kernel(const FfnParams
   uint8_t* stages = smem;
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + (size_t)p.nstage * p.stage_bytes);
   uint64_t* empty = full + p.nstage;
-  float* red = reinterpret_cast<float*>(empty + p.nstage);
+  uint64_t* red_full = empty + p.nstage;    // [2] partials of a unit written by the consumer warps
+  uint64_t* red_empty = red_full + 2;       // [2] the reducer has read them
+  float* red = reinterpret_cast<float*>(red_empty + 2);
   Group* groups = reinterpret_cast<Group*>(red + 2 * kNW * kRedWarp);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(groups + kMaxGroups);
 
@@ -266,8 +274,12 @@ __global__ void __launch_bounds__(kThreads, 1) ffn_decode_kernel(const FfnParams
   }
   if (tid == 0) {
     for (int s = 0; s < p.nstage; ++s) {
-      mbar_init(&full[s], 1);
-      mbar_init(&empty[s], p.aw / p.nparts);
+      mbar_init(&full[s], 1);                  // the producer's expect_tx arrival
+      mbar_init(&empty[s], p.aw / p.nparts);   // one arrival per consumer warp of the part
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&red_full[b], p.aw);
+      mbar_init(&red_empty[b], 1);
     }
     *abort_flag = 0;
     fence_barrier_init();
@@ -277,31 +289,38 @@ __global__ void __launch_bounds__(kThreads, 1) ffn_decode_kernel(const FfnParams
   const int part_chunks = (p.K / 32) / p.nparts;
   const uint32_t scale_bytes = kRows * (p.K / p.G) * 2;
 
-  if (warp == kNW) {
-    // ---------------- producer: one thread issues the bulk copies, part by part
-    if (lane == 0) {
-      const size_t row_bytes = p.K / 2;
-      int it = 0;
-      for (int u = ub; u < ue; ++u) {
-        const int a = u / upe, r0 = (u - a * upe) * kRows;
-        const Group& gr = groups[a];
-        if ((gr.flags & 3) != 1) continue;   // skipped or host-resident
-        bool stop = false;
-        for (int part = 0; part < p.nparts; ++part, ++it) {
-          const int s = it % p.nstage;
-          if (!mbar_wait_bounded(&empty[s], ((it / p.nstage) & 1) ^ 1, abort_flag, p.status)) {
-            stop = true;
-            break;
-          }
-          uint8_t* dst = stages + (size_t)s * p.stage_bytes;
-          const uint8_t* src = gr.w + (size_t)r0 * row_bytes + (size_t)part * p.part_bytes;
-          mbar_arrive_expect_tx(&full[s], kRows * p.part_bytes + scale_bytes);
-          for (int r = 0; r < kRows; ++r) bulk_copy_g2s(dst + r * p.pitch, src + r * row_bytes, p.part_bytes, &full[s]);
-          bulk_copy_g2s(dst + kRows * p.pitch, gr.s + (size_t)r0 * (p.K / p.G), scale_bytes, &full[s]);
+  if (warp == kProducerWarp) {
+    // ---------------- producer: per part-stage, lane r issues the 1-D bulk (TMA)
+    // copy of row r and lane 0 the scales, so the 33 copies of a stage leave in
+    // one warp-wide instruction instead of 33 serial ones from a single thread.
+    const size_t row_bytes = p.K / 2;
+    int it = 0;
+    for (int u = ub; u < ue; ++u) {
+      const int a = u / upe, r0 = (u - a * upe) * kRows;
+      const Group& gr = groups[a];
+      if ((gr.flags & 3) != 1) continue;   // skipped or host-resident
+      bool stop = false;
+      for (int part = 0; part < p.nparts; ++part, ++it) {
+        const int s = it % p.nstage;
+        int ok = 1;
+        if (lane == 0) {
+          ok = mbar_wait_bounded(&empty[s], ((it / p.nstage) & 1) ^ 1, abort_flag, p.status) ? 1 : 0;
+          if (ok) mbar_arrive_expect_tx(&full[s], kRows * p.part_bytes + scale_bytes);
         }
-        if (stop) break;
+        if (!__shfl_sync(0xffffffffu, ok, 0)) {   // warp-uniform
+          stop = true;
+          break;
+        }
+        uint8_t* dst = stages + (size_t)s * p.stage_bytes;
+        const uint8_t* src = gr.w + (size_t)r0 * row_bytes + (size_t)part * p.part_bytes;
+        bulk_copy_g2s(dst + lane * p.pitch, src + lane * row_bytes, p.part_bytes, &full[s]);   // kRows == 32
+        if (lane == 0)
+          bulk_copy_g2s(dst + kRows * p.pitch, gr.s + (size_t)r0 * (p.K / p.G), scale_bytes, &full[s]);
       }
-      // Every issued copy must land before the CTA exits (also after an abort).
+      if (stop) break;
+    }
+    // Every issued copy must land before the CTA exits (also after an abort).
+    if (lane == 0) {
       const int first = it > p.nstage ? it - p.nstage : 0;
       for (int j = first; j < it; ++j)
         mbar_wait_bounded(&full[j % p.nstage], (j / p.nstage) & 1, nullptr, p.status);
@@ -309,93 +328,119 @@ __global__ void __launch_bounds__(kThreads, 1) ffn_decode_kernel(const FfnParams
     return;
   }
 
+  if (warp == kReducerWarp) {
+    // ---------------- reducer: adds the consumer warps' partials of each unit in
+    // fixed warp order (deterministic) while the consumers go on with the next
+    // unit; two partial buffers.
+    int ru = 0;
+    for (int u = ub; u < ue; ++u) {
+      const int a = u / upe, r0 = (u - a * upe) * kRows;
+      const Group& gr = groups[a];
+      if (!(gr.flags & 1)) continue;
+      const int buf = ru & 1;
+      int ok = 1;
+      if (lane == 0) ok = mbar_wait_bounded(&red_full[buf], (ru >> 1) & 1, abort_flag, p.status) ? 1 : 0;
+      ok = __shfl_sync(0xffffffffu, ok, 0);
+      const float* rb = red + (size_t)buf * kNW * kRedWarp;
+      if (ok) {
+        if constexpr (MODE == 0) {
+          // gate row r and up row r of token n -> h = silu(g) * u, stored as the
+          // down kernel's B fragment: feature f = r0/2 + r of chunk f/32, lane
+          // 4n + (f%32)/8, pair (f%8)%4, half (f%8)/4; high part then remainder.
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            const int o = lane + 32 * j, n = o >> 4, r = o & 15;
+            float gs = 0.f, us = 0.f;
+#pragma unroll
+            for (int w = 0; w < kNW; ++w) {
+              if (w < p.aw) {
+                gs += rb[w * kRedWarp + n * kRedStride + r];
+                us += rb[w * kRedWarp + kRedTile + n * kRedStride + r];
+              }
+            }
+            const float h = silu_f32(gs) * us;
+            const __half hh = __float2half_rn(h);
+            const __half hl = __float2half_rn(h - __half2float(hh));
+            const int f = r0 / 2 + r;
+            const int c = f >> 5, tt = (f & 31) >> 3, i8 = f & 7;
+            const size_t base = (((size_t)a * (p.I / 32) + c) * 32 + (4 * n + tt)) * 16;
+            p.hfrag[base + (i8 & 3) * 2 + (i8 >> 2)] = __half_as_ushort(hh);
+            p.hfrag[base + (4 + (i8 & 3)) * 2 + (i8 >> 2)] = __half_as_ushort(hl);
+          }
+        } else {
+#pragma unroll
+          for (int j = 0; j < 8; ++j) {
+            const int o = lane + 32 * j, i = o >> 7, n = (o >> 4) & 7, r = o & 15;
+            float v = 0.f;
+#pragma unroll
+            for (int w = 0; w < kNW; ++w)
+              if (w < p.aw) v += rb[w * kRedWarp + i * kRedTile + n * kRedStride + r];
+            const int q = gr.outq[n];
+            if (q >= 0) p.expert_out[(size_t)q * p.H + r0 + 16 * i + r] = v;
+          }
+        }
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&red_empty[buf]);
+      ++ru;
+    }
+    return;
+  }
+
   // ---------------- consumers
   const int g = lane >> 2, t = lane & 3;
-  const bool working = warp < p.aw;
+  if (warp >= p.aw) return;                 // no K range for this warp (small shapes)
   const int c0 = warp * CPW;
-  const int wpart = working ? warp / (p.aw / p.nparts) : 0;
+  const int wpart = warp / (p.aw / p.nparts);
   uint32_t bfr[CPW][NB];
-  if constexpr (MODE == 0) {
-    if (working) load_x_frags<CPW>(p, c0, g, t, bfr);
-  }
-  int cur_a = -1, units0 = 0, buf = 0;
+  if constexpr (MODE == 0) load_x_frags<CPW>(p, c0, g, t, bfr);
+  int cur_a = -1, units0 = 0, ru = 0;
   for (int u = ub; u < ue; ++u) {
     const int a = u / upe, r0 = (u - a * upe) * kRows;
     const Group& gr = groups[a];
     if (!(gr.flags & 1)) {
-      if (tid == 0) set_status(p.status, QRE_DEV_NULL_SLOT);
+      if (threadIdx.x == 0) set_status(p.status, QRE_DEV_NULL_SLOT);
       continue;
     }
     const bool host = gr.flags & 2;
     if constexpr (MODE == 1) {
-      if (a != cur_a && working) load_h_frags<CPW>(p, a, c0, lane, bfr);
+      if (a != cur_a) load_h_frags<CPW>(p, a, c0, lane, bfr);
     }
     cur_a = a;
-    if (working) {
-      float acc[kTiles][4];
+    float acc[kTiles][4];
 #pragma unroll
-      for (int i = 0; i < kTiles; ++i) acc[i][0] = acc[i][1] = acc[i][2] = acc[i][3] = 0.f;
-      if (!host) {
-        const int it = units0 * p.nparts + wpart;
-        const int s = it % p.nstage;
-        const bool have = mbar_wait_bounded(&full[s], (it / p.nstage) & 1, abort_flag, p.status);
-        const uint8_t* wb = stages + (size_t)s * p.stage_bytes;
-        if (have)
-          unit_dot<CPW, NB, true>(wb, p.pitch, reinterpret_cast<const uint16_t*>(wb + kRows * p.pitch), p.K / p.G,
-                                  c0, wpart * part_chunks, p.gc, g, t, bfr, acc);
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&empty[s]);
-      } else {
-        unit_dot<CPW, NB, false>(gr.w + (size_t)r0 * (p.K / 2), p.K / 2, gr.s + (size_t)r0 * (p.K / p.G), p.K / p.G,
-                                 c0, 0, p.gc, g, t, bfr, acc);
-      }
-      float* rw = red + (size_t)(buf * kNW + warp) * kRedWarp;
-#pragma unroll
-      for (int i = 0; i < kTiles; ++i) {
-        rw[i * kRedTile + (2 * t) * kRedStride + g] = acc[i][0];
-        rw[i * kRedTile + (2 * t + 1) * kRedStride + g] = acc[i][1];
-        rw[i * kRedTile + (2 * t) * kRedStride + g + 8] = acc[i][2];
-        rw[i * kRedTile + (2 * t + 1) * kRedStride + g + 8] = acc[i][3];
-      }
-    }
-    if (!host) ++units0;
-    named_barrier_sync(1, kNW * 32);
-    const float* rb = red + (size_t)buf * kNW * kRedWarp;
-    if constexpr (MODE == 0) {
-      if (tid < 16 * kTok) {
-        // gate row r and up row r of token n -> h = silu(g) * u, stored as the
-        // down kernel's B fragment: feature f = r0/2 + r of chunk f/32, lane
-        // 4n + (f%32)/8, pair (f%8)%4, half (f%8)/4; high part then remainder.
-        const int n = tid >> 4, r = tid & 15;
-        float gs = 0.f, us = 0.f;
-#pragma unroll
-        for (int w = 0; w < kNW; ++w) {
-          if (w < p.aw) {
-            gs += rb[w * kRedWarp + n * kRedStride + r];
-            us += rb[w * kRedWarp + kRedTile + n * kRedStride + r];
-          }
-        }
-        const float h = silu_f32(gs) * us;
-        const __half hh = __float2half_rn(h);
-        const __half hl = __float2half_rn(h - __half2float(hh));
-        const int f = r0 / 2 + r;
-        const int c = f >> 5, tt = (f & 31) >> 3, i8 = f & 7;
-        const size_t base = (((size_t)a * (p.I / 32) + c) * 32 + (4 * n + tt)) * 16;
-        p.hfrag[base + (i8 & 3) * 2 + (i8 >> 2)] = __half_as_ushort(hh);
-        p.hfrag[base + (4 + (i8 & 3)) * 2 + (i8 >> 2)] = __half_as_ushort(hl);
-      }
+    for (int i = 0; i < kTiles; ++i) acc[i][0] = acc[i][1] = acc[i][2] = acc[i][3] = 0.f;
+    if (!host) {
+      const int it = units0 * p.nparts + wpart;
+      const int s = it % p.nstage;
+      const bool have = mbar_wait_bounded(&full[s], (it / p.nstage) & 1, abort_flag, p.status);
+      const uint32_t wb = after_wait(smem_addr(stages + (size_t)s * p.stage_bytes));
+      if (have)
+        unit_dot<CPW, NB, true>(nullptr, wb, p.pitch, nullptr, wb + kRows * p.pitch, p.K / p.G, c0,
+                                wpart * part_chunks, p.gc, g, t, bfr, acc);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&empty[s]);
+      ++units0;
     } else {
-      if (tid < kTiles * 16 * kTok) {
-        const int i = tid >> 7, n = (tid >> 4) & 7, r = tid & 15;
-        float v = 0.f;
-#pragma unroll
-        for (int w = 0; w < kNW; ++w)
-          if (w < p.aw) v += rb[w * kRedWarp + i * kRedTile + n * kRedStride + r];
-        const int q = gr.outq[n];
-        if (q >= 0) p.expert_out[(size_t)q * p.H + r0 + 16 * i + r] = v;
-      }
+      unit_dot<CPW, NB, false>(gr.w + (size_t)r0 * (p.K / 2), 0, p.K / 2, gr.s + (size_t)r0 * (p.K / p.G), 0,
+                               p.K / p.G, c0, 0, p.gc, g, t, bfr, acc);
     }
-    buf ^= 1;
+    const int buf = ru & 1;
+    int ok = 1;
+    if (lane == 0) ok = mbar_wait_bounded(&red_empty[buf], ((ru >> 1) & 1) ^ 1, abort_flag, p.status) ? 1 : 0;
+    __syncwarp();
+    (void)ok;
+    float* rw = red + (size_t)(buf * kNW + warp) * kRedWarp;
+#pragma unroll
+    for (int i = 0; i < kTiles; ++i) {
+      rw[i * kRedTile + (2 * t) * kRedStride + g] = acc[i][0];
+      rw[i * kRedTile + (2 * t + 1) * kRedStride + g] = acc[i][1];
+      rw[i * kRedTile + (2 * t) * kRedStride + g + 8] = acc[i][2];
+      rw[i * kRedTile + (2 * t + 1) * kRedStride + g + 8] = acc[i][3];
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&red_full[buf]);
+    ++ru;
   }
 }
 
@@ -421,7 +466,7 @@ Plan make_plan(int K, int G, int smem_budget) {
   pl.pitch = ((pl.part_bytes + 127) / 128) * 128 + 16;
   pl.stage_bytes = kRows * pl.pitch + kRows * (K / G) * 2;
   pl.stage_bytes = (pl.stage_bytes + 127) / 128 * 128;
-  const int fixed = 2 * kNW * kRedWarp * 4 + kMaxGroups * (int)sizeof(Group) + 16;
+  const int fixed = 4 * 8 + 2 * kNW * kRedWarp * 4 + kMaxGroups * (int)sizeof(Group) + 16;
   int ns = (smem_budget - fixed) / (pl.stage_bytes + 16);
   if (ns > 8) ns = 8;
   if (ns < 2) return pl;

@@ -10,7 +10,10 @@
 // Three kernels:
 //   gather   Xg[q] = fp16(x[token of pick perm[q]]) for the T*k sorted picks,
 //            then Xg[T*k + t] = fp16(x[t]) for the shared expert.  Every
-//            expert's tokens become a contiguous row range of Xg.
+//            expert's tokens become a contiguous row range of Xg.  Inside each
+//            group of 8 reduction elements the order is (0,4,1,5,2,6,3,7), the
+//            order in which the 4-bit decode yields weight pairs; h16 uses the
+//            same order, so no operand needs a permute.
 //   GEMM 1   per tile (expert, 128 rows of the interleaved gate/up matrix, <=256
 //            tokens); the epilogue pairs each gate row with its up row (they sit
 //            16 TMEM lanes apart) and writes h = silu(g) * u as fp16 to h16.
@@ -86,13 +89,16 @@ __global__ void __launch_bounds__(256) gather_x_kernel(int T, int H, int k, cons
   const int c = (int)(i - q * per_row) * 8;
   const int t = q < P ? __ldg(perm + q) / k : (int)(q - P);
   const uint4 v = __ldg(reinterpret_cast<const uint4*>(x + (size_t)t * H + c));
-  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+  float f[8];
+  f[0] = bf16_bits_to_float(v.x & 0xFFFFu); f[1] = bf16_bits_to_float(v.x >> 16);
+  f[2] = bf16_bits_to_float(v.y & 0xFFFFu); f[3] = bf16_bits_to_float(v.y >> 16);
+  f[4] = bf16_bits_to_float(v.z & 0xFFFFu); f[5] = bf16_bits_to_float(v.z >> 16);
+  f[6] = bf16_bits_to_float(v.w & 0xFFFFu); f[7] = bf16_bits_to_float(v.w >> 16);
   uint32_t o[4];
   bool bad = false;
 #pragma unroll
-  for (int j = 0; j < 4; ++j) {
-    const float lo = bf16_bits_to_float(w[j] & 0xFFFFu), hi = bf16_bits_to_float(w[j] >> 16);
-    const __half2 h = __floats2half2_rn(lo, hi);
+  for (int j = 0; j < 4; ++j) {   // pair order (x_j, x_{j+4}), the order the weight decode produces
+    const __half2 h = __floats2half2_rn(f[j], f[j + 4]);
     bad |= __hisinf(__low2half(h)) || __hisinf(__high2half(h));
     o[j] = h2_as_u32(h);
   }
@@ -133,20 +139,18 @@ __device__ __forceinline__ Tile decode_tile(int t, int ngroups, const int* tstar
   return tl;
 }
 
-// Eight nibbles (k, k+1, ..., k+7 from the low end of w) -> eight fp16 values
-// q*s in natural k order, as four half2.
+// Eight nibbles (k .. k+7 from the low end of w) -> eight fp16 values q*s in
+// pair order (q0,q4) (q1,q5) (q2,q6) (q3,q7).  The token operand (gather) and h
+// (GEMM 1 epilogue) are stored with the same order inside every group of 8
+// reduction elements, so the products pair up as in natural order.
 __device__ __forceinline__ uint4 dequant8(uint32_t w, __half2 s2) {
   uint32_t p[4];
-  decode_nibbles(w, p);  // (q0,q4) (q1,q5) (q2,q6) (q3,q7)
-  const uint32_t n01 = __byte_perm(p[0], p[1], 0x5410);
-  const uint32_t n23 = __byte_perm(p[2], p[3], 0x5410);
-  const uint32_t n45 = __byte_perm(p[0], p[1], 0x7632);
-  const uint32_t n67 = __byte_perm(p[2], p[3], 0x7632);
+  decode_nibbles(w, p);
   uint4 r;
-  r.x = h2_as_u32(__hmul2(u32_as_h2(n01), s2));
-  r.y = h2_as_u32(__hmul2(u32_as_h2(n23), s2));
-  r.z = h2_as_u32(__hmul2(u32_as_h2(n45), s2));
-  r.w = h2_as_u32(__hmul2(u32_as_h2(n67), s2));
+  r.x = h2_as_u32(__hmul2(u32_as_h2(p[0]), s2));
+  r.y = h2_as_u32(__hmul2(u32_as_h2(p[1]), s2));
+  r.z = h2_as_u32(__hmul2(u32_as_h2(p[2]), s2));
+  r.w = h2_as_u32(__hmul2(u32_as_h2(p[3]), s2));
   return r;
 }
 
@@ -378,7 +382,9 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_gemm_kernel(const Prefill
                 const float h = g / (1.0f + expf(-g)) * up;
                 const __half hh = __float2half_rn(h);
                 if (__hisinf(hh)) set_status(p.status, QRE_DEV_FP16_RANGE);
-                p.h16[(size_t)(tl.row0 + tl.n0 + n) * p.I + feat] = hh;
+                // within each group of 8 features, feature i sits at 2*(i%4) + i/4
+                const int pos = (feat & ~7) | (((feat & 3) << 1) | ((feat >> 2) & 1));
+                p.h16[(size_t)(tl.row0 + tl.n0 + n) * p.I + pos] = hh;
               }
             }
           } else {

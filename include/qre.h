@@ -96,21 +96,26 @@ typedef struct {
  * expert from a cache slot to host memory is a write of this struct.
  *
  * Weight format (packed 4-bit symmetric groups, fp16 scales), for a matrix
- * W [N, K] with K contiguous and groups of G along K:
+ * W [N, K] (N a multiple of 128, K of 64) with groups of G along K:
  *   s = fp16_RNE(max|w| / 7) (fp64 quotient), q = clamp(rint_half_even(w / s),
- *   -8, 7) (q = 0 when s == 0), nibble u = q + 8 at byte (n*K + k)/2, even k in
- *   the low nibble; dequantized value (u - 8) * s.
+ *   -8, 7) (q = 0 when s == 0), nibble u = q + 8, even k in the low nibble of
+ *   its byte; dequantized value (u - 8) * s.
+ * Storage is tiled so that a warp reading 32 rows of one 32-column slice reads
+ * 512 contiguous bytes:
+ *   packed: 4096-byte chunks, chunk (n/128)*(K/64) + k/64; inside it byte
+ *           2048*((k%64)/32) + 16*(n%128) + (k%32)/2
+ *   scales: fp16 of (n, group g) at ((n/128)*(K/G) + g)*128 + n%128
  * The gate and up projections ([I, H] each) are stored as one [2I, H] matrix
  * whose rows alternate in blocks of 16 (16 gate rows, 16 up rows, ...).
  */
 typedef struct {
-  const uint8_t*  w_gate_up;  /* [2I][H/2] packed, device or host-mapped        */
-  const uint16_t* s_gate_up;  /* fp16 [2I][H/G], device or host-mapped          */
-  const uint8_t*  w_down;     /* [H][I/2] packed, device or host-mapped         */
-  const uint16_t* s_down;     /* fp16 [H][I/G], device or host-mapped           */
-  uint32_t tier;              /* 0 = device memory (read through shared-memory
-                                 bulk copies), 1 = host-mapped (read with direct
-                                 loads over the host link)                      */
+  const uint8_t*  w_gate_up;  /* 2I x H packed (I*H bytes), device or host-mapped */
+  const uint16_t* s_gate_up;  /* 2I x H/G fp16 scales, device or host-mapped      */
+  const uint8_t*  w_down;     /* H x I packed (H*I/2 bytes), device or host-mapped */
+  const uint16_t* s_down;     /* H x I/G fp16 scales, device or host-mapped       */
+  uint32_t tier;              /* 0 = device memory, 1 = host-mapped (read with
+                                 direct loads over the host link); both are read
+                                 the same way, the tier is informational         */
   uint32_t reserved;          /* must be 0                                      */
 } qre_slot;
 
@@ -136,9 +141,10 @@ QRE_API qre_status qre_workspace_size(const qre_layer_shape* shape, int32_t T, s
  * slot table's comment).  This is the offline step that produces expert
  * weights; it is not part of the per-token path.
  *   w       [n_rows][k_dim] fp32, device
- *   packed  [n_rows][k_dim/2] uint8, device (written)
- *   scales  [n_rows][k_dim/group] fp16 bits, device (written)
- * group in {32, 64, 128}; k_dim a positive multiple of group; n_rows >= 0.
+ *   packed  n_rows*k_dim/2 bytes, tiled as above, device (written)
+ *   scales  n_rows*k_dim/group fp16 bits, tiled as above, device (written)
+ * group in {32, 64, 128}; k_dim a positive multiple of group and of 64; n_rows
+ * a multiple of 128 (0 is a no-op).
  * A non-finite scale sets QRE_DEV_BAD_SCALE in the device status word.
  */
 QRE_API qre_status qre_quantize(int32_t n_rows, int32_t k_dim, int32_t group, const float* w,
@@ -147,10 +153,10 @@ QRE_API qre_status qre_quantize(int32_t n_rows, int32_t k_dim, int32_t group, co
 /*
  * Quantize one expert's gate and up projections (w_gate, w_up: [inter][hidden]
  * fp32, device) into the interleaved [2*inter][hidden] layout described at
- * qre_slot: packed [2*inter][hidden/2] uint8 and scales [2*inter][hidden/group]
- * fp16 bits (device, written).  inter a positive multiple of 16, hidden a
- * positive multiple of group, group in {32, 64, 128}.  A non-finite scale sets
- * QRE_DEV_BAD_SCALE.
+ * qre_slot, tiled as described there: packed 2*inter*hidden/2 bytes and scales
+ * 2*inter*hidden/group fp16 bits (device, written).  inter a positive multiple
+ * of 64, hidden a positive multiple of group and of 64, group in {32, 64, 128}.
+ * A non-finite scale sets QRE_DEV_BAD_SCALE.
  */
 QRE_API qre_status qre_quantize_gate_up(int32_t inter, int32_t hidden, int32_t group, const float* w_gate,
                                         const float* w_up, uint8_t* packed, uint16_t* scales,

@@ -174,8 +174,9 @@ qre_status qre_workspace_size(const qre_layer_shape* shape, int32_t T, size_t* b
 qre_status qre_quantize(int32_t n_rows, int32_t k_dim, int32_t group, const float* w, uint8_t* packed,
                         uint16_t* scales, qre_stream_t stream) {
   if (group != 32 && group != 64 && group != 128) return fail(QRE_ERR_UNSUPPORTED, "group %d not in {32, 64, 128}", group);
-  if (n_rows < 0 || k_dim <= 0 || k_dim % group)
-    return fail(QRE_ERR_INVALID_ARG, "need n_rows >= 0 and k_dim a positive multiple of group (got %d, %d)", n_rows,
+  if (n_rows < 0 || n_rows % 128 || k_dim <= 0 || k_dim % group || k_dim % 64)
+    return fail(QRE_ERR_INVALID_ARG,
+                "need n_rows a multiple of 128 and k_dim a positive multiple of group and of 64 (got %d, %d)", n_rows,
                 k_dim);
   if (n_rows == 0) return QRE_OK;
   QRE_REQUIRE_PTR(w);
@@ -189,9 +190,9 @@ qre_status qre_quantize(int32_t n_rows, int32_t k_dim, int32_t group, const floa
 qre_status qre_quantize_gate_up(int32_t inter, int32_t hidden, int32_t group, const float* w_gate, const float* w_up,
                                 uint8_t* packed, uint16_t* scales, qre_stream_t stream) {
   if (group != 32 && group != 64 && group != 128) return fail(QRE_ERR_UNSUPPORTED, "group %d not in {32, 64, 128}", group);
-  if (inter <= 0 || inter % 16 || hidden <= 0 || hidden % group)
-    return fail(QRE_ERR_INVALID_ARG, "need inter a positive multiple of 16 and hidden a positive multiple of group "
-                "(got %d, %d)", inter, hidden);
+  if (inter <= 0 || inter % 64 || hidden <= 0 || hidden % group || hidden % 64)
+    return fail(QRE_ERR_INVALID_ARG, "need inter a positive multiple of 64 and hidden a positive multiple of group "
+                "and of 64 (got %d, %d)", inter, hidden);
   QRE_REQUIRE_PTR(w_gate);
   QRE_REQUIRE_PTR(w_up);
   QRE_REQUIRE_PTR(packed);

@@ -102,12 +102,16 @@ __global__ void __launch_bounds__(256) quantize_kernel(long long n_threads, int 
     }
     word |= (uint32_t)(q + 8) << (4 * j);
   }
-  reinterpret_cast<uint32_t*>(packed)[i] = word;
+  // tiled storage: 4 KB chunks of 128 rows x 64 elements; inside a chunk the
+  // first 32 elements of every row (16 bytes each, rows in order), then the last 32
   const long long elem = i * 8;
   const long long row = elem / K;
   const int col = (int)(elem - row * K);
+  const long long chunk = (row >> 7) * (K >> 6) + (col >> 6);
+  const long long byte = chunk * 4096 + ((col >> 5) & 1) * 2048 + (row & 127) * 16 + ((col & 31) >> 1);
+  reinterpret_cast<uint32_t*>(packed)[byte >> 2] = word;
   if (col % G == 0) {
-    scales[row * (K / G) + col / G] = __half_as_ushort(s16);
+    scales[((row >> 7) * (K / G) + col / G) * 128 + (row & 127)] = __half_as_ushort(s16);
     if (!finite) set_status(status, QRE_DEV_BAD_SCALE);
   }
 }

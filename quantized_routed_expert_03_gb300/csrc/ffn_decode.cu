@@ -2,66 +2,66 @@
 //
 // The decode step of a routed MoE layer reads every byte of the union of the
 // experts its tokens picked, plus the shared expert, once (glm53-flash-offload
-// README, "Batched decode": streams share the per-layer expert union).  The
-// work is a matrix-vector product per expert over 4-bit weights; the bound is
-// HBM bandwidth, so the design goal is to stream packed weights at full rate
-// and keep every other cost under it.
+// README, "Batched decode": streams share the per-layer expert union).  The work
+// is a matrix-vector product per expert over 4-bit weights and the bound is HBM
+// bandwidth, so the packed weights must stream at full rate while everything
+// else stays under that.
 //
-// Layout of the work
-//   * A unit is 32 consecutive output rows of one expert's matrix (for gate/up,
-//     one block of 16 gate rows and the matching 16 up rows) over the full
-//     reduction length K, staged in two K halves ("parts").
+// Layout of the work (5th-generation tensor cores, weights in tensor memory)
+//   * A unit is 128 consecutive rows of one expert's matrix (UMMA M = 128; for
+//     gate/up four blocks of 16 gate rows, each followed by its 16 up rows).
 //     Units of all active experts and the shared expert are split into equal
-//     contiguous ranges, one per CTA; one CTA per SM (persistent).
-//   * A producer warp streams each unit from HBM into a ring of shared-memory
-//     stages with 1-D bulk (TMA) copies, one row per lane, so a stage's copies
-//     leave in one warp-wide instruction (one thread issuing them one by one was
-//     measured to cap the stream near 2 TB/s), completing on an mbarrier.  Rows land at a pitch of 16 mod 128 bytes so
-//     the consumers' 32-bit loads are free of bank conflicts.  Units of host-resident experts (slot tier 1) skip
-//     the ring: the consumers read them with direct loads over the host link,
-//     as the README's "Zero-copy home" does.
-//   * 16 consumer warps split K; each warp owns a fixed K range, so the
-//     activation operand for that range is loaded once into registers (gate/up)
-//     or once per expert (down).  The tokens are the N = 8 side of the
-//     m16n8k16 tensor-core MMA: rows of weights are M, T <= 8 tokens are N.  A
-//     32-bit word of 8 nibbles decodes to four fp16 pairs of exact integer codes;
-//     the MMA multiplies them by fp16 activations exactly and accumulates in
-//     fp32 per quantization group, and the group's fp16 scale is applied in fp32.
-//     The K order inside a 32-element chunk is permuted identically in weights
-//     and activations, which leaves every dot product unchanged.
-//   * Per unit, the 16 warps' partial sums go to one of two shared buffers and a
-//     reducer warp adds them in fixed warp order (deterministic) while the
-//     consumers continue with the next unit; the result goes to the gate/up
-//     workspace (gate/up kernel) or to the expert's output rows (down kernel).
-// The down kernel computes h = silu(g) * u from the gate/up workspace while it
-// loads its activation operand, and splits h into an fp16 high part and an fp16
-// remainder so that its products stay accurate to about fp32.
+//     contiguous ranges, one per CTA; one CTA per SM.
+//   * The four warpgroups of a CTA split the reduction length K.  Thread r of a
+//     warpgroup owns weight row r of the unit and tensor-memory lane r.  The
+//     packed weights are stored in 4 KB chunks of 128 rows x 64 reduction
+//     elements, so each warp's 16-byte loads cover 512 contiguous bytes; they are
+//     prefetched up to four stages ahead, across unit boundaries (host-resident
+//     experts are read the same way, zero-copy).  Each thread decodes its 64
+//     nibbles per stage into fp16 pairs of exact integer codes and writes them
+//     into its lane with tcgen05.st.
+//   * One tcgen05.mma (A from tensor memory, B from shared memory, M=128, N=16,
+//     K=16) is cheap for the tensor core but takes a warp on the order of a
+//     hundred cycles to issue, while issues from different warps overlap.  So
+//     every warp issues: stage g of a warpgroup is issued by its warp g mod 4,
+//     once all four warps have arrived on the stage's mbarrier, and completes
+//     on one commit per stage; no warp waits for the others between stages.
+//   * B holds the tokens (T <= 8) in shared memory, 128-byte swizzled: rows 0-7
+//     the fp16 high parts, rows 8-15 the fp16 remainders (x - high), so the
+//     products stay accurate to about fp32.  The weights are exact codes, so the
+//     only rounding is the fp32 accumulation.
+//   * Every quantization group accumulates into its own buffer (four rotate); one
+//     stage later the owning threads read it back (tcgen05.ld), add the two
+//     halves and apply the group's fp16 scale in fp32.
+//   * The four warpgroups' partial rows are added in fixed order (deterministic);
+//     gate/up pairs each gate row with its up row (16 lanes apart, a shuffle) and
+//     stores h = silu(g) * u as fp16 high part and remainder for the down kernel;
+//     down writes the expert's output rows.
+//   * Inside every group of 8 reduction elements the tokens and h are stored in
+//     the order the nibble decode yields weight pairs (0,4,1,5,2,6,3,7), which
+//     leaves every dot product unchanged.
 #include "common.cuh"
 #include "internal.h"
+#include "tc.cuh"
 
 namespace qre {
 namespace {
 
-constexpr int kNW = 16;                    // consumer warps
-constexpr int kProducerWarp = kNW;
-constexpr int kReducerWarp = kNW + 1;
-constexpr int kThreads = (kNW + 2) * 32;   // + one producer warp + one reducer warp
-constexpr int kTiles = 2;                  // MMA M tiles (16 rows each) per unit
-constexpr int kRows = 16 * kTiles;         // rows per unit: one gate block + one up block
-static_assert(kRows == 32, "the producer issues one row copy per lane");
-constexpr int kTok = kDecodeMaxTokens;     // MMA N
-constexpr int kRedStride = 20;             // floats between token columns of a partial
-constexpr int kRedTile = kTok * kRedStride;
-constexpr int kRedWarp = kTiles * kRedTile;
+constexpr int kWG = 4;                    // warpgroups (K splits) per CTA
+constexpr int kThreads = kWG * 128;
+constexpr int BM = 128;                   // weight rows per unit (UMMA M, one TMEM lane each)
+constexpr int BN = 16;                    // UMMA N: token high parts, then remainders
+constexpr int SK = 64;                    // reduction elements per stage (32 TMEM columns)
+constexpr int kTok = kDecodeMaxTokens;    // tokens
+constexpr int kColsPerWG = 128;           // TMEM columns per warpgroup: NA A buffers of 32, then the D buffers
 constexpr int kMaxGroups = kDecodeMaxTokens * 16 + 1;   // T*k active experts + the shared one
+constexpr int kChunk = BM * SK / 2;       // bytes of one packed 128 x 64 chunk
 
-// One active expert (or the shared expert) as this kernel sees it; built once
-// per CTA in shared memory so that no unit waits on dependent global loads.
 struct Group {
   const uint8_t* w;    // packed matrix of this kernel (gate/up or down)
   const uint16_t* s;   // its scales
   int e;               // expert id (E = shared)
-  int flags;           // bit 0: usable, bit 1: host-resident (read with direct loads)
+  int flags;           // bit 0: usable
   int outq[kTok];      // down kernel: expert_out row of token n, or -1
 };
 
@@ -69,13 +69,10 @@ struct FfnParams {
   int H, I, E, k, G, T;
   int K;            // reduction length: H (gate/up) or I (down)
   int n_out;        // rows per expert: 2I (gate/up) or H (down)
-  int gc;           // 32-element chunks per quantization group
-  int aw;           // working consumer warps
-  int nparts;       // K is staged in this many parts; warp w reads part w / (aw / nparts)
-  int pitch;        // shared-memory row pitch in bytes (16 mod 128)
-  int part_bytes;   // bytes of one row in one part
-  int stage_bytes;  // rows of one part + the unit's scales
-  int nstage;
+  int kq;           // warpgroups sharing K (1, 2 or 4)
+  int lgG;          // log2 G
+  int lgS;          // log2 of the accumulation segment: min(G, K / kq)
+  int nB;           // B buffers in shared memory (down kernel: experts resident at once)
   int amax;         // largest possible number of active experts, min(E, T*k)
   const uint16_t* x;
   const qre_slot* slots;
@@ -83,189 +80,112 @@ struct FfnParams {
   const int32_t* perm;
   const int32_t* active;
   const int32_t* n_active;
-  uint16_t* hfrag;    // [(amax+1)][I/32][32 lanes][16 halves]: h as MMA B fragments
+  __half* hbuf;       // [(amax+1)][2][kTok][I]: h high parts, then remainders (reordered in 8-groups)
   float* expert_out;  // [T*k + T][H]
   int* status;
 };
 
-__device__ __forceinline__ uint32_t ldg_u32(const void* p) {
-  return __ldg(reinterpret_cast<const unsigned int*>(p));
-}
-__device__ __forceinline__ float ldg_half_as_float(const uint16_t* p) {
-  return __half2float(__ushort_as_half(__ldg(reinterpret_cast<const unsigned short*>(p))));
+struct Layout {
+  int b_off, red_off, bar_off, grp_off, misc_off;
+  size_t bytes;
+};
+
+__host__ __device__ inline Layout make_layout(int K, int nB) {
+  Layout L;
+  L.b_off = 0;                                          // nB x (BN x K fp16, swizzled; 1024-aligned)
+  L.red_off = L.b_off + nB * K * BN * 2;                // 2 x kWG x BM x kTok fp32
+  L.bar_off = L.red_off + 2 * kWG * BM * kTok * 4;      // a_full[kWG][3], done[kWG][3]
+  L.grp_off = L.bar_off + kWG * 6 * 8;
+  L.misc_off = L.grp_off + kMaxGroups * (int)sizeof(Group);
+  L.bytes = (size_t)L.misc_off + 16 + 1024;             // + alignment slack
+  return L;
 }
 
-// Dot products of one unit's 32 rows (two 16-row MMA tiles) with the warp's K
-// range.  SMEM: wbase/sbase point into the shared-memory stage (the staged part
-// and the unit's scales); otherwise global addresses of row 0 and its scales.
-// cbase is subtracted from the global chunk index to address the staged part.
-// Each tile accumulates into kAcc independent fragments (chunk cl goes to
-// cl % kAcc) so consecutive MMAs do not wait on each other; they are summed
-// when a quantization group ends.
-constexpr int kAcc = 2;
-template <int CPW, int NB, bool SMEM>
-__device__ __forceinline__ void unit_dot(const uint8_t* wbase, uint32_t wbase_s, int wpitch, const uint16_t* sbase,
-                                         uint32_t sbase_s, int s_stride, int c0, int cbase, int gc, int g, int t,
-                                         const uint32_t (&bfr)[CPW][NB], float (&acc)[kTiles][4]) {
-  float d[kTiles][kAcc][4];
-#pragma unroll
-  for (int i = 0; i < kTiles; ++i)
-#pragma unroll
-    for (int j = 0; j < kAcc; ++j) d[i][j][0] = d[i][j][1] = d[i][j][2] = d[i][j][3] = 0.f;
-  // Loads are issued one quantization group (GCMAX chunks at most) ahead of
-  // their use, so they overlap the previous group's MMAs.
-  constexpr int GCMAX = CPW < 4 ? CPW : 4;
-  uint32_t wv[GCMAX][kTiles][2];
-#pragma unroll
-  for (int cl = 0; cl < CPW; ++cl) {
-    const int c = c0 + cl;
-    const int j = cl % kAcc;
-    if (cl % GCMAX == 0) {
-#pragma unroll
-      for (int u = 0; u < GCMAX; ++u) {
-        const int col = (c + u - cbase) * 16 + t * 4;
-#pragma unroll
-        for (int i = 0; i < kTiles; ++i) {
-          if constexpr (SMEM) {
-            const uint32_t a_lo = wbase_s + (uint32_t)((16 * i + g) * wpitch + col);
-            wv[u][i][0] = lds32(a_lo);
-            wv[u][i][1] = lds32(a_lo + 8 * wpitch);
-          } else {
-            const uint8_t* r_lo = wbase + (size_t)(16 * i + g) * wpitch + col;
-            wv[u][i][0] = ldg_u32(r_lo);
-            wv[u][i][1] = ldg_u32(r_lo + (size_t)8 * wpitch);
-          }
-        }
-      }
-    }
-    const int u = cl % GCMAX;
-#pragma unroll
-    for (int i = 0; i < kTiles; ++i) {
-      uint32_t pl[4], ph[4];
-      decode_nibbles(wv[u][i][0], pl);
-      decode_nibbles(wv[u][i][1], ph);
-      mma_f16_16816(d[i][j], pl[0], ph[0], pl[1], ph[1], bfr[cl][0], bfr[cl][1]);
-      if constexpr (NB == 8) mma_f16_16816(d[i][j], pl[0], ph[0], pl[1], ph[1], bfr[cl][4], bfr[cl][5]);
-      mma_f16_16816(d[i][j], pl[2], ph[2], pl[3], ph[3], bfr[cl][2], bfr[cl][3]);
-      if constexpr (NB == 8) mma_f16_16816(d[i][j], pl[2], ph[2], pl[3], ph[3], bfr[cl][6], bfr[cl][7]);
-    }
-    if (((cl + 1) & (gc - 1)) == 0) {  // end of a quantization group
-      const int grp = c / gc;
-#pragma unroll
-      for (int i = 0; i < kTiles; ++i) {
-        const size_t e_lo = (size_t)(16 * i + g) * s_stride + grp;
-        const size_t e_hi = e_lo + (size_t)8 * s_stride;
-        float slo, shi;
-        if constexpr (SMEM) {
-          slo = __half2float(__ushort_as_half(lds16(sbase_s + (uint32_t)(e_lo * 2))));
-          shi = __half2float(__ushort_as_half(lds16(sbase_s + (uint32_t)(e_hi * 2))));
-        } else {
-          slo = ldg_half_as_float(sbase + e_lo);
-          shi = ldg_half_as_float(sbase + e_hi);
-        }
-        float v[4];
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          v[q] = d[i][0][q];
-#pragma unroll
-          for (int jj = 1; jj < kAcc; ++jj) v[q] += d[i][jj][q];
-        }
-        acc[i][0] = fmaf(slo, v[0], acc[i][0]);
-        acc[i][1] = fmaf(slo, v[1], acc[i][1]);
-        acc[i][2] = fmaf(shi, v[2], acc[i][2]);
-        acc[i][3] = fmaf(shi, v[3], acc[i][3]);
-#pragma unroll
-        for (int jj = 0; jj < kAcc; ++jj) d[i][jj][0] = d[i][jj][1] = d[i][jj][2] = d[i][jj][3] = 0.f;
-      }
-    }
-  }
-}
-
-// Activation operand for gate/up: x[token g][32c + 8t .. +7] as fp16 pairs
-// (x0,x4) (x1,x5) (x2,x6) (x3,x7), matching decode_nibbles' pair order.
-template <int CPW>
-__device__ __forceinline__ void load_x_frags(const FfnParams& p, int c0, int g, int t, uint32_t (&bfr)[CPW][4]) {
-#pragma unroll
-  for (int cl = 0; cl < CPW; ++cl) {
-    if (g < p.T) {
-      const uint4 v = __ldg(reinterpret_cast<const uint4*>(p.x + (size_t)g * p.H + (c0 + cl) * 32 + t * 8));
-      const float f0 = bf16_bits_to_float(v.x & 0xFFFFu), f1 = bf16_bits_to_float(v.x >> 16);
-      const float f2 = bf16_bits_to_float(v.y & 0xFFFFu), f3 = bf16_bits_to_float(v.y >> 16);
-      const float f4 = bf16_bits_to_float(v.z & 0xFFFFu), f5 = bf16_bits_to_float(v.z >> 16);
-      const float f6 = bf16_bits_to_float(v.w & 0xFFFFu), f7 = bf16_bits_to_float(v.w >> 16);
-      bfr[cl][0] = pack_half2(f0, f4);
-      bfr[cl][1] = pack_half2(f1, f5);
-      bfr[cl][2] = pack_half2(f2, f6);
-      bfr[cl][3] = pack_half2(f3, f7);
-    } else {
-      bfr[cl][0] = bfr[cl][1] = bfr[cl][2] = bfr[cl][3] = 0u;
-    }
-  }
-}
-
-// Activation operand for down: the fragments the gate/up kernel stored.
-template <int CPW>
-__device__ __forceinline__ void load_h_frags(const FfnParams& p, int a, int c0, int lane, uint32_t (&bfr)[CPW][8]) {
-  const int nch = p.I / 32;
-#pragma unroll
-  for (int cl = 0; cl < CPW; ++cl) {
-    const uint4* src = reinterpret_cast<const uint4*>(p.hfrag + (((size_t)a * nch + c0 + cl) * 32 + lane) * 16);
-    const uint4 v0 = src[0], v1 = src[1];
-    bfr[cl][0] = v0.x; bfr[cl][1] = v0.y; bfr[cl][2] = v0.z; bfr[cl][3] = v0.w;
-    bfr[cl][4] = v1.x; bfr[cl][5] = v1.y; bfr[cl][6] = v1.z; bfr[cl][7] = v1.w;
-  }
+// Byte offset of (row n, logical reduction index l) in a swizzled B operand.
+__device__ __forceinline__ uint32_t b_offset(int n, int l) {
+  const int byte = (l & 63) * 2;
+  return (uint32_t)((l >> 6) * (BN * 128) + (n >> 3) * 1024 + (n & 7) * 128 + ((((byte >> 4) ^ (n & 7))) << 4) +
+                    (byte & 15));
 }
 
 __device__ __forceinline__ float silu_f32(float z) { return z / (1.0f + expf(-z)); }
 
-template <int MODE, int CPW>
+// fp16 high part and remainder of v.
+__device__ __forceinline__ void split_half(float v, __half& hi, __half& lo) {
+  hi = __float2half_rn(v);
+  lo = __float2half_rn(v - __half2float(hi));
+}
+
+// h of group a (high parts and remainders of the first T tokens) into B buffer `dst`.
+__device__ __forceinline__ void load_h(uint8_t* dst, const __half* hbuf, int a, int I, int T) {
+  const __half* hb = hbuf + (size_t)a * 2 * kTok * I;
+  for (int i = threadIdx.x; i < 2 * T * (I / 8); i += blockDim.x) {
+    const int j = i / (I / 8), g8 = i - j * (I / 8);
+    const int row = j < T ? j : 8 + (j - T);   // part * 8 + token
+    *reinterpret_cast<uint4*>(dst + b_offset(row, 8 * g8)) =
+        *reinterpret_cast<const uint4*>(hb + (size_t)row * I + 8 * g8);
+  }
+}
+
+// NA: A buffers per warpgroup.  Stage g's MMAs are issued during iteration g + 1
+// by lane 0 of one warp of the warpgroup and complete on done[g mod NA].  MMAs
+// from different threads are not ordered among themselves, so every stage of an
+// accumulation segment is issued by the same warp: warp (segment mod 4).
+// iteration g waits for stage g - NA, which frees A buffer g mod NA and makes
+// the accumulation segments that ended in stage g - NA readable.  With
+// NA = 3 a segment covers two stages (two D buffers suffice), with NA = 2 it
+// covers at most one (four D buffers).
+template <int MODE, int R, int NA>
 __global__ void __launch_bounds__(kThreads, 1) ffn_decode_kernel(const FfnParams p) {
-  constexpr int NB = MODE == 0 ? 4 : 8;
-  extern __shared__ __align__(128) uint8_t smem[];
+  constexpr int ND = NA == 3 ? 2 : 4;
+  constexpr int SPS = NA == 3 ? 2 : 1;    // stages per accumulation segment (at least)
+  constexpr int kD0 = 32 * NA;            // first D column of a warpgroup
+  static_assert(32 * NA + 16 * ND <= kColsPerWG, "TMEM columns per warpgroup");
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
+  const Layout L = make_layout(p.K, p.nB);
+  uint8_t* Bs = smem + L.b_off;
+  const uint32_t b_bytes = (uint32_t)p.K * BN * 2;
+  float* red = reinterpret_cast<float*>(smem + L.red_off);
+  uint64_t* a_full = reinterpret_cast<uint64_t*>(smem + L.bar_off);   // [kWG][3]: the 4 warps stored stage A
+  uint64_t* done = a_full + kWG * 3;                                  // [kWG][3]: the stage's MMAs completed
+  Group* groups = reinterpret_cast<Group*>(smem + L.grp_off);
+  uint32_t* tmem_base_p = reinterpret_cast<uint32_t*>(smem + L.misc_off);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L.misc_off + 4);
+
   int n_act = *p.n_active;
   n_act = n_act < 0 ? 0 : (n_act > p.amax ? p.amax : n_act);
   const int ngroups = n_act + 1;
-  const int upe = p.n_out / kRows;                 // units per expert
+  const int upe = p.n_out / BM;
   const int U = ngroups * upe;
   const int ub = (int)((long long)blockIdx.x * U / gridDim.x);
   const int ue = (int)((long long)(blockIdx.x + 1) * U / gridDim.x);
   if (ub >= ue) return;
 
-  uint8_t* stages = smem;
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + (size_t)p.nstage * p.stage_bytes);
-  uint64_t* empty = full + p.nstage;
-  uint64_t* red_full = empty + p.nstage;    // [2] partials of a unit written by the consumer warps
-  uint64_t* red_empty = red_full + 2;       // [2] the reducer has read them
-  float* red = reinterpret_cast<float*>(red_empty + 2);
-  Group* groups = reinterpret_cast<Group*>(red + 2 * kNW * kRedWarp);
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(groups + kMaxGroups);
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int wg = tid >> 7, r = tid & 127, wq = warp & 3;
 
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int tid = threadIdx.x;
-  // Only the groups this CTA's units touch are needed; filling all is cheap.
+  // per-CTA table of the groups (expert, pointers, output rows)
   for (int a = tid; a < ngroups; a += blockDim.x) {
-    Group gr;
-    gr.e = a < n_act ? __ldg(p.active + a) : p.E;
-    gr.w = nullptr;
-    gr.s = nullptr;
-    gr.flags = 0;
-    if (gr.e >= 0 && gr.e <= p.E) {
-      const qre_slot* sl = p.slots + gr.e;
-      gr.w = MODE == 0 ? sl->w_gate_up : sl->w_down;
-      gr.s = MODE == 0 ? sl->s_gate_up : sl->s_down;
-      const bool ok = gr.w && gr.s &&
-                      ((reinterpret_cast<uintptr_t>(gr.w) | reinterpret_cast<uintptr_t>(gr.s)) & 15) == 0;
-      gr.flags = (ok ? 1 : 0) | (sl->tier != 0 ? 2 : 0);
+    const int e = a < n_act ? __ldg(p.active + a) : p.E;
+    const uint8_t* w = nullptr;
+    const uint16_t* sc = nullptr;
+    int flags = 0;
+    if (e >= 0 && e <= p.E) {
+      const qre_slot* sl = p.slots + e;
+      w = MODE == 0 ? sl->w_gate_up : sl->w_down;
+      sc = MODE == 0 ? sl->s_gate_up : sl->s_down;
+      flags = (w && sc && ((reinterpret_cast<uintptr_t>(w) | reinterpret_cast<uintptr_t>(sc)) & 15) == 0) ? 1 : 0;
     }
     Group& dst = groups[a];
-    dst.w = gr.w;
-    dst.s = gr.s;
-    dst.e = gr.e;
-    dst.flags = gr.flags;
+    dst.w = w;
+    dst.s = sc;
+    dst.e = e;
+    dst.flags = flags;
 #pragma unroll
     for (int n = 0; n < kTok; ++n) dst.outq[n] = (MODE == 1 && a == n_act && n < p.T) ? p.T * p.k + n : -1;
-    if (MODE == 1 && a < n_act && (gr.flags & 1)) {
-      const int lo = __ldg(p.offsets + gr.e), hi = __ldg(p.offsets + gr.e + 1);
+    if (MODE == 1 && a < n_act && flags) {
+      const int lo = __ldg(p.offsets + e), hi = __ldg(p.offsets + e + 1);
       for (int q = lo; q < hi && q < lo + kTok; ++q) {
         const int tk = __ldg(p.perm + q) / p.k;
         if (tk >= 0 && tk < kTok) dst.outq[tk] = q;
@@ -273,254 +193,352 @@ __global__ void __launch_bounds__(kThreads, 1) ffn_decode_kernel(const FfnParams
     }
   }
   if (tid == 0) {
-    for (int s = 0; s < p.nstage; ++s) {
-      mbar_init(&full[s], 1);                  // the producer's expect_tx arrival
-      mbar_init(&empty[s], p.aw / p.nparts);   // one arrival per consumer warp of the part
-    }
-    for (int b = 0; b < 2; ++b) {
-      mbar_init(&red_full[b], p.aw);
-      mbar_init(&red_empty[b], 1);
+    for (int i = 0; i < kWG * 3; ++i) {
+      mbar_init(&a_full[i], 4);
+      mbar_init(&done[i], 1);
     }
     *abort_flag = 0;
     fence_barrier_init();
   }
-  __syncthreads();
-
-  const int part_chunks = (p.K / 32) / p.nparts;
-  const uint32_t scale_bytes = kRows * (p.K / p.G) * 2;
-
-  if (warp == kProducerWarp) {
-    // ---------------- producer: per part-stage, lane r issues the 1-D bulk (TMA)
-    // copy of row r and lane 0 the scales, so the 33 copies of a stage leave in
-    // one warp-wide instruction instead of 33 serial ones from a single thread.
-    const size_t row_bytes = p.K / 2;
-    int it = 0;
-    for (int u = ub; u < ue; ++u) {
-      const int a = u / upe, r0 = (u - a * upe) * kRows;
-      const Group& gr = groups[a];
-      if ((gr.flags & 3) != 1) continue;   // skipped or host-resident
-      bool stop = false;
-      for (int part = 0; part < p.nparts; ++part, ++it) {
-        const int s = it % p.nstage;
-        int ok = 1;
-        if (lane == 0) {
-          ok = mbar_wait_bounded(&empty[s], ((it / p.nstage) & 1) ^ 1, abort_flag, p.status) ? 1 : 0;
-          if (ok) mbar_arrive_expect_tx(&full[s], kRows * p.part_bytes + scale_bytes);
-        }
-        if (!__shfl_sync(0xffffffffu, ok, 0)) {   // warp-uniform
-          stop = true;
-          break;
-        }
-        uint8_t* dst = stages + (size_t)s * p.stage_bytes;
-        const uint8_t* src = gr.w + (size_t)r0 * row_bytes + (size_t)part * p.part_bytes;
-        bulk_copy_g2s(dst + lane * p.pitch, src + lane * row_bytes, p.part_bytes, &full[s]);   // kRows == 32
-        if (lane == 0)
-          bulk_copy_g2s(dst + kRows * p.pitch, gr.s + (size_t)r0 * (p.K / p.G), scale_bytes, &full[s]);
+  if (warp == 0) {
+    __syncwarp();
+    tmem_alloc(tmem_base_p, kWG * kColsPerWG);
+    tmem_relinquish();
+  }
+  const int a_first = ub / upe;
+  if constexpr (MODE == 0) {
+    // B = tokens: rows 0-7 fp16 high parts, 8-15 remainders.  Rows of tokens
+    // n >= T are left as they are: they only feed accumulator columns n, n + 8,
+    // which nothing reads.
+    for (int i = tid; i < p.T * (p.K / 8); i += blockDim.x) {
+      const int n = i / (p.K / 8), g8 = i - n * (p.K / 8);
+      const uint4 v = __ldg(reinterpret_cast<const uint4*>(p.x + (size_t)n * p.H + 8 * g8));
+      const uint32_t wv[4] = {v.x, v.y, v.z, v.w};
+      float f[8];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        f[2 * j] = bf16_bits_to_float(wv[j] & 0xFFFFu);
+        f[2 * j + 1] = bf16_bits_to_float(wv[j] >> 16);
       }
-      if (stop) break;
+      uint32_t hi[4], lo[4];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {   // pair (x_j, x_{j+4})
+        __half h0, l0, h1, l1;
+        split_half(f[j], h0, l0);
+        split_half(f[j + 4], h1, l1);
+        hi[j] = h2_as_u32(__halves2half2(h0, h1));
+        lo[j] = h2_as_u32(__halves2half2(l0, l1));
+      }
+      *reinterpret_cast<uint4*>(Bs + b_offset(n, 8 * g8)) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+      *reinterpret_cast<uint4*>(Bs + b_offset(8 + n, 8 * g8)) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
     }
-    // Every issued copy must land before the CTA exits (also after an abort).
-    if (lane == 0) {
-      const int first = it > p.nstage ? it - p.nstage : 0;
-      for (int j = first; j < it; ++j)
-        mbar_wait_bounded(&full[j % p.nstage], (j / p.nstage) & 1, nullptr, p.status);
+  } else {
+    // B = h of the first nB experts of this CTA's range
+    const int a_last = (ue - 1) / upe;
+    for (int j = 0; j < p.nB && a_first + j <= a_last; ++j) load_h(Bs + j * b_bytes, p.hbuf, a_first + j, p.I, p.T);
+  }
+  fence_proxy_async_smem();
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+
+  const uint32_t tmem_wg = *tmem_base_p + wg * kColsPerWG;
+  const uint32_t tlane = (uint32_t)(32 * wq) << 16;   // this warp's TMEM lane quarter
+  const int Kq = p.K / p.kq;
+  const int nst = Kq / SK;
+  const bool active_wg = wg < p.kq;
+  const int k0 = wg * Kq;
+  const int KS = p.K / SK;              // chunks per row block
+  const int KG = p.K >> p.lgG;
+  const int segL = 1 << p.lgS;
+  const int spu = Kq >> p.lgS;          // accumulation segments per unit
+  const uint32_t idesc = umma_idesc_f16(BM, BN);
+  const uint32_t bbase0 = smem_addr(Bs);
+
+  // load cursor: the next stage to prefetch (unit lu, stage lst)
+  int lu = ub, lst = 0;
+  const uint4* lptr = nullptr;
+  const unsigned short* lsp = nullptr;
+  auto cursor_unit = [&](int u) {
+    const int a = u / upe, m0 = (u - a * upe) * BM;
+    const Group& gr = groups[a];
+    if (gr.flags & 1) {
+      lptr = reinterpret_cast<const uint4*>(gr.w + ((size_t)(m0 / BM) * KS + k0 / SK) * kChunk) + r;
+      lsp = reinterpret_cast<const unsigned short*>(gr.s) + (size_t)(m0 / BM) * KG * BM + r;
+    } else {
+      lptr = nullptr;
+      lsp = nullptr;
     }
-    return;
+  };
+  cursor_unit(lu);
+
+  uint4 ring[R][2];
+  uint32_t sring[R];   // the stage's two scales (elements 0-31 low half, 32-63 high half)
+  auto load_next = [&](uint4 (&dst)[2], uint32_t& sdst) {
+    if (lptr) {
+      dst[0] = __ldg(lptr + lst * (kChunk / 16));
+      dst[1] = __ldg(lptr + lst * (kChunk / 16) + kChunk / 32);
+      const int kk = k0 + lst * SK;
+      sdst = (uint32_t)__ldg(lsp + (size_t)(kk >> p.lgG) * BM) |
+             ((uint32_t)__ldg(lsp + (size_t)((kk + 32) >> p.lgG) * BM) << 16);
+    } else {
+      dst[0] = dst[1] = make_uint4(0x88888888u, 0x88888888u, 0x88888888u, 0x88888888u);
+      sdst = 0;
+    }
+    if (++lst == nst) {
+      lst = 0;
+      if (++lu < ue) cursor_unit(lu);
+    }
+  };
+  if (active_wg) {
+#pragma unroll
+    for (int j = 0; j < R; ++j)
+      if (lu < ue) load_next(ring[j], sring[j]);
   }
 
-  if (warp == kReducerWarp) {
-    // ---------------- reducer: adds the consumer warps' partials of each unit in
-    // fixed warp order (deterministic) while the consumers go on with the next
-    // unit; two partial buffers.
-    int ru = 0;
-    for (int u = ub; u < ue; ++u) {
-      const int a = u / upe, r0 = (u - a * upe) * kRows;
-      const Group& gr = groups[a];
-      if (!(gr.flags & 1)) continue;
-      const int buf = ru & 1;
-      int ok = 1;
-      if (lane == 0) ok = mbar_wait_bounded(&red_full[buf], (ru >> 1) & 1, abort_flag, p.status) ? 1 : 0;
-      ok = __shfl_sync(0xffffffffu, ok, 0);
-      const float* rb = red + (size_t)buf * kNW * kRedWarp;
-      if (ok) {
-        if constexpr (MODE == 0) {
-          // gate row r and up row r of token n -> h = silu(g) * u, stored as the
-          // down kernel's B fragment: feature f = r0/2 + r of chunk f/32, lane
-          // 4n + (f%32)/8, pair (f%8)%4, half (f%8)/4; high part then remainder.
+  float acc[kTok];
+  // Adds the accumulation segments that end in unit stage `st` (scales sp) to
+  // acc; the stage's MMAs have completed.
+  auto readback = [&](int st, int ul, uint32_t sp) {
 #pragma unroll
-          for (int j = 0; j < 4; ++j) {
-            const int o = lane + 32 * j, n = o >> 4, r = o & 15;
-            float gs = 0.f, us = 0.f;
+    for (int q = 0; q < 4; ++q) {
+      const int kk = st * SK + 16 * q;
+      if (((kk + 16) & (segL - 1)) == 0) {
+        const int d = (ul * spu + (kk >> p.lgS)) & (ND - 1);
+        uint32_t dv[16];
+        tmem_ld_32x32b_x16(tlane + tmem_wg + kD0 + 16 * d, dv);
+        tmem_ld_wait();
+        const float sc = __half2float(__ushort_as_half((unsigned short)(q < 2 ? sp & 0xFFFFu : sp >> 16)));
 #pragma unroll
-            for (int w = 0; w < kNW; ++w) {
-              if (w < p.aw) {
-                gs += rb[w * kRedWarp + n * kRedStride + r];
-                us += rb[w * kRedWarp + kRedTile + n * kRedStride + r];
-              }
+        for (int n = 0; n < kTok; ++n) acc[n] = fmaf(sc, __uint_as_float(dv[n]) + __uint_as_float(dv[n + 8]), acc[n]);
+      }
+    }
+  };
+  auto wait_done = [&](int gs) {
+    mbar_wait_bounded(&done[wg * 3 + gs % NA], (gs / NA) & 1, abort_flag, p.status);
+    __syncwarp();
+    tc_fence_after();
+  };
+  // the warp that issues global stage gs
+  auto issuer = [&](int gs) { return ((gs / SPS) & 3) == wq; };
+  // lane 0 of the issuing warp: the four MMAs of global stage gs (unit stage st)
+  auto issue = [&](int gs, int st, int ul, uint32_t bbase) {
+    mbar_wait_bounded(&a_full[wg * 3 + gs % NA], (gs / NA) & 1, abort_flag, p.status);
+    tc_fence_after();
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const int kk = st * SK + 16 * q;
+      const int d = (ul * spu + (kk >> p.lgS)) & (ND - 1);
+      const int kb = k0 + kk;
+      const uint64_t bdesc = umma_desc_sw128(bbase + (uint32_t)((kb >> 6) * (BN * 128) + (kb & 63) * 2));
+      umma_f16_tmem_a(tmem_wg + kD0 + 16 * d, tmem_wg + (gs % NA) * 32 + 8 * q, bdesc, idesc,
+                      (kk & (segL - 1)) ? 1u : 0u);
+    }
+    umma_commit(&done[wg * 3 + gs % NA]);
+  };
+
+  int g = 0, buf = 0, cur_a = a_first, bsel = 0;
+  for (int u = ub, ul = 0; u < ue; ++u, ++ul) {
+    const int a = u / upe, m0 = (u - a * upe) * BM;
+    const Group& gr = groups[a];
+    if (!(gr.flags & 1) && tid == 0) set_status(p.status, QRE_DEV_NULL_SLOT);
+    if constexpr (MODE == 1) {
+      if (a != cur_a) {
+        cur_a = a;
+        const int la = a - a_first;
+        bsel = la % p.nB;
+        if (la >= p.nB) {   // buffer bsel held expert la - nB, whose MMAs all completed: refill it
+          __syncthreads();
+          load_h(Bs + bsel * b_bytes, p.hbuf, a, p.I, p.T);
+          fence_proxy_async_smem();
+          __syncthreads();
+        }
+      }
+    }
+    const uint32_t bbase = bbase0 + bsel * b_bytes;
+#pragma unroll
+    for (int n = 0; n < kTok; ++n) acc[n] = 0.f;
+
+    if (active_wg) {
+      uint32_t h1 = 0, h2 = 0, h3 = 0;   // scales of unit stages st-1, st-2, st-3
+      for (int st0 = 0; st0 < nst; st0 += R) {
+#pragma unroll
+        for (int j = 0; j < R; ++j) {
+          const int st = st0 + j, gs = g + st, ab = gs % NA;
+          // (1) stage gs - NA completed: A buffer ab is free, its segments are readable
+          if (gs >= NA) wait_done(gs - NA);
+          // (2) decode 64 nibbles into 32 fp16 pairs of this row, store them in TMEM
+          {
+            const uint32_t wd[8] = {ring[j][0].x, ring[j][0].y, ring[j][0].z, ring[j][0].w,
+                                    ring[j][1].x, ring[j][1].y, ring[j][1].z, ring[j][1].w};
+            uint32_t av[32];
+#pragma unroll
+            for (int w = 0; w < 8; ++w) {
+              uint32_t pr[4];
+              decode_nibbles(wd[w], pr);
+              av[4 * w + 0] = pr[0];
+              av[4 * w + 1] = pr[1];
+              av[4 * w + 2] = pr[2];
+              av[4 * w + 3] = pr[3];
             }
-            const float h = silu_f32(gs) * us;
-            const __half hh = __float2half_rn(h);
-            const __half hl = __float2half_rn(h - __half2float(hh));
-            const int f = r0 / 2 + r;
-            const int c = f >> 5, tt = (f & 31) >> 3, i8 = f & 7;
-            const size_t base = (((size_t)a * (p.I / 32) + c) * 32 + (4 * n + tt)) * 16;
-            p.hfrag[base + (i8 & 3) * 2 + (i8 >> 2)] = __half_as_ushort(hh);
-            p.hfrag[base + (4 + (i8 & 3)) * 2 + (i8 >> 2)] = __half_as_ushort(hl);
+            tmem_st_32x32b_x32(tlane + tmem_wg + ab * 32, av);
+          }
+          // (3) while the store drains: segments of unit stage st - NA
+          if (st >= NA) readback(st - NA, ul, NA == 3 ? h3 : h2);
+          // (4) scales of this stage, prefetch R stages ahead
+          h3 = h2;
+          h2 = h1;
+          h1 = sring[j];
+          if (lu < ue) load_next(ring[j], sring[j]);
+          // (5) publish the stored A
+          tmem_st_wait();
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&a_full[wg * 3 + ab]);
+          // (6) issue the previous stage if it is this warp's turn
+          if (st >= 1 && issuer(gs - 1) && lane == 0) issue(gs - 1, st - 1, ul, bbase);
+          __syncwarp();
+        }
+      }
+      // unit end: issue the last stage, wait for the unit's last stages, read them back
+      const int gl = g + nst - 1;
+      if (issuer(gl) && lane == 0) issue(gl, nst - 1, ul, bbase);
+      __syncwarp();
+      const int first = nst > NA ? nst - NA : 0;
+      for (int st = first; st < nst; ++st) {
+        wait_done(g + st);
+        const int back = nst - st;   // 1 = the last stage
+        readback(st, ul, back == 1 ? h1 : (back == 2 ? h2 : h3));
+      }
+      tc_fence_before();
+      float* rw = red + ((size_t)(buf * kWG + wg) * BM + r) * kTok;
+#pragma unroll
+      for (int n = 0; n < kTok; n += 4)
+        *reinterpret_cast<float4*>(rw + n) = make_float4(acc[n], acc[n + 1], acc[n + 2], acc[n + 3]);
+    }
+    g += nst;
+    __syncthreads();
+    {
+      // epilogue: thread (wg, r) finishes row r for tokens 2wg, 2wg + 1
+      const int n0 = 2 * wg;
+      float v0 = 0.f, v1 = 0.f;
+      for (int w = 0; w < p.kq; ++w) {
+        const float* rr = red + ((size_t)(buf * kWG + w) * BM + r) * kTok + n0;
+        v0 += rr[0];
+        v1 += rr[1];
+      }
+      if (gr.flags & 1) {
+        if constexpr (MODE == 0) {
+          // lanes 0-15 of each warp hold gate rows, lanes 16-31 the matching up rows
+          const float up0 = __shfl_down_sync(0xffffffffu, v0, 16);
+          const float up1 = __shfl_down_sync(0xffffffffu, v1, 16);
+          const int f = m0 / 2 + 16 * (r >> 5) + (r & 15);
+          const int pos = (f & ~7) | (((f & 3) << 1) | ((f >> 2) & 1));
+          __half* hb = p.hbuf + (size_t)a * 2 * kTok * p.I;
+          if ((lane & 16) == 0) {
+            __half hh, hl;
+            if (n0 < p.T) {
+              split_half(silu_f32(v0) * up0, hh, hl);
+              hb[(size_t)n0 * p.I + pos] = hh;
+              hb[(size_t)(kTok + n0) * p.I + pos] = hl;
+            }
+            if (n0 + 1 < p.T) {
+              split_half(silu_f32(v1) * up1, hh, hl);
+              hb[(size_t)(n0 + 1) * p.I + pos] = hh;
+              hb[(size_t)(kTok + n0 + 1) * p.I + pos] = hl;
+            }
           }
         } else {
-#pragma unroll
-          for (int j = 0; j < 8; ++j) {
-            const int o = lane + 32 * j, i = o >> 7, n = (o >> 4) & 7, r = o & 15;
-            float v = 0.f;
-#pragma unroll
-            for (int w = 0; w < kNW; ++w)
-              if (w < p.aw) v += rb[w * kRedWarp + i * kRedTile + n * kRedStride + r];
-            const int q = gr.outq[n];
-            if (q >= 0) p.expert_out[(size_t)q * p.H + r0 + 16 * i + r] = v;
-          }
+          const int q0 = gr.outq[n0], q1 = gr.outq[n0 + 1];
+          if (q0 >= 0) p.expert_out[(size_t)q0 * p.H + m0 + r] = v0;
+          if (q1 >= 0) p.expert_out[(size_t)q1 * p.H + m0 + r] = v1;
         }
       }
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&red_empty[buf]);
-      ++ru;
     }
-    return;
+    buf ^= 1;
   }
 
-  // ---------------- consumers
-  const int g = lane >> 2, t = lane & 3;
-  if (warp >= p.aw) return;                 // no K range for this warp (small shapes)
-  const int c0 = warp * CPW;
-  const int wpart = warp / (p.aw / p.nparts);
-  uint32_t bfr[CPW][NB];
-  if constexpr (MODE == 0) load_x_frags<CPW>(p, c0, g, t, bfr);
-  int cur_a = -1, units0 = 0, ru = 0;
-  for (int u = ub; u < ue; ++u) {
-    const int a = u / upe, r0 = (u - a * upe) * kRows;
-    const Group& gr = groups[a];
-    if (!(gr.flags & 1)) {
-      if (threadIdx.x == 0) set_status(p.status, QRE_DEV_NULL_SLOT);
-      continue;
-    }
-    const bool host = gr.flags & 2;
-    if constexpr (MODE == 1) {
-      if (a != cur_a) load_h_frags<CPW>(p, a, c0, lane, bfr);
-    }
-    cur_a = a;
-    float acc[kTiles][4];
-#pragma unroll
-    for (int i = 0; i < kTiles; ++i) acc[i][0] = acc[i][1] = acc[i][2] = acc[i][3] = 0.f;
-    if (!host) {
-      const int it = units0 * p.nparts + wpart;
-      const int s = it % p.nstage;
-      const bool have = mbar_wait_bounded(&full[s], (it / p.nstage) & 1, abort_flag, p.status);
-      const uint32_t wb = after_wait(smem_addr(stages + (size_t)s * p.stage_bytes));
-      if (have)
-        unit_dot<CPW, NB, true>(nullptr, wb, p.pitch, nullptr, wb + kRows * p.pitch, p.K / p.G, c0,
-                                wpart * part_chunks, p.gc, g, t, bfr, acc);
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&empty[s]);
-      ++units0;
-    } else {
-      unit_dot<CPW, NB, false>(gr.w + (size_t)r0 * (p.K / 2), 0, p.K / 2, gr.s + (size_t)r0 * (p.K / p.G), 0,
-                               p.K / p.G, c0, 0, p.gc, g, t, bfr, acc);
-    }
-    const int buf = ru & 1;
-    int ok = 1;
-    if (lane == 0) ok = mbar_wait_bounded(&red_empty[buf], ((ru >> 1) & 1) ^ 1, abort_flag, p.status) ? 1 : 0;
-    __syncwarp();
-    (void)ok;
-    float* rw = red + (size_t)(buf * kNW + warp) * kRedWarp;
-#pragma unroll
-    for (int i = 0; i < kTiles; ++i) {
-      rw[i * kRedTile + (2 * t) * kRedStride + g] = acc[i][0];
-      rw[i * kRedTile + (2 * t + 1) * kRedStride + g] = acc[i][1];
-      rw[i * kRedTile + (2 * t) * kRedStride + g + 8] = acc[i][2];
-      rw[i * kRedTile + (2 * t + 1) * kRedStride + g + 8] = acc[i][3];
-    }
-    __syncwarp();
-    if (lane == 0) mbar_arrive(&red_full[buf]);
-    ++ru;
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) {
+    tc_fence_after();
+    tmem_dealloc(*tmem_base_p, kWG * kColsPerWG);
   }
 }
 
-struct Plan {
-  int cpw = 0, aw = 0, gc = 0, nparts = 1, pitch = 0, part_bytes = 0, stage_bytes = 0, nstage = 0;
-  size_t smem = 0;
-  bool ok = false;
-};
+int ilog2(int v) {
+  int l = 0;
+  while ((1 << (l + 1)) <= v) ++l;
+  return l;
+}
 
-Plan make_plan(int K, int G, int smem_budget) {
-  Plan pl;
-  const int nchunks = K / 32;
-  pl.gc = G / 32;
-  for (int c : {1, 2, 4, 8}) {
-    if (c < pl.gc || c % pl.gc || nchunks % c || nchunks / c > kNW) continue;
-    pl.cpw = c;
-    break;
+// Warpgroups that split K: whole stages each, and accumulation segments that
+// are either whole groups or whole K slices.
+int pick_kq(int K, int G) {
+  for (int kq : {4, 2, 1}) {
+    const int Kq = K / kq;
+    if (K % kq == 0 && Kq % SK == 0 && (Kq % G == 0 || G % Kq == 0)) return kq;
   }
-  if (!pl.cpw) return pl;
-  pl.aw = nchunks / pl.cpw;
-  pl.nparts = (pl.aw % 2 == 0) ? 2 : 1;
-  pl.part_bytes = K / 2 / pl.nparts;
-  pl.pitch = ((pl.part_bytes + 127) / 128) * 128 + 16;
-  pl.stage_bytes = kRows * pl.pitch + kRows * (K / G) * 2;
-  pl.stage_bytes = (pl.stage_bytes + 127) / 128 * 128;
-  const int fixed = 4 * 8 + 2 * kNW * kRedWarp * 4 + kMaxGroups * (int)sizeof(Group) + 16;
-  int ns = (smem_budget - fixed) / (pl.stage_bytes + 16);
-  if (ns > 8) ns = 8;
-  if (ns < 2) return pl;
-  pl.nstage = ns;
-  pl.smem = (size_t)ns * pl.stage_bytes + (size_t)ns * 16 + fixed;
-  pl.ok = true;
-  return pl;
+  return 0;
+}
+
+int smem_needed(int K, int nB) {
+  const size_t b = make_layout(K, nB).bytes;
+  // at least ~120 KB so that no second CTA (and no second TMEM allocation) shares an SM
+  return (int)(b > 120 * 1024 ? b : 120 * 1024);
+}
+
+template <int MODE, int R, int NA>
+cudaError_t launch_r(const FfnParams& p, int grid, int smem, cudaStream_t stream) {
+  cudaError_t err = ensure_smem_limit(reinterpret_cast<const void*>(ffn_decode_kernel<MODE, R, NA>), smem);
+  if (err != cudaSuccess) return err;
+  ffn_decode_kernel<MODE, R, NA><<<grid, kThreads, smem, stream>>>(p);
+  return cudaGetLastError();
+}
+
+template <int MODE, int NA>
+cudaError_t launch_na(const FfnParams& p, int nst, int grid, int smem, cudaStream_t stream) {
+  if (nst % 4 == 0) return launch_r<MODE, 4, NA>(p, grid, smem, stream);
+  if (nst % 2 == 0) return launch_r<MODE, 2, NA>(p, grid, smem, stream);
+  return launch_r<MODE, 1, NA>(p, grid, smem, stream);
 }
 
 template <int MODE>
-cudaError_t launch_mode(const FfnParams& base, const Plan& pl, int grid, cudaStream_t stream) {
+cudaError_t launch_mode(const FfnParams& base, int grid, cudaStream_t stream) {
   FfnParams p = base;
-  p.gc = pl.gc;
-  p.aw = pl.aw;
-  p.nparts = pl.nparts;
-  p.pitch = pl.pitch;
-  p.part_bytes = pl.part_bytes;
-  p.stage_bytes = pl.stage_bytes;
-  p.nstage = pl.nstage;
-  void (*kern)(const FfnParams) = nullptr;
-  switch (pl.cpw) {
-    case 1: kern = ffn_decode_kernel<MODE, 1>; break;
-    case 2: kern = ffn_decode_kernel<MODE, 2>; break;
-    case 4: kern = ffn_decode_kernel<MODE, 4>; break;
-    case 8: kern = ffn_decode_kernel<MODE, 8>; break;
-    default: return cudaErrorInvalidValue;
-  }
-  cudaError_t err = ensure_smem_limit(reinterpret_cast<const void*>(kern), (int)pl.smem);
-  if (err != cudaSuccess) return err;
-  kern<<<grid, kThreads, pl.smem, stream>>>(p);
-  return cudaGetLastError();
+  p.kq = pick_kq(p.K, p.G);
+  const int Kq = p.K / p.kq;
+  p.lgG = ilog2(p.G);
+  p.lgS = ilog2(Kq < p.G ? Kq : p.G);
+  const int budget = device_max_smem_optin();
+  p.nB = (MODE == 1 && smem_needed(p.K, 2) <= budget) ? 2 : 1;
+  const int smem = smem_needed(p.K, p.nB);
+  const int nst = Kq / SK;
+  // segments of two stages (G = 128 within a K slice): three A buffers, two D buffers
+  if (p.lgS == 7) return launch_na<MODE, 3>(p, nst, grid, smem, stream);
+  return launch_na<MODE, 2>(p, nst, grid, smem, stream);
 }
 
 }  // namespace
 
 bool ffn_decode_supported(const qre_layer_shape& s) {
   const int budget = device_max_smem_optin();
-  return make_plan(s.hidden, s.group, budget).ok && make_plan(s.inter, s.group, budget).ok;
+  const bool pow2 = s.group == 32 || s.group == 64 || s.group == 128;
+  return pow2 && pick_kq(s.hidden, s.group) && pick_kq(s.inter, s.group) && (2 * s.inter) % BM == 0 &&
+         s.hidden % BM == 0 && smem_needed(s.hidden, 1) <= budget && smem_needed(s.inter, 1) <= budget;
 }
 
 size_t ffn_ws_bytes(const qre_layer_shape& s, int T) {
   const long long pk = (long long)T * s.top_k;
   const long long amax = pk < s.n_experts ? pk : s.n_experts;
-  return (size_t)(amax + 1) * (s.inter / 32) * 32 * 16 * sizeof(uint16_t);
+  return (size_t)(amax + 1) * 2 * kTok * s.inter * sizeof(__half);
 }
 
 cudaError_t launch_ffn_decode(const qre_layer_shape& s, int T, const uint16_t* x, const qre_slot* slots,
                               const int32_t* offsets, const int32_t* perm, const int32_t* active,
                               const int32_t* n_active, float* expert_out, void* ws, int* status,
                               cudaStream_t stream) {
-  const int budget = device_max_smem_optin();
-  const Plan gu_plan = make_plan(s.hidden, s.group, budget);
-  const Plan dn_plan = make_plan(s.inter, s.group, budget);
-  if (!gu_plan.ok || !dn_plan.ok) return cudaErrorInvalidValue;
+  if (!ffn_decode_supported(s)) return cudaErrorInvalidValue;
   FfnParams p{};
   p.H = s.hidden;
   p.I = s.inter;
@@ -534,26 +552,23 @@ cudaError_t launch_ffn_decode(const qre_layer_shape& s, int T, const uint16_t* x
   p.perm = perm;
   p.active = active;
   p.n_active = n_active;
-  p.hfrag = static_cast<uint16_t*>(ws);
+  p.hbuf = static_cast<__half*>(ws);
   p.expert_out = expert_out;
   p.status = status;
   const long long pk = (long long)T * s.top_k;
-  const int amax = (int)(pk < s.n_experts ? pk : s.n_experts);
-  p.amax = amax;
+  p.amax = (int)(pk < s.n_experts ? pk : s.n_experts);
   const int sms = device_sm_count();
 
   p.K = s.hidden;
   p.n_out = 2 * s.inter;
-  long long units = (long long)(amax + 1) * (p.n_out / kRows);
-  int grid = (int)(units < sms ? units : sms);
-  cudaError_t err = launch_mode<0>(p, gu_plan, grid, stream);
+  long long units = (long long)(p.amax + 1) * (p.n_out / BM);
+  cudaError_t err = launch_mode<0>(p, (int)(units < sms ? units : sms), stream);
   if (err != cudaSuccess) return err;
 
   p.K = s.inter;
   p.n_out = s.hidden;
-  units = (long long)(amax + 1) * (p.n_out / kRows);
-  grid = (int)(units < sms ? units : sms);
-  return launch_mode<1>(p, dn_plan, grid, stream);
+  units = (long long)(p.amax + 1) * (p.n_out / BM);
+  return launch_mode<1>(p, (int)(units < sms ? units : sms), stream);
 }
 
 }  // namespace qre

@@ -312,16 +312,21 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_gemm_kernel(const Prefill
       const uint16_t* sb = MODE == 0 ? sl->s_gate_up : sl->s_down;
       const bool valid = wb && sb && ((reinterpret_cast<uintptr_t>(wb) | reinterpret_cast<uintptr_t>(sb)) & 15) == 0;
       if (!valid && dq == 0) set_status(p.status, QRE_DEV_NULL_SLOT);
-      // 16 bytes (32 nibbles) of row m0 + r per stage, and the scale of its group
-      const uint4* wrow = valid ? reinterpret_cast<const uint4*>(wb + (size_t)(tl.m0 + r) * (p.K / 2)) + hf : nullptr;
-      const uint16_t* srow = valid ? sb + (size_t)(tl.m0 + r) * KG : nullptr;
+      // 16 bytes (32 nibbles) of row m0 + r per stage, and the scale of its group:
+      // stage kb of the tile is the 4 KB chunk (m0 / 128, kb); this thread's
+      // 16 bytes sit at 2048 * hf + 16 * r in it, and the scale of group g of
+      // the tile's rows at (m0 / 128 * KG + g) * 128 + r
+      const uint4* wrow = valid ? reinterpret_cast<const uint4*>(wb + (size_t)(tl.m0 / BM) * (p.K / BK) * 4096) +
+                                      128 * hf + r
+                                : nullptr;
+      const uint16_t* srow = valid ? sb + (size_t)(tl.m0 / BM) * KG * BM + r : nullptr;
       uint4 ring[4];
       unsigned short sring[4];
 #pragma unroll
       for (int j = 0; j < 4; ++j) {
         if (valid && j < KB) {
-          ring[j] = __ldg(wrow + 2 * j);
-          sring[j] = __ldg(reinterpret_cast<const unsigned short*>(srow) + (j * BK + 32 * hf) / p.G);
+          ring[j] = __ldg(wrow + 256 * j);
+          sring[j] = __ldg(reinterpret_cast<const unsigned short*>(srow) + (j * BK + 32 * hf) / p.G * BM);
         } else {
           ring[j] = make_uint4(0x88888888u, 0x88888888u, 0x88888888u, 0x88888888u);
           sring[j] = 0;
@@ -348,8 +353,8 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_gemm_kernel(const Prefill
             mbar_arrive(&full_a[s]);
             ++it;
             if (valid && kb + 4 < KB) {
-              ring[j] = __ldg(wrow + 2 * (kb + 4));
-              sring[j] = __ldg(reinterpret_cast<const unsigned short*>(srow) + ((kb + 4) * BK + 32 * hf) / p.G);
+              ring[j] = __ldg(wrow + 256 * (kb + 4));
+              sring[j] = __ldg(reinterpret_cast<const unsigned short*>(srow) + ((kb + 4) * BK + 32 * hf) / p.G * BM);
             }
           }
         }

@@ -79,16 +79,34 @@ class ExpertArena:
                 self.view(e, n).copy_(t, non_blocking=False)
 
     def to_numpy(self, e: int) -> dict:
-        """The packed arrays of slot e on the host (for checks)."""
+        """The packed arrays of slot e on the host, row-major (for checks)."""
         H, I, G = self.H, self.I, self.G
-        import numpy as np
         out = {}
-        shapes = {"w_gate_up": ((2 * I, H // 2), np.uint8), "s_gate_up": ((2 * I, H // G), np.float16),
-                  "w_down": ((H, I // 2), np.uint8), "s_down": ((H, I // G), np.float16)}
-        for n, (shape, dt) in shapes.items():
-            raw = self.view(e, n).cpu().numpy()
-            out[n] = raw.view(dt).reshape(shape)
+        for n, (rows, cols) in {"w_gate_up": (2 * I, H), "w_down": (H, I)}.items():
+            out[n] = packed_rows(self.view(e, n).cpu().numpy(), rows, cols)
+        for n, (rows, cols) in {"s_gate_up": (2 * I, H), "s_down": (H, I)}.items():
+            out[n] = scale_rows(self.view(e, n).cpu().numpy(), rows, cols, G)
         return out
+
+
+def packed_rows(raw, rows: int, cols: int):
+    """Row-major [rows][cols/2] bytes from the library's tiled packed storage.
+
+    The storage holds 4 KB chunks, one per 128-row block and 64-column stage
+    (block-major); inside a chunk, the 16 bytes of columns 0-31 of each of the
+    128 rows in order, then the 16 bytes of columns 32-63.
+    """
+    import numpy as np
+    t = np.asarray(raw, dtype=np.uint8).reshape(rows // 128, cols // 64, 2, 128, 16)
+    return np.ascontiguousarray(t.transpose(0, 3, 1, 2, 4)).reshape(rows, cols // 2)
+
+
+def scale_rows(raw, rows: int, cols: int, G: int):
+    """Row-major fp16 [rows][cols/G] scales from the tiled storage: for each
+    128-row block and group, the 128 rows' scales in order."""
+    import numpy as np
+    t = np.asarray(raw).view(np.float16).reshape(rows // 128, cols // G, 128)
+    return np.ascontiguousarray(t.transpose(0, 2, 1)).reshape(rows, cols // G)
 
 
 class MoELayer:

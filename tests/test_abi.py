@@ -110,6 +110,13 @@ def test_other_argument_errors(lib):
     assert st == qre.QRE_ERR_UNSUPPORTED
     st, msg = _status(lambda: qre.qre_quantize_gate_up(24, 128, 32, A, A, A, A, stream=0))
     assert st == qre.QRE_ERR_INVALID_ARG
+    # the tiled storage needs whole 128-row blocks and 64-column stages
+    st, msg = _status(lambda: qre.qre_quantize(100, 128, 32, A, A, A, stream=0))
+    assert st == qre.QRE_ERR_INVALID_ARG and "128" in msg
+    st, msg = _status(lambda: qre.qre_quantize(128, 96, 32, A, A, A, stream=0))
+    assert st == qre.QRE_ERR_INVALID_ARG
+    st, msg = _status(lambda: qre.qre_quantize_gate_up(96, 128, 32, A, A, A, A, stream=0))
+    assert st == qre.QRE_ERR_INVALID_ARG
 
 
 def test_empty_calls_launch_nothing(lib):

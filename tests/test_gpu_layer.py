@@ -133,6 +133,22 @@ def test_token_order_invariance_bit_exact():
     np.testing.assert_array_equal(g2["y"], g1["y"][order])
 
 
+@pytest.mark.parametrize("cfg,T", [(MID, 1), (MID, 8), (ODD, 5),
+                                   (synthetic.LayerConfig("g32", 512, 256, 32, 4, 32, 8), 8)])
+def test_repeated_calls_bit_identical(cfg, T):
+    """The same call gives the same bits every time: the expert FFN's
+    accumulation order does not depend on scheduling (its segments span one or
+    two pipeline stages depending on the group size)."""
+    built = BuiltLayer(cfg.hidden, cfg.inter, cfg.n_experts, cfg.top_k, cfg.group, T, DEV, numpy_source(cfg))
+    x_bits, wr, _ = _inputs(cfg, T, step=9)
+    first = _run(built, x_bits, wr, None)
+    for _ in range(24):
+        again = _run(built, x_bits, wr, None)
+        np.testing.assert_array_equal(again["expert_out"], first["expert_out"])
+        np.testing.assert_array_equal(again["y"], first["y"])
+    assert qre.qre_read_device_status() == 0
+
+
 def test_zero_weight_expert_contributes_nothing():
     cfg = synthetic.CONFIGS["tiny"]
     built = BuiltLayer(cfg.hidden, cfg.inter, cfg.n_experts, cfg.top_k, cfg.group, 8, DEV, numpy_source(cfg))
@@ -182,6 +198,8 @@ def test_full_size_decode_one_token():
     x_bits, wr, _ = _inputs(cfg, 1, step=1)
     got = _run(built, x_bits, wr, None)
     _check_layer(built, got, built.oracle_layer(x_bits, wr, None))
+    for _ in range(10):   # and bit-identical on every repetition
+        np.testing.assert_array_equal(_run(built, x_bits, wr, None)["y"], got["y"])
 
 
 @pytest.mark.slow

@@ -23,20 +23,22 @@
 //   * One tcgen05.mma (A from tensor memory, B from shared memory, M=128, N=16,
 //     K=16) is cheap for the tensor core but takes a warp on the order of a
 //     hundred cycles to issue, while issues from different warps overlap.  So
-//     every warp issues: stage g of a warpgroup is issued by its warp g mod 4,
-//     once all four warps have arrived on the stage's mbarrier, and completes
-//     on one commit per stage; no warp waits for the others between stages.
-//   * B holds the tokens (T <= 8) in shared memory, 128-byte swizzled: rows 0-7
-//     the fp16 high parts, rows 8-15 the fp16 remainders (x - high), so the
-//     products stay accurate to about fp32.  The weights are exact codes, so the
-//     only rounding is the fp32 accumulation.
-//   * Every quantization group accumulates into its own buffer (four rotate); one
-//     stage later the owning threads read it back (tcgen05.ld), add the two
-//     halves and apply the group's fp16 scale in fp32.
-//   * The four warpgroups' partial rows are added in fixed order (deterministic);
-//     gate/up pairs each gate row with its up row (16 lanes apart, a shuffle) and
-//     stores h = silu(g) * u as fp16 high part and remainder for the down kernel;
-//     down writes the expert's output rows.
+//     every warp issues: the stages of a warpgroup are issued in turn by its
+//     four warps, one stage late, once all four warps have arrived on the
+//     stage's mbarrier, and complete on one commit per stage.
+//   * B holds the tokens (T <= 8) in shared memory, 128-byte swizzled: row 2n
+//     the fp16 high part of token n, row 2n + 1 the fp16 remainder (x - high),
+//     so the products stay accurate to about fp32.  The weights are exact codes,
+//     so the only rounding is the fp32 accumulation.
+//   * Every quantization group accumulates into its own buffer; a few stages
+//     later the owning threads read it back (tcgen05.ld; two columns for a
+//     single token, sixteen for eight), add the two halves and apply the
+//     group's fp16 scale in fp32.
+//   * The warpgroups' partial rows are added in fixed order (deterministic), one
+//     unit after they were handed over: gate/up pairs each gate row with its up
+//     row (16 lanes apart, a shuffle) and stores h = silu(g) * u as fp16 high
+//     part and remainder for the down kernel; down writes the expert's output
+//     rows.
 //   * Inside every group of 8 reduction elements the tokens and h are stored in
 //     the order the nibble decode yields weight pairs (0,4,1,5,2,6,3,7), which
 //     leaves every dot product unchanged.
@@ -71,7 +73,6 @@ struct FfnParams {
   int n_out;        // rows per expert: 2I (gate/up) or H (down)
   int kq;           // warpgroups sharing K (1, 2 or 4)
   int lgG;          // log2 G
-  int lgS;          // log2 of the accumulation segment: min(G, K / kq)
   int nB;           // B buffers in shared memory (down kernel: experts resident at once)
   int amax;         // largest possible number of active experts, min(E, T*k)
   const uint16_t* x;
@@ -80,7 +81,7 @@ struct FfnParams {
   const int32_t* perm;
   const int32_t* active;
   const int32_t* n_active;
-  __half* hbuf;       // [(amax+1)][2][kTok][I]: h high parts, then remainders (reordered in 8-groups)
+  __half* hbuf;       // [(amax+1)][2*kTok][I]: row 2n = h high part of token n, 2n+1 its remainder
   float* expert_out;  // [T*k + T][H]
   int* status;
 };
@@ -90,12 +91,12 @@ struct Layout {
   size_t bytes;
 };
 
-__host__ __device__ inline Layout make_layout(int K, int nB) {
+__host__ __device__ inline Layout make_layout(int K, int nB, int TT) {
   Layout L;
   L.b_off = 0;                                          // nB x (BN x K fp16, swizzled; 1024-aligned)
-  L.red_off = L.b_off + nB * K * BN * 2;                // 2 x kWG x BM x kTok fp32
-  L.bar_off = L.red_off + 2 * kWG * BM * kTok * 4;      // a_full[kWG][3], done[kWG][3]
-  L.grp_off = L.bar_off + kWG * 6 * 8;
+  L.red_off = L.b_off + nB * K * BN * 2;                // 2 x kWG x BM x TT fp32
+  L.bar_off = L.red_off + 2 * kWG * BM * TT * 4;        // a_full[kWG][3], done[kWG][3], red_full[2], red_empty[2]
+  L.grp_off = L.bar_off + (kWG * 6 + 4) * 8;
   L.misc_off = L.grp_off + kMaxGroups * (int)sizeof(Group);
   L.bytes = (size_t)L.misc_off + 16 + 1024;             // + alignment slack
   return L;
@@ -116,39 +117,100 @@ __device__ __forceinline__ void split_half(float v, __half& hi, __half& lo) {
   lo = __float2half_rn(v - __half2float(hi));
 }
 
-// h of group a (high parts and remainders of the first T tokens) into B buffer `dst`.
+// h of group a (rows 0 .. 2T-1: high part and remainder of each token) into B buffer `dst`.
 __device__ __forceinline__ void load_h(uint8_t* dst, const __half* hbuf, int a, int I, int T) {
   const __half* hb = hbuf + (size_t)a * 2 * kTok * I;
   for (int i = threadIdx.x; i < 2 * T * (I / 8); i += blockDim.x) {
-    const int j = i / (I / 8), g8 = i - j * (I / 8);
-    const int row = j < T ? j : 8 + (j - T);   // part * 8 + token
+    const int row = i / (I / 8), g8 = i - row * (I / 8);
     *reinterpret_cast<uint4*>(dst + b_offset(row, 8 * g8)) =
         *reinterpret_cast<const uint4*>(hb + (size_t)row * I + 8 * g8);
   }
 }
 
-// NA: A buffers per warpgroup.  Stage g's MMAs are issued during iteration g + 1
-// by lane 0 of one warp of the warpgroup and complete on done[g mod NA].  MMAs
-// from different threads are not ordered among themselves, so every stage of an
-// accumulation segment is issued by the same warp: warp (segment mod 4).
-// iteration g waits for stage g - NA, which frees A buffer g mod NA and makes
-// the accumulation segments that ended in stage g - NA readable.  With
-// NA = 3 a segment covers two stages (two D buffers suffice), with NA = 2 it
-// covers at most one (four D buffers).
-template <int MODE, int R, int NA>
+// A unit's epilogue (local unit v of the CTA's range starting at unit ub).
+// TT = 8: thread (wg, r) finishes row r for tokens 2wg and 2wg + 1; TT = 1:
+// warpgroup 0 finishes token 0.  Gate/up: h = silu(gate) * up of each row pair
+// (gate row in lanes 0-15, its up row 16 lanes above) into hbuf as fp16 high
+// part and remainder; down: the expert's output rows.  Whole warps call it;
+// every thread of the CTA arrives on red_empty.
+template <int MODE, int TT>
+__device__ __noinline__ void finish_unit(int v, int ub, int upe, const Group* groups, const float* red,
+                                         uint64_t* red_full, uint64_t* red_empty, int kq, int T, int I, int H,
+                                         __half* hbuf, float* expert_out, volatile int* abort_flag, int* status) {
+  const int tid = threadIdx.x, lane = tid & 31, wg = tid >> 7, r = tid & 127;
+  const int u = ub + v, a = u / upe, m0 = (u - a * upe) * BM;
+  const Group& gr = groups[a];
+  mbar_wait_bounded(&red_full[v & 1], (v >> 1) & 1, abort_flag, status);
+  constexpr int NT = TT == 1 ? 1 : 2;   // tokens per thread
+  const int n0 = TT == 1 ? 0 : 2 * wg;
+  if ((TT > 1 || wg == 0) && (gr.flags & 1)) {
+    float vv[NT];
+#pragma unroll
+    for (int t = 0; t < NT; ++t) vv[t] = 0.f;
+    for (int w = 0; w < kq; ++w) {
+      const float* rr = red + ((size_t)((v & 1) * kWG + w) * BM + r) * TT + n0;
+#pragma unroll
+      for (int t = 0; t < NT; ++t) vv[t] += rr[t];
+    }
+    if constexpr (MODE == 0) {
+      const int f = m0 / 2 + 16 * (r >> 5) + (r & 15);
+      const int pos = (f & ~7) | (((f & 3) << 1) | ((f >> 2) & 1));
+      __half* hb = hbuf + (size_t)a * 2 * kTok * I;
+#pragma unroll
+      for (int t = 0; t < NT; ++t) {
+        const float up = __shfl_down_sync(0xffffffffu, vv[t], 16);
+        if ((lane & 16) == 0 && n0 + t < T) {
+          __half hh, hl;
+          split_half(silu_f32(vv[t]) * up, hh, hl);
+          hb[(size_t)(2 * (n0 + t)) * I + pos] = hh;
+          hb[(size_t)(2 * (n0 + t) + 1) * I + pos] = hl;
+        }
+      }
+    } else {
+#pragma unroll
+      for (int t = 0; t < NT; ++t) {
+        const int q = gr.outq[n0 + t];
+        if (q >= 0) expert_out[(size_t)q * H + m0 + r] = vv[t];
+      }
+    }
+  }
+  mbar_arrive(&red_empty[v & 1]);
+}
+
+// The pipeline of a warpgroup runs over the global stages g of its CTA (all
+// units back to back; four stages per unrolled block, the register ring).
+// Iteration g: wait for stage g - NA's MMAs (A buffer g mod NA is free again,
+// the segments that ended in stage g - NA are readable); decode and store stage
+// g; read back stage g - NA (after a unit's last stage the thread's partial
+// sums go to the reduction buffer); publish stage g; and, on its warp's turn,
+// issue stage g - 1.  MMAs from different threads are not ordered among
+// themselves, so all stages of one accumulation segment are issued by the same
+// warp: warp (segment mod 4).  SEG = the accumulation segment, min(G, K slice):
+// 128 covers two stages (three A buffers, two D buffers), 64 one stage and 32
+// half a stage (two A buffers, four D buffers).  A unit's epilogue (sum of the
+// warpgroups' partials, SwiGLU or output rows) runs one unit later, so no warp
+// waits for a slower one at unit boundaries; mbarriers hand the double-buffered
+// reduction area over.  TT = token capacity (1 or 8): B row 2n is the fp16 high
+// part of token n, row 2n + 1 its remainder, and accumulator columns 0 .. 2TT-1
+// are the ones read back.
+template <int MODE, int SEG, int TT>
 __global__ void __launch_bounds__(kThreads, 1) ffn_decode_kernel(const FfnParams p) {
-  constexpr int ND = NA == 3 ? 2 : 4;
-  constexpr int SPS = NA == 3 ? 2 : 1;    // stages per accumulation segment (at least)
+  constexpr int R = 4;                    // register ring depth = unroll
+  constexpr int NA = SEG == 128 ? 3 : 2;  // A buffers per warpgroup
+  constexpr int ND = SEG == 128 ? 2 : 4;  // D buffers per warpgroup
   constexpr int kD0 = 32 * NA;            // first D column of a warpgroup
   static_assert(32 * NA + 16 * ND <= kColsPerWG, "TMEM columns per warpgroup");
+  static_assert(TT == 1 || TT == kTok, "token capacity");
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
-  const Layout L = make_layout(p.K, p.nB);
+  const Layout L = make_layout(p.K, p.nB, TT);
   uint8_t* Bs = smem + L.b_off;
   const uint32_t b_bytes = (uint32_t)p.K * BN * 2;
   float* red = reinterpret_cast<float*>(smem + L.red_off);
   uint64_t* a_full = reinterpret_cast<uint64_t*>(smem + L.bar_off);   // [kWG][3]: the 4 warps stored stage A
   uint64_t* done = a_full + kWG * 3;                                  // [kWG][3]: the stage's MMAs completed
+  uint64_t* red_full = done + kWG * 3;                                // [2]: every partial of a unit written
+  uint64_t* red_empty = red_full + 2;                                 // [2]: every epilogue of a unit read
   Group* groups = reinterpret_cast<Group*>(smem + L.grp_off);
   uint32_t* tmem_base_p = reinterpret_cast<uint32_t*>(smem + L.misc_off);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L.misc_off + 4);
@@ -177,6 +239,7 @@ __global__ void __launch_bounds__(kThreads, 1) ffn_decode_kernel(const FfnParams
       sc = MODE == 0 ? sl->s_gate_up : sl->s_down;
       flags = (w && sc && ((reinterpret_cast<uintptr_t>(w) | reinterpret_cast<uintptr_t>(sc)) & 15) == 0) ? 1 : 0;
     }
+    if (!flags && a >= ub / upe && a <= (ue - 1) / upe) set_status(p.status, QRE_DEV_NULL_SLOT);
     Group& dst = groups[a];
     dst.w = w;
     dst.s = sc;
@@ -197,6 +260,10 @@ __global__ void __launch_bounds__(kThreads, 1) ffn_decode_kernel(const FfnParams
       mbar_init(&a_full[i], 4);
       mbar_init(&done[i], 1);
     }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&red_full[i], 128 * p.kq);
+      mbar_init(&red_empty[i], kThreads);
+    }
     *abort_flag = 0;
     fence_barrier_init();
   }
@@ -207,9 +274,9 @@ __global__ void __launch_bounds__(kThreads, 1) ffn_decode_kernel(const FfnParams
   }
   const int a_first = ub / upe;
   if constexpr (MODE == 0) {
-    // B = tokens: rows 0-7 fp16 high parts, 8-15 remainders.  Rows of tokens
-    // n >= T are left as they are: they only feed accumulator columns n, n + 8,
-    // which nothing reads.
+    // B = tokens, row 2n the fp16 high part of token n, row 2n + 1 the remainder.
+    // Rows of tokens n >= T are left as they are: they only feed accumulator
+    // columns that nothing reads.
     for (int i = tid; i < p.T * (p.K / 8); i += blockDim.x) {
       const int n = i / (p.K / 8), g8 = i - n * (p.K / 8);
       const uint4 v = __ldg(reinterpret_cast<const uint4*>(p.x + (size_t)n * p.H + 8 * g8));
@@ -229,236 +296,261 @@ __global__ void __launch_bounds__(kThreads, 1) ffn_decode_kernel(const FfnParams
         hi[j] = h2_as_u32(__halves2half2(h0, h1));
         lo[j] = h2_as_u32(__halves2half2(l0, l1));
       }
-      *reinterpret_cast<uint4*>(Bs + b_offset(n, 8 * g8)) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
-      *reinterpret_cast<uint4*>(Bs + b_offset(8 + n, 8 * g8)) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+      *reinterpret_cast<uint4*>(Bs + b_offset(2 * n, 8 * g8)) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+      *reinterpret_cast<uint4*>(Bs + b_offset(2 * n + 1, 8 * g8)) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
     }
   } else {
-    // B = h of the first nB experts of this CTA's range
+    // B = h of the experts of this CTA's range (at most nB of them, by the launch)
     const int a_last = (ue - 1) / upe;
     for (int j = 0; j < p.nB && a_first + j <= a_last; ++j) load_h(Bs + j * b_bytes, p.hbuf, a_first + j, p.I, p.T);
+    if (a_last - a_first >= p.nB && tid == 0) set_status(p.status, QRE_DEV_BAD_INDEX);
   }
   fence_proxy_async_smem();
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
 
-  const uint32_t tmem_wg = *tmem_base_p + wg * kColsPerWG;
-  const uint32_t tlane = (uint32_t)(32 * wq) << 16;   // this warp's TMEM lane quarter
+  const int NU = ue - ub;
   const int Kq = p.K / p.kq;
   const int nst = Kq / SK;
-  const bool active_wg = wg < p.kq;
+  const int NS = NU * nst;              // stages of each active warpgroup
   const int k0 = wg * Kq;
-  const int KS = p.K / SK;              // chunks per row block
-  const int KG = p.K >> p.lgG;
-  const int segL = 1 << p.lgS;
-  const int spu = Kq >> p.lgS;          // accumulation segments per unit
-  const uint32_t idesc = umma_idesc_f16(BM, BN);
-  const uint32_t bbase0 = smem_addr(Bs);
 
-  // load cursor: the next stage to prefetch (unit lu, stage lst)
-  int lu = ub, lst = 0;
-  const uint4* lptr = nullptr;
-  const unsigned short* lsp = nullptr;
-  auto cursor_unit = [&](int u) {
-    const int a = u / upe, m0 = (u - a * upe) * BM;
-    const Group& gr = groups[a];
-    if (gr.flags & 1) {
-      lptr = reinterpret_cast<const uint4*>(gr.w + ((size_t)(m0 / BM) * KS + k0 / SK) * kChunk) + r;
-      lsp = reinterpret_cast<const unsigned short*>(gr.s) + (size_t)(m0 / BM) * KG * BM + r;
-    } else {
-      lptr = nullptr;
-      lsp = nullptr;
-    }
+  auto epilogue = [&](int v) {
+    finish_unit<MODE, TT>(v, ub, upe, groups, red, red_full, red_empty, p.kq, p.T, p.I, p.H, p.hbuf, p.expert_out,
+                          abort_flag, p.status);
   };
-  cursor_unit(lu);
+  int epi = -1;   // a unit whose epilogue is due (it runs after the current block of stages)
 
-  uint4 ring[R][2];
-  uint32_t sring[R];   // the stage's two scales (elements 0-31 low half, 32-63 high half)
-  auto load_next = [&](uint4 (&dst)[2], uint32_t& sdst) {
-    if (lptr) {
-      dst[0] = __ldg(lptr + lst * (kChunk / 16));
-      dst[1] = __ldg(lptr + lst * (kChunk / 16) + kChunk / 32);
-      const int kk = k0 + lst * SK;
-      sdst = (uint32_t)__ldg(lsp + (size_t)(kk >> p.lgG) * BM) |
-             ((uint32_t)__ldg(lsp + (size_t)((kk + 32) >> p.lgG) * BM) << 16);
-    } else {
-      dst[0] = dst[1] = make_uint4(0x88888888u, 0x88888888u, 0x88888888u, 0x88888888u);
-      sdst = 0;
-    }
-    if (++lst == nst) {
-      lst = 0;
-      if (++lu < ue) cursor_unit(lu);
-    }
-  };
-  if (active_wg) {
+  if (wg < p.kq) {
+    const uint32_t tmem_wg = *tmem_base_p + wg * kColsPerWG;
+    const uint32_t tlane = (uint32_t)(32 * wq) << 16;   // this warp's TMEM lane quarter
+    const int KS = p.K / SK;              // chunks per row block
+    const int KG = p.K >> p.lgG;
+    const uint32_t idesc = umma_idesc_f16(BM, BN);
+    const uint32_t bbase0 = smem_addr(Bs);
+
+    // load cursor: the next stage to prefetch (unit lu, stage lst)
+    int lu = ub, lst = 0;
+    const uint4* lptr = nullptr;
+    const unsigned short* lsp = nullptr;
+    auto cursor_unit = [&](int u) {
+      const int a = u / upe, m0 = (u - a * upe) * BM;
+      const Group& gr = groups[a];
+      if (gr.flags & 1) {
+        lptr = reinterpret_cast<const uint4*>(gr.w + ((size_t)(m0 / BM) * KS + k0 / SK) * kChunk) + r;
+        lsp = reinterpret_cast<const unsigned short*>(gr.s) + (size_t)(m0 / BM) * KG * BM + r;
+      } else {
+        lptr = nullptr;
+        lsp = nullptr;
+      }
+    };
+    cursor_unit(lu);
+    uint4 ring[R][2];
+    uint32_t sring[R];   // scales: SEG 32 both halves (low 16 bits: elements 0-31), else one
+    // `first` = the stage starts a segment (SEG 128: only those load a scale)
+    auto load_next = [&](uint4 (&dst)[2], uint32_t& sdst, bool first) {
+      if (lptr) {
+        dst[0] = __ldg(lptr + lst * (kChunk / 16));
+        dst[1] = __ldg(lptr + lst * (kChunk / 16) + kChunk / 32);
+        const int kk = k0 + lst * SK;
+        if (SEG == 32)
+          sdst = (uint32_t)__ldg(lsp + (size_t)(kk >> p.lgG) * BM) |
+                 ((uint32_t)__ldg(lsp + (size_t)((kk + 32) >> p.lgG) * BM) << 16);
+        else if (SEG == 64 || first)
+          sdst = __ldg(lsp + (size_t)(kk >> p.lgG) * BM);
+      } else {
+        dst[0] = dst[1] = make_uint4(0x88888888u, 0x88888888u, 0x88888888u, 0x88888888u);
+        sdst = 0;
+      }
+      if (++lst == nst) {
+        lst = 0;
+        if (++lu < ue) cursor_unit(lu);
+      }
+    };
 #pragma unroll
     for (int j = 0; j < R; ++j)
-      if (lu < ue) load_next(ring[j], sring[j]);
-  }
+      if (j < NS) load_next(ring[j], sring[j], (j & 1) == 0);
 
-  float acc[kTok];
-  // Adds the accumulation segments that end in unit stage `st` (scales sp) to
-  // acc; the stage's MMAs have completed.
-  auto readback = [&](int st, int ul, uint32_t sp) {
+    float acc[TT];
 #pragma unroll
-    for (int q = 0; q < 4; ++q) {
-      const int kk = st * SK + 16 * q;
-      if (((kk + 16) & (segL - 1)) == 0) {
-        const int d = (ul * spu + (kk >> p.lgS)) & (ND - 1);
-        uint32_t dv[16];
-        tmem_ld_32x32b_x16(tlane + tmem_wg + kD0 + 16 * d, dv);
-        tmem_ld_wait();
-        const float sc = __half2float(__ushort_as_half((unsigned short)(q < 2 ? sp & 0xFFFFu : sp >> 16)));
+    for (int n = 0; n < TT; ++n) acc[n] = 0.f;
+    // Segments that end in global stage e (odd: e is odd; stage est of local
+    // unit eul; scale word sp): add them to acc; after a unit's last stage,
+    // hand the partial sums over.
+    auto readback = [&](int e, bool odd, int est, int eul, uint32_t sp) {
 #pragma unroll
-        for (int n = 0; n < kTok; ++n) acc[n] = fmaf(sc, __uint_as_float(dv[n]) + __uint_as_float(dv[n + 8]), acc[n]);
-      }
-    }
-  };
-  auto wait_done = [&](int gs) {
-    mbar_wait_bounded(&done[wg * 3 + gs % NA], (gs / NA) & 1, abort_flag, p.status);
-    __syncwarp();
-    tc_fence_after();
-  };
-  // the warp that issues global stage gs
-  auto issuer = [&](int gs) { return ((gs / SPS) & 3) == wq; };
-  // lane 0 of the issuing warp: the four MMAs of global stage gs (unit stage st)
-  auto issue = [&](int gs, int st, int ul, uint32_t bbase) {
-    mbar_wait_bounded(&a_full[wg * 3 + gs % NA], (gs / NA) & 1, abort_flag, p.status);
-    tc_fence_after();
+      for (int q = 0; q < 4; ++q) {
+        const bool seg_end = SEG == 128 ? (odd && q == 3) : (SEG == 64 ? q == 3 : (q & 1) == 1);
+        if (seg_end) {
+          const int d = SEG == 128 ? ((e >> 1) & 1) : (SEG == 64 ? (e & 3) : ((2 * e + (q >> 1)) & 3));
+          const float sc =
+              __half2float(__ushort_as_half((unsigned short)(SEG == 32 && q >= 2 ? sp >> 16 : sp & 0xFFFFu)));
+          if constexpr (TT == 1) {
+            uint32_t dv[2];
+            asm volatile("tcgen05.ld.sync.aligned.32x32b.x2.b32 {%0,%1}, [%2];"
+                         : "=r"(dv[0]), "=r"(dv[1])
+                         : "r"(tlane + tmem_wg + kD0 + 16 * d));
+            tmem_ld_wait();
+            acc[0] = fmaf(sc, __uint_as_float(dv[0]) + __uint_as_float(dv[1]), acc[0]);
+          } else {
+            uint32_t dv[16];
+            tmem_ld_32x32b_x16(tlane + tmem_wg + kD0 + 16 * d, dv);
+            tmem_ld_wait();
 #pragma unroll
-    for (int q = 0; q < 4; ++q) {
-      const int kk = st * SK + 16 * q;
-      const int d = (ul * spu + (kk >> p.lgS)) & (ND - 1);
-      const int kb = k0 + kk;
-      const uint64_t bdesc = umma_desc_sw128(bbase + (uint32_t)((kb >> 6) * (BN * 128) + (kb & 63) * 2));
-      umma_f16_tmem_a(tmem_wg + kD0 + 16 * d, tmem_wg + (gs % NA) * 32 + 8 * q, bdesc, idesc,
-                      (kk & (segL - 1)) ? 1u : 0u);
-    }
-    umma_commit(&done[wg * 3 + gs % NA]);
-  };
-
-  int g = 0, buf = 0, cur_a = a_first, bsel = 0;
-  for (int u = ub, ul = 0; u < ue; ++u, ++ul) {
-    const int a = u / upe, m0 = (u - a * upe) * BM;
-    const Group& gr = groups[a];
-    if (!(gr.flags & 1) && tid == 0) set_status(p.status, QRE_DEV_NULL_SLOT);
-    if constexpr (MODE == 1) {
-      if (a != cur_a) {
-        cur_a = a;
-        const int la = a - a_first;
-        bsel = la % p.nB;
-        if (la >= p.nB) {   // buffer bsel held expert la - nB, whose MMAs all completed: refill it
-          __syncthreads();
-          load_h(Bs + bsel * b_bytes, p.hbuf, a, p.I, p.T);
-          fence_proxy_async_smem();
-          __syncthreads();
+            for (int n = 0; n < TT; ++n)
+              acc[n] = fmaf(sc, __uint_as_float(dv[2 * n]) + __uint_as_float(dv[2 * n + 1]), acc[n]);
+          }
         }
       }
-    }
-    const uint32_t bbase = bbase0 + bsel * b_bytes;
+      if (est == nst - 1) {
+        if (eul >= 2) mbar_wait_bounded(&red_empty[eul & 1], ((eul >> 1) - 1) & 1, abort_flag, p.status);
+        float* rw = red + ((size_t)((eul & 1) * kWG + wg) * BM + r) * TT;
 #pragma unroll
-    for (int n = 0; n < kTok; ++n) acc[n] = 0.f;
+        for (int n = 0; n < TT; ++n) {
+          rw[n] = acc[n];
+          acc[n] = 0.f;
+        }
+        mbar_arrive(&red_full[eul & 1]);
+      }
+    };
+    auto bbase_of = [&](int ul) {
+      if constexpr (MODE == 1) return bbase0 + ((((ub + ul) / upe) - a_first) % p.nB) * b_bytes;
+      return bbase0;
+    };
+    // lane 0 of the issuing warp: the four MMAs of global stage i (odd: i is odd;
+    // stage ist of local unit iul; A buffer ib, whose phases have parity iph)
+    auto issue = [&](int i, bool odd, int ist, int iul, int ib, int iph) {
+      mbar_wait_bounded(&a_full[wg * 3 + ib], iph, abort_flag, p.status);
+      tc_fence_after();
+      const uint32_t bstage = bbase_of(iul) + (uint32_t)((k0 / SK + ist) * (BN * 128));
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const int d = SEG == 128 ? ((i >> 1) & 1) : (SEG == 64 ? (i & 3) : ((2 * i + (q >> 1)) & 3));
+        const bool fresh = SEG == 128 ? (!odd && q == 0) : (SEG == 64 ? q == 0 : (q & 1) == 0);
+        umma_f16_tmem_a(tmem_wg + kD0 + 16 * d, tmem_wg + ib * 32 + 8 * q, umma_desc_sw128(bstage + 32 * q), idesc,
+                        fresh ? 0u : 1u);
+      }
+      umma_commit(&done[wg * 3 + ib]);
+    };
+    auto issuer = [&](int i) { return ((SEG == 128 ? (i >> 1) : i) & 3) == wq; };
 
-    if (active_wg) {
-      uint32_t h1 = 0, h2 = 0, h3 = 0;   // scales of unit stages st-1, st-2, st-3
-      for (int st0 = 0; st0 < nst; st0 += R) {
+    uint32_t h1 = 0, h2 = 0, h3 = 0;   // scale words of global stages gs-1, gs-2, gs-3
+    int st = 0, ul = 0;                // stage and local unit of gs
+    int ab = 0, aph = 0;               // A buffer of gs and the parity of its phase there
+    for (int gs0 = 0; gs0 < NS; gs0 += R) {
 #pragma unroll
-        for (int j = 0; j < R; ++j) {
-          const int st = st0 + j, gs = g + st, ab = gs % NA;
+      for (int j = 0; j < R; ++j) {
+        const int gs = gs0 + j;
+        if (gs < NS) {
+          // (0) take this stage's weights and scales, refill the ring slot R stages ahead
+          const uint32_t wd[8] = {ring[j][0].x, ring[j][0].y, ring[j][0].z, ring[j][0].w,
+                                  ring[j][1].x, ring[j][1].y, ring[j][1].z, ring[j][1].w};
+          // SEG 128: an odd stage continues the segment (and the scale) of the stage before
+          const uint32_t sp = (SEG == 128 && (j & 1)) ? h1 : sring[j];
+          if (gs + R < NS) load_next(ring[j], sring[j], (j & 1) == 0);
           // (1) stage gs - NA completed: A buffer ab is free, its segments are readable
-          if (gs >= NA) wait_done(gs - NA);
+          if (gs >= NA) {
+            mbar_wait_bounded(&done[wg * 3 + ab], aph ^ 1, abort_flag, p.status);
+            __syncwarp();
+            tc_fence_after();
+          }
           // (2) decode 64 nibbles into 32 fp16 pairs of this row, store them in TMEM
-          {
-            const uint32_t wd[8] = {ring[j][0].x, ring[j][0].y, ring[j][0].z, ring[j][0].w,
-                                    ring[j][1].x, ring[j][1].y, ring[j][1].z, ring[j][1].w};
-            uint32_t av[32];
 #pragma unroll
-            for (int w = 0; w < 8; ++w) {
+          for (int half = 0; half < 2; ++half) {
+            uint32_t av[16];
+#pragma unroll
+            for (int w = 0; w < 4; ++w) {
               uint32_t pr[4];
-              decode_nibbles(wd[w], pr);
+              decode_nibbles(wd[4 * half + w], pr);
               av[4 * w + 0] = pr[0];
               av[4 * w + 1] = pr[1];
               av[4 * w + 2] = pr[2];
               av[4 * w + 3] = pr[3];
             }
-            tmem_st_32x32b_x32(tlane + tmem_wg + ab * 32, av);
+            tmem_st_32x32b_x16(tlane + tmem_wg + ab * 32 + 16 * half, av);
           }
-          // (3) while the store drains: segments of unit stage st - NA
-          if (st >= NA) readback(st - NA, ul, NA == 3 ? h3 : h2);
-          // (4) scales of this stage, prefetch R stages ahead
+          // (3) while the store drains: read back stage gs - NA
+          if (gs >= NA) {
+            int est = st - NA, eul = ul;
+            while (est < 0) {
+              est += nst;
+              --eul;
+            }
+            // a second unit end in one block (units shorter than a block): the
+            // earlier unit's epilogue must run before this hand-over waits for it
+            if (est == nst - 1 && epi >= 0) {
+              epilogue(epi);
+              epi = -1;
+            }
+            readback(gs - NA, ((j - NA) & 1) != 0, est, eul, NA == 3 ? h3 : h2);
+            if (est == nst - 1 && eul >= 1) epi = eul - 1;
+          }
           h3 = h2;
           h2 = h1;
-          h1 = sring[j];
-          if (lu < ue) load_next(ring[j], sring[j]);
-          // (5) publish the stored A
+          h1 = sp;
+          // (4) publish the stored A
           tmem_st_wait();
           tc_fence_before();
           __syncwarp();
           if (lane == 0) mbar_arrive(&a_full[wg * 3 + ab]);
-          // (6) issue the previous stage if it is this warp's turn
-          if (st >= 1 && issuer(gs - 1) && lane == 0) issue(gs - 1, st - 1, ul, bbase);
-          __syncwarp();
-        }
-      }
-      // unit end: issue the last stage, wait for the unit's last stages, read them back
-      const int gl = g + nst - 1;
-      if (issuer(gl) && lane == 0) issue(gl, nst - 1, ul, bbase);
-      __syncwarp();
-      const int first = nst > NA ? nst - NA : 0;
-      for (int st = first; st < nst; ++st) {
-        wait_done(g + st);
-        const int back = nst - st;   // 1 = the last stage
-        readback(st, ul, back == 1 ? h1 : (back == 2 ? h2 : h3));
-      }
-      tc_fence_before();
-      float* rw = red + ((size_t)(buf * kWG + wg) * BM + r) * kTok;
-#pragma unroll
-      for (int n = 0; n < kTok; n += 4)
-        *reinterpret_cast<float4*>(rw + n) = make_float4(acc[n], acc[n + 1], acc[n + 2], acc[n + 3]);
-    }
-    g += nst;
-    __syncthreads();
-    {
-      // epilogue: thread (wg, r) finishes row r for tokens 2wg, 2wg + 1
-      const int n0 = 2 * wg;
-      float v0 = 0.f, v1 = 0.f;
-      for (int w = 0; w < p.kq; ++w) {
-        const float* rr = red + ((size_t)(buf * kWG + w) * BM + r) * kTok + n0;
-        v0 += rr[0];
-        v1 += rr[1];
-      }
-      if (gr.flags & 1) {
-        if constexpr (MODE == 0) {
-          // lanes 0-15 of each warp hold gate rows, lanes 16-31 the matching up rows
-          const float up0 = __shfl_down_sync(0xffffffffu, v0, 16);
-          const float up1 = __shfl_down_sync(0xffffffffu, v1, 16);
-          const int f = m0 / 2 + 16 * (r >> 5) + (r & 15);
-          const int pos = (f & ~7) | (((f & 3) << 1) | ((f >> 2) & 1));
-          __half* hb = p.hbuf + (size_t)a * 2 * kTok * p.I;
-          if ((lane & 16) == 0) {
-            __half hh, hl;
-            if (n0 < p.T) {
-              split_half(silu_f32(v0) * up0, hh, hl);
-              hb[(size_t)n0 * p.I + pos] = hh;
-              hb[(size_t)(kTok + n0) * p.I + pos] = hl;
-            }
-            if (n0 + 1 < p.T) {
-              split_half(silu_f32(v1) * up1, hh, hl);
-              hb[(size_t)(n0 + 1) * p.I + pos] = hh;
-              hb[(size_t)(kTok + n0 + 1) * p.I + pos] = hl;
-            }
+          // (5) issue the previous stage if it is this warp's turn
+          if (gs >= 1 && issuer(gs - 1) && lane == 0) {
+            const int ist = st > 0 ? st - 1 : nst - 1, iul = st > 0 ? ul : ul - 1;
+            issue(gs - 1, ((j - 1) & 1) != 0, ist, iul, ab > 0 ? ab - 1 : NA - 1, ab > 0 ? aph : aph ^ 1);
           }
-        } else {
-          const int q0 = gr.outq[n0], q1 = gr.outq[n0 + 1];
-          if (q0 >= 0) p.expert_out[(size_t)q0 * p.H + m0 + r] = v0;
-          if (q1 >= 0) p.expert_out[(size_t)q1 * p.H + m0 + r] = v1;
+          __syncwarp();
+          if (++st == nst) {
+            st = 0;
+            ++ul;
+          }
+          if (++ab == NA) {
+            ab = 0;
+            aph ^= 1;
+          }
         }
       }
+      // (6) soon after handing over unit v's partial sums, finish unit v - 1
+      if (epi >= 0) {
+        epilogue(epi);
+        epi = -1;
+      }
     }
-    buf ^= 1;
+    // tail: issue the last stage, read back the last stages, finish the last units
+    if (issuer(NS - 1) && lane == 0)
+      issue(NS - 1, ((NS - 1) & 1) != 0, st > 0 ? st - 1 : nst - 1, st > 0 ? ul : ul - 1, ab > 0 ? ab - 1 : NA - 1,
+            ab > 0 ? aph : aph ^ 1);
+    __syncwarp();
+    for (int back = NA < NS ? NA : NS; back >= 1; --back) {
+      const int e = NS - back;
+      int eb = ab - back, eph = aph;
+      if (eb < 0) {
+        eb += NA;
+        eph ^= 1;
+      }
+      mbar_wait_bounded(&done[wg * 3 + eb], eph, abort_flag, p.status);
+      __syncwarp();
+      tc_fence_after();
+      int est = st - back, eul = ul;
+      while (est < 0) {
+        est += nst;
+        --eul;
+      }
+      if (est == nst - 1 && epi >= 0) {
+        epilogue(epi);
+        epi = -1;
+      }
+      readback(e, (e & 1) != 0, est, eul, back == 1 ? h1 : (back == 2 ? h2 : h3));
+      if (est == nst - 1 && eul >= 1) epi = eul - 1;
+    }
+    tc_fence_before();
+    if (epi >= 0) epilogue(epi);
+    epilogue(NU - 1);
+  } else {
+    // warpgroups without a K slice only finish units
+    for (int v = 0; v < NU; ++v) epilogue(v);
   }
 
-  tc_fence_before();
   __syncthreads();
   if (warp == 0) {
     tc_fence_after();
@@ -482,41 +574,47 @@ int pick_kq(int K, int G) {
   return 0;
 }
 
-int smem_needed(int K, int nB) {
-  const size_t b = make_layout(K, nB).bytes;
+int smem_needed(int K, int nB, int TT) {
+  const size_t b = make_layout(K, nB, TT).bytes;
   // at least ~120 KB so that no second CTA (and no second TMEM allocation) shares an SM
   return (int)(b > 120 * 1024 ? b : 120 * 1024);
 }
 
-template <int MODE, int R, int NA>
-cudaError_t launch_r(const FfnParams& p, int grid, int smem, cudaStream_t stream) {
-  cudaError_t err = ensure_smem_limit(reinterpret_cast<const void*>(ffn_decode_kernel<MODE, R, NA>), smem);
+template <int MODE, int SEG, int TT>
+cudaError_t launch_k(const FfnParams& p, int grid, int smem, cudaStream_t stream) {
+  cudaError_t err = ensure_smem_limit(reinterpret_cast<const void*>(ffn_decode_kernel<MODE, SEG, TT>), smem);
   if (err != cudaSuccess) return err;
-  ffn_decode_kernel<MODE, R, NA><<<grid, kThreads, smem, stream>>>(p);
+  ffn_decode_kernel<MODE, SEG, TT><<<grid, kThreads, smem, stream>>>(p);
   return cudaGetLastError();
 }
 
-template <int MODE, int NA>
-cudaError_t launch_na(const FfnParams& p, int nst, int grid, int smem, cudaStream_t stream) {
-  if (nst % 4 == 0) return launch_r<MODE, 4, NA>(p, grid, smem, stream);
-  if (nst % 2 == 0) return launch_r<MODE, 2, NA>(p, grid, smem, stream);
-  return launch_r<MODE, 1, NA>(p, grid, smem, stream);
+template <int MODE, int TT>
+cudaError_t launch_tt(const FfnParams& p, int seg, int grid, int smem, cudaStream_t stream) {
+  if (seg == 128) return launch_k<MODE, 128, TT>(p, grid, smem, stream);
+  if (seg == 64) return launch_k<MODE, 64, TT>(p, grid, smem, stream);
+  return launch_k<MODE, 32, TT>(p, grid, smem, stream);
 }
 
 template <int MODE>
-cudaError_t launch_mode(const FfnParams& base, int grid, cudaStream_t stream) {
+cudaError_t launch_mode(const FfnParams& base, long long units, cudaStream_t stream) {
   FfnParams p = base;
+  const int sms = device_sm_count();
   p.kq = pick_kq(p.K, p.G);
   const int Kq = p.K / p.kq;
   p.lgG = ilog2(p.G);
-  p.lgS = ilog2(Kq < p.G ? Kq : p.G);
+  const int seg = Kq < p.G ? Kq : p.G;
+  const int TT = p.T == 1 ? 1 : kTok;
   const int budget = device_max_smem_optin();
-  p.nB = (MODE == 1 && smem_needed(p.K, 2) <= budget) ? 2 : 1;
-  const int smem = smem_needed(p.K, p.nB);
-  const int nst = Kq / SK;
-  // segments of two stages (G = 128 within a K slice): three A buffers, two D buffers
-  if (p.lgS == 7) return launch_na<MODE, 3>(p, nst, grid, smem, stream);
-  return launch_na<MODE, 2>(p, nst, grid, smem, stream);
+  p.nB = (MODE == 1 && smem_needed(p.K, 2, TT) <= budget) ? 2 : 1;
+  const int smem = smem_needed(p.K, p.nB, TT);
+  // one CTA per SM; the down kernel holds h of every expert of its range in
+  // shared memory, so its ranges span at most nB experts: with two buffers at
+  // least one CTA per group (ranges of at most one expert's units), with one
+  // buffer one unit per CTA
+  long long grid = units < sms ? units : sms;
+  if (MODE == 1) grid = p.nB == 2 ? (grid > p.amax + 1 ? grid : p.amax + 1) : units;
+  if (TT == 1) return launch_tt<MODE, 1>(p, seg, (int)grid, smem, stream);
+  return launch_tt<MODE, kTok>(p, seg, (int)grid, smem, stream);
 }
 
 }  // namespace
@@ -525,7 +623,7 @@ bool ffn_decode_supported(const qre_layer_shape& s) {
   const int budget = device_max_smem_optin();
   const bool pow2 = s.group == 32 || s.group == 64 || s.group == 128;
   return pow2 && pick_kq(s.hidden, s.group) && pick_kq(s.inter, s.group) && (2 * s.inter) % BM == 0 &&
-         s.hidden % BM == 0 && smem_needed(s.hidden, 1) <= budget && smem_needed(s.inter, 1) <= budget;
+         s.hidden % BM == 0 && smem_needed(s.hidden, 1, kTok) <= budget && smem_needed(s.inter, 1, kTok) <= budget;
 }
 
 size_t ffn_ws_bytes(const qre_layer_shape& s, int T) {
@@ -557,18 +655,14 @@ cudaError_t launch_ffn_decode(const qre_layer_shape& s, int T, const uint16_t* x
   p.status = status;
   const long long pk = (long long)T * s.top_k;
   p.amax = (int)(pk < s.n_experts ? pk : s.n_experts);
-  const int sms = device_sm_count();
-
   p.K = s.hidden;
   p.n_out = 2 * s.inter;
-  long long units = (long long)(p.amax + 1) * (p.n_out / BM);
-  cudaError_t err = launch_mode<0>(p, (int)(units < sms ? units : sms), stream);
+  cudaError_t err = launch_mode<0>(p, (long long)(p.amax + 1) * (p.n_out / BM), stream);
   if (err != cudaSuccess) return err;
 
   p.K = s.inter;
   p.n_out = s.hidden;
-  units = (long long)(p.amax + 1) * (p.n_out / BM);
-  return launch_mode<1>(p, (int)(units < sms ? units : sms), stream);
+  return launch_mode<1>(p, (long long)(p.amax + 1) * (p.n_out / BM), stream);
 }
 
 }  // namespace qre

@@ -102,6 +102,18 @@ def test_mid_layers_match_oracle(cfg, T):
     _check_layer(built, got, ref)
 
 
+def test_wide_intermediate_layer_matches_oracle():
+    """I = 4096: the down projection's h of one expert fills most of shared
+    memory, so the down kernel holds one expert at a time and gives every CTA a
+    single 128-row unit (more CTAs than SMs)."""
+    cfg = synthetic.LayerConfig("wide", 512, 4096, 64, 8, 128, 8)
+    built = BuiltLayer(cfg.hidden, cfg.inter, cfg.n_experts, cfg.top_k, cfg.group, 8, DEV, numpy_source(cfg))
+    x_bits, wr, _ = _inputs(cfg, 8, step=3)
+    got = _run(built, x_bits, wr, None)
+    _check_layer(built, got, built.oracle_layer(x_bits, wr, None))
+    assert qre.qre_read_device_status() == 0
+
+
 def test_host_resident_experts_match_and_are_bit_identical_to_hbm():
     """Slot placement invariance: experts read zero-copy from pinned host memory
     give the same bits as the same experts in device memory."""

@@ -215,6 +215,9 @@ __global__ void __launch_bounds__(kThreads, 1) ffn_decode_kernel(const FfnParams
   uint32_t* tmem_base_p = reinterpret_cast<uint32_t*>(smem + L.misc_off);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L.misc_off + 4);
 
+  // the possible active ids are read together with their count (one dependent
+  // load less before the slot table)
+  const int a_spec = threadIdx.x < p.amax ? __ldg(p.active + threadIdx.x) : p.E;
   int n_act = *p.n_active;
   n_act = n_act < 0 ? 0 : (n_act > p.amax ? p.amax : n_act);
   const int ngroups = n_act + 1;
@@ -229,7 +232,7 @@ __global__ void __launch_bounds__(kThreads, 1) ffn_decode_kernel(const FfnParams
 
   // per-CTA table of the groups (expert, pointers, output rows)
   for (int a = tid; a < ngroups; a += blockDim.x) {
-    const int e = a < n_act ? __ldg(p.active + a) : p.E;
+    const int e = a < n_act ? (a == tid ? a_spec : __ldg(p.active + a)) : p.E;
     const uint8_t* w = nullptr;
     const uint16_t* sc = nullptr;
     int flags = 0;
@@ -443,12 +446,11 @@ __global__ void __launch_bounds__(kThreads, 1) ffn_decode_kernel(const FfnParams
       for (int j = 0; j < R; ++j) {
         const int gs = gs0 + j;
         if (gs < NS) {
-          // (0) take this stage's weights and scales, refill the ring slot R stages ahead
+          // (0) this stage's weights and scales
           const uint32_t wd[8] = {ring[j][0].x, ring[j][0].y, ring[j][0].z, ring[j][0].w,
                                   ring[j][1].x, ring[j][1].y, ring[j][1].z, ring[j][1].w};
           // SEG 128: an odd stage continues the segment (and the scale) of the stage before
           const uint32_t sp = (SEG == 128 && (j & 1)) ? h1 : sring[j];
-          if (gs + R < NS) load_next(ring[j], sring[j], (j & 1) == 0);
           // (1) stage gs - NA completed: A buffer ab is free, its segments are readable
           if (gs >= NA) {
             mbar_wait_bounded(&done[wg * 3 + ab], aph ^ 1, abort_flag, p.status);
@@ -489,6 +491,8 @@ __global__ void __launch_bounds__(kThreads, 1) ffn_decode_kernel(const FfnParams
           h3 = h2;
           h2 = h1;
           h1 = sp;
+          // the slot is decoded: refill it R stages ahead
+          if (gs + R < NS) load_next(ring[j], sring[j], (j & 1) == 0);
           // (4) publish the stored A
           tmem_st_wait();
           tc_fence_before();

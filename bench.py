@@ -21,6 +21,7 @@ has) on a bounded sample of the same workload.
 from __future__ import annotations
 
 import argparse
+import hashlib
 import json
 import math
 import os
@@ -46,6 +47,26 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 def dist_env():
     return (int(os.environ.get("RANK", 0)), int(os.environ.get("LOCAL_RANK", 0)),
             int(os.environ.get("WORLD_SIZE", 1)))
+
+
+# DRAM bytes per expert-FFN call (both kernels) measured with ncu on the decode1
+# workload, for the FFN kernel sources with the given sha256 prefix (the capture and
+# its command are summarised in profiles/ffn_decode_decode1.md).  Reported only while
+# the sources still hash to that value; a changed kernel reports null.
+MEASURED_TRAFFIC = {"decode1": (117485568, "5ea43859ee936137")}
+FFN_SOURCES = ("ffn_decode.cu", "common.cuh", "tc.cuh", "internal.h")
+
+
+def recorded_traffic(workload):
+    rec = MEASURED_TRAFFIC.get(workload)
+    if rec is None:
+        return None
+    csrc = os.path.join(os.path.dirname(os.path.abspath(__file__)), "quantized_routed_expert_03_gb300", "csrc")
+    h = hashlib.sha256()
+    for f in FFN_SOURCES:
+        with open(os.path.join(csrc, f), "rb") as fh:
+            h.update(fh.read())
+    return rec[0] if h.hexdigest()[:16] == rec[1] else None
 
 
 def load_peaks():
@@ -298,9 +319,11 @@ def run_ours(args, rank, local_rank, world):
     if ffn_ms and not prefill:
         achieved = float(np.mean(ffn_bytes)) / (float(np.mean(ffn_ms)) / 1e3) / 1e9
         peak = float(peaks["hbm_gbs"])
+        traffic = args.traffic if args.traffic is not None else recorded_traffic(args.workload)
         roofline = {"bound": "hbm", "kernel": "qre_expert_ffn (gate/up + down dequant-GEMV kernels)",
                     "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
-                    "frac": round(achieved / peak, 4), "traffic": args.traffic,
+                    "frac": round(achieved / peak, 4), "traffic": traffic,
+                    "traffic_unit": "bytes per FFN call (ncu dram read + write)",
                     "peak_source": "of measured (MEASURED_PEAKS.json hbm_gbs)" if peak_src == "measured" else
                     "of fallback 6.8 TB/s",
                     "ffn_us_mean": round(float(np.mean(ffn_ms)) * 1e3, 2),

@@ -46,6 +46,8 @@
 #include "internal.h"
 #include "tc.cuh"
 
+#include <cuda_fp8.h>
+
 namespace qre {
 namespace {
 
@@ -562,6 +564,364 @@ __global__ void __launch_bounds__(kThreads, 1) ffn_decode_kernel(const FfnParams
   }
 }
 
+// ---------------------------------------------------------------- gate/up with FP8 weights in tensor memory
+//
+// For G = 128 the gate/up phase can hold the weights in tensor memory as FP8
+// E4M3 codes of the unsigned nibbles u = q + 8 (0..15, all exact in E4M3): one
+// byte per weight instead of two, so half the tcgen05.st traffic and half the
+// MMAs (kind::f8f6f4 consumes K = 32), and a 128-element stage (one whole
+// group) per synchronisation.  The tokens enter as E4M3 too: for each token
+// and group, x * 2^e (e puts the group's largest |x| in [128, 256)) is written
+// as the sum of three E4M3 terms, which holds a bf16 value exactly unless it is
+// more than ~2^9 below the group's largest.  The group's dot product is then
+//   sum_k q_k x_k = 2^-e * sum_k u_k (t1 + t2 + t3)_k - 8 * sum_k x_k,
+// with the first sum from the tensor core (products exact, fp32 accumulation)
+// and the correction precomputed per token and group from the same terms.
+// B rows: 3n + j = term j of token n (N = 16 for one token, 32 for eight).
+// Pipeline as in the 64-element kernel with segment = stage: two A buffers, two
+// D buffers, item g read back during iteration g + 2, issued during g + 1 by
+// warp g mod 4.
+constexpr int SK8 = 128;                   // reduction elements per stage (one group)
+constexpr int kA8 = SK8 / 4;               // TMEM columns of one A buffer (4 codes per column)
+
+__host__ __device__ inline int bn8(int TT) { return TT == 1 ? 16 : 32; }
+
+struct Layout8 {
+  int b_off, ec_off, red_off, bar_off, grp_off, misc_off;
+  size_t bytes;
+};
+
+__host__ __device__ inline Layout8 make_layout8(int K, int TT) {
+  Layout8 L;
+  L.b_off = 0;                                          // bn8 rows x K bytes, swizzled (1024-aligned)
+  L.ec_off = L.b_off + bn8(TT) * K;                     // E[TT][K/128], C[TT][K/128] fp32
+  L.red_off = L.ec_off + 2 * TT * (K / SK8) * 4;        // 2 x kWG x BM x TT fp32
+  L.bar_off = L.red_off + 2 * kWG * BM * TT * 4;
+  L.grp_off = L.bar_off + (kWG * 6 + 4) * 8;
+  L.misc_off = L.grp_off + kMaxGroups * (int)sizeof(Group);
+  L.bytes = (size_t)L.misc_off + 16 + 1024;
+  return L;
+}
+
+// Byte offset of (row n, reduction index l) in an E4M3 B operand of `rows` rows.
+__device__ __forceinline__ uint32_t b8_offset(int n, int l, int rows) {
+  const int byte = l & 127;
+  return (uint32_t)((l >> 7) * (rows * 128) + (n >> 3) * 1024 + (n & 7) * 128 + ((((byte >> 4) ^ (n & 7))) << 4) +
+                    (byte & 15));
+}
+
+template <int TT>
+__global__ void __launch_bounds__(kThreads, 1) ffn_gateup_e4m3_kernel(const FfnParams p) {
+  constexpr int R = 2;                     // ring depth = unroll (2 x 64 bytes per thread in flight)
+  constexpr int NA = 2;                    // A buffers (and D buffers) per warpgroup
+  constexpr int BN8 = TT == 1 ? 16 : 32;   // MMA N
+  constexpr int kD0 = NA * kA8;            // first D column
+  static_assert(kD0 + NA * BN8 <= kColsPerWG, "TMEM columns per warpgroup");
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
+  const Layout8 L = make_layout8(p.K, TT);
+  uint8_t* Bs = smem + L.b_off;
+  float* Et = reinterpret_cast<float*>(smem + L.ec_off);          // [TT][KG]: 2^-e
+  float* Ct = Et + TT * (p.K / SK8);                               // [TT][KG]: 8 * sum x
+  float* red = reinterpret_cast<float*>(smem + L.red_off);
+  uint64_t* a_full = reinterpret_cast<uint64_t*>(smem + L.bar_off);
+  uint64_t* done = a_full + kWG * 3;
+  uint64_t* red_full = done + kWG * 3;
+  uint64_t* red_empty = red_full + 2;
+  Group* groups = reinterpret_cast<Group*>(smem + L.grp_off);
+  uint32_t* tmem_base_p = reinterpret_cast<uint32_t*>(smem + L.misc_off);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L.misc_off + 4);
+
+  const int a_spec = threadIdx.x < p.amax ? __ldg(p.active + threadIdx.x) : p.E;
+  int n_act = *p.n_active;
+  n_act = n_act < 0 ? 0 : (n_act > p.amax ? p.amax : n_act);
+  const int ngroups = n_act + 1;
+  const int upe = p.n_out / BM;
+  const int U = ngroups * upe;
+  const int ub = (int)((long long)blockIdx.x * U / gridDim.x);
+  const int ue = (int)((long long)(blockIdx.x + 1) * U / gridDim.x);
+  if (ub >= ue) return;
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int wg = tid >> 7, r = tid & 127, wq = warp & 3;
+  const int KG = p.K / SK8;
+
+  for (int a = tid; a < ngroups; a += blockDim.x) {
+    const int e = a < n_act ? (a == tid ? a_spec : __ldg(p.active + a)) : p.E;
+    const uint8_t* w = nullptr;
+    const uint16_t* sc = nullptr;
+    int flags = 0;
+    if (e >= 0 && e <= p.E) {
+      const qre_slot* sl = p.slots + e;
+      w = sl->w_gate_up;
+      sc = sl->s_gate_up;
+      flags = (w && sc && ((reinterpret_cast<uintptr_t>(w) | reinterpret_cast<uintptr_t>(sc)) & 15) == 0) ? 1 : 0;
+    }
+    if (!flags && a >= ub / upe && a <= (ue - 1) / upe) set_status(p.status, QRE_DEV_NULL_SLOT);
+    Group& dst = groups[a];
+    dst.w = w;
+    dst.s = sc;
+    dst.e = e;
+    dst.flags = flags;
+#pragma unroll
+    for (int n = 0; n < kTok; ++n) dst.outq[n] = -1;
+  }
+  if (tid == 0) {
+    for (int i = 0; i < kWG * 3; ++i) {
+      mbar_init(&a_full[i], 4);
+      mbar_init(&done[i], 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&red_full[i], 128 * p.kq);
+      mbar_init(&red_empty[i], kThreads);
+    }
+    *abort_flag = 0;
+    fence_barrier_init();
+  }
+  if (warp == 0) {
+    __syncwarp();
+    tmem_alloc(tmem_base_p, kWG * kColsPerWG);
+    tmem_relinquish();
+  }
+  // B: per (token, group) one warp; lane l handles elements 4l .. 4l + 3 of the group
+  for (int tg = warp; tg < p.T * KG; tg += kThreads / 32) {
+    const int n = tg / KG, g = tg - n * KG;
+    const uint2 raw = __ldg(reinterpret_cast<const uint2*>(p.x + (size_t)n * p.H + g * SK8 + 4 * lane));
+    float v[4] = {bf16_bits_to_float(raw.x & 0xFFFFu), bf16_bits_to_float(raw.x >> 16),
+                  bf16_bits_to_float(raw.y & 0xFFFFu), bf16_bits_to_float(raw.y >> 16)};
+    float m = fmaxf(fmaxf(fabsf(v[0]), fabsf(v[1])), fmaxf(fabsf(v[2]), fabsf(v[3])));
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+    // 2^e with m * 2^e in [128, 256): from the exponent field of m
+    int ex = m > 0.f ? 7 - (int)((__float_as_uint(m) >> 23) & 0xFF) + 127 : 0;
+    ex = ex < -100 ? -100 : (ex > 100 ? 100 : ex);
+    const float up = __uint_as_float((uint32_t)(127 + ex) << 23), down = __uint_as_float((uint32_t)(127 - ex) << 23);
+    uint32_t t[3] = {0u, 0u, 0u};   // 4 codes of each term
+    float back = 0.f;               // sum of the represented values of this lane's 4 elements
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      float rem = v[i] * up, rep = 0.f;
+#pragma unroll
+      for (int j = 0; j < 3; ++j) {
+        const __nv_fp8_storage_t c = __nv_cvt_float_to_fp8(rem, __NV_SATFINITE, __NV_E4M3);
+        const float cv = __half2float(__half(__nv_cvt_fp8_to_halfraw(c, __NV_E4M3)));
+        t[j] |= (uint32_t)c << (8 * i);
+        rem -= cv;
+        rep += cv;
+      }
+      back += rep;
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) back += __shfl_xor_sync(0xffffffffu, back, o);
+#pragma unroll
+    for (int j = 0; j < 3; ++j)
+      *reinterpret_cast<uint32_t*>(Bs + b8_offset(3 * n + j, g * SK8 + 4 * lane, BN8)) = t[j];
+    if (lane == 0) {
+      Et[n * KG + g] = down;
+      Ct[n * KG + g] = 8.0f * back * down;
+    }
+  }
+  fence_proxy_async_smem();
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+
+  const int NU = ue - ub;
+  const int Kq = p.K / p.kq;
+  const int nst = Kq / SK8;
+  const int NS = NU * nst;
+  const int k0 = wg * Kq;
+  const int g0 = k0 / SK8;           // first group of this warpgroup's slice
+
+  auto epilogue = [&](int v) {
+    finish_unit<0, TT>(v, ub, upe, groups, red, red_full, red_empty, p.kq, p.T, p.I, p.H, p.hbuf, p.expert_out,
+                       abort_flag, p.status);
+  };
+  int epi = -1;
+
+  if (wg < p.kq) {
+    const uint32_t tmem_wg = *tmem_base_p + wg * kColsPerWG;
+    const uint32_t tlane = (uint32_t)(32 * wq) << 16;
+    const int KS = p.K / SK;                       // 64-element chunks per row block
+    const uint32_t idesc = umma_idesc_e4m3(BM, BN8);
+    const uint32_t bbase = smem_addr(Bs);
+
+    int lu = ub, lst = 0;
+    const uint4* lptr = nullptr;
+    const unsigned short* lsp = nullptr;
+    auto cursor_unit = [&](int u) {
+      const int a = u / upe, m0 = (u - a * upe) * BM;
+      const Group& gr = groups[a];
+      if (gr.flags & 1) {
+        lptr = reinterpret_cast<const uint4*>(gr.w + ((size_t)(m0 / BM) * KS + k0 / SK) * kChunk) + r;
+        lsp = reinterpret_cast<const unsigned short*>(gr.s) + ((size_t)(m0 / BM) * KG + g0) * BM + r;
+      } else {
+        lptr = nullptr;
+        lsp = nullptr;
+      }
+    };
+    cursor_unit(lu);
+    uint4 ring[R][4];
+    uint32_t sring[R];
+    auto load_next = [&](uint4 (&dst)[4], uint32_t& sdst) {
+      if (lptr) {
+        const uint4* c = lptr + (size_t)lst * (2 * kChunk / 16);   // chunks 2*lst and 2*lst + 1 of the slice
+        dst[0] = __ldg(c);
+        dst[1] = __ldg(c + kChunk / 32);
+        dst[2] = __ldg(c + kChunk / 16);
+        dst[3] = __ldg(c + kChunk / 16 + kChunk / 32);
+        sdst = __ldg(lsp + (size_t)lst * BM);
+      } else {
+        dst[0] = dst[1] = dst[2] = dst[3] = make_uint4(0x88888888u, 0x88888888u, 0x88888888u, 0x88888888u);
+        sdst = 0;
+      }
+      if (++lst == nst) {
+        lst = 0;
+        if (++lu < ue) cursor_unit(lu);
+      }
+    };
+#pragma unroll
+    for (int j = 0; j < R; ++j)
+      if (j < NS) load_next(ring[j], sring[j]);
+
+    float acc[TT];
+#pragma unroll
+    for (int n = 0; n < TT; ++n) acc[n] = 0.f;
+    // stage est of local unit eul (D buffer db, weight scale sp) completed: add it
+    auto readback = [&](int est, int eul, int db, uint32_t sp) {
+      const float sc = __half2float(__ushort_as_half((unsigned short)sp));
+      const int g = g0 + est;
+      if constexpr (TT == 1) {
+        uint32_t dv[4];
+        asm volatile("tcgen05.ld.sync.aligned.32x32b.x4.b32 {%0,%1,%2,%3}, [%4];"
+                     : "=r"(dv[0]), "=r"(dv[1]), "=r"(dv[2]), "=r"(dv[3])
+                     : "r"(tlane + tmem_wg + kD0 + BN8 * db));
+        tmem_ld_wait();
+        const float d = __uint_as_float(dv[0]) + __uint_as_float(dv[1]) + __uint_as_float(dv[2]);
+        acc[0] = fmaf(sc, fmaf(d, Et[g], -Ct[g]), acc[0]);
+      } else {
+        uint32_t dv[32];
+        tmem_ld_32x32b_x32(tlane + tmem_wg + kD0 + BN8 * db, dv);
+        tmem_ld_wait();
+#pragma unroll
+        for (int n = 0; n < TT; ++n) {
+          const float d = __uint_as_float(dv[3 * n]) + __uint_as_float(dv[3 * n + 1]) + __uint_as_float(dv[3 * n + 2]);
+          acc[n] = fmaf(sc, fmaf(d, Et[n * KG + g], -Ct[n * KG + g]), acc[n]);
+        }
+      }
+      if (est == nst - 1) {
+        if (epi >= 0) {
+          epilogue(epi);
+          epi = -1;
+        }
+        if (eul >= 2) mbar_wait_bounded(&red_empty[eul & 1], ((eul >> 1) - 1) & 1, abort_flag, p.status);
+        float* rw = red + ((size_t)((eul & 1) * kWG + wg) * BM + r) * TT;
+#pragma unroll
+        for (int n = 0; n < TT; ++n) {
+          rw[n] = acc[n];
+          acc[n] = 0.f;
+        }
+        mbar_arrive(&red_full[eul & 1]);
+        if (eul >= 1) epi = eul - 1;
+      }
+    };
+    // lane 0 of warp (stage mod 4): the 4 MMAs of global stage i (stage ist of its unit), A/D buffer i & 1
+    auto issue = [&](int i, int ist) {
+      const int ib = i & 1;
+      mbar_wait_bounded(&a_full[wg * 3 + ib], (i >> 1) & 1, abort_flag, p.status);
+      tc_fence_after();
+      const uint32_t bstage = bbase + (uint32_t)((g0 + ist) * (BN8 * 128));
+#pragma unroll
+      for (int q = 0; q < 4; ++q)
+        umma_e4m3_tmem_a(tmem_wg + kD0 + BN8 * ib, tmem_wg + ib * kA8 + 8 * q, umma_desc_sw128(bstage + 32 * q), idesc,
+                         q ? 1u : 0u);
+      umma_commit(&done[wg * 3 + ib]);
+    };
+
+    uint32_t h1 = 0, h2 = 0;   // weight scales of stages gs-1, gs-2
+    int st = 0, ul = 0;
+    for (int gs0 = 0; gs0 < NS; gs0 += R) {
+#pragma unroll
+      for (int j = 0; j < R; ++j) {
+        const int gs = gs0 + j, ab = j & 1;   // gs0 is a multiple of R = 2: buffer = gs & 1 = j & 1
+        if (gs < NS) {
+          // (1) stage gs - 2 completed: A buffer ab is free, its D readable
+          if (gs >= 2) {
+            mbar_wait_bounded(&done[wg * 3 + ab], ((gs - 2) >> 1) & 1, abort_flag, p.status);
+            __syncwarp();
+            tc_fence_after();
+          }
+          // (2) decode 128 nibbles of this row into 128 E4M3 codes, store them in TMEM
+          {
+            uint32_t av[32];
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+              const uint32_t wd[4] = {ring[j][c].x, ring[j][c].y, ring[j][c].z, ring[j][c].w};
+#pragma unroll
+              for (int w = 0; w < 4; ++w) decode_nibbles_e4m3(wd[w], av[8 * c + 2 * w], av[8 * c + 2 * w + 1]);
+            }
+            tmem_st_32x32b_x32(tlane + tmem_wg + ab * kA8, av);
+          }
+          const uint32_t sp = sring[j];
+          if (gs + R < NS) load_next(ring[j], sring[j]);
+          // (3) while the store drains: read back stage gs - 2
+          if (gs >= 2) {
+            int est = st - 2, eul = ul;
+            while (est < 0) {
+              est += nst;
+              --eul;
+            }
+            readback(est, eul, ab, h2);
+          }
+          h2 = h1;
+          h1 = sp;
+          // (4) publish the stored A
+          tmem_st_wait();
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&a_full[wg * 3 + ab]);
+          // (5) issue stage gs - 1 if it is this warp's turn
+          if (gs >= 1 && ((gs - 1) & 3) == wq && lane == 0) issue(gs - 1, st > 0 ? st - 1 : nst - 1);
+          __syncwarp();
+          if (++st == nst) {
+            st = 0;
+            ++ul;
+          }
+        }
+      }
+      if (epi >= 0) {
+        epilogue(epi);
+        epi = -1;
+      }
+    }
+    if (((NS - 1) & 3) == wq && lane == 0) issue(NS - 1, st > 0 ? st - 1 : nst - 1);
+    __syncwarp();
+    for (int back = NS < 2 ? NS : 2; back >= 1; --back) {
+      const int e = NS - back;
+      mbar_wait_bounded(&done[wg * 3 + (e & 1)], (e >> 1) & 1, abort_flag, p.status);
+      __syncwarp();
+      tc_fence_after();
+      int est = st - back, eul = ul;
+      while (est < 0) {
+        est += nst;
+        --eul;
+      }
+      readback(est, eul, e & 1, back == 1 ? h1 : h2);
+    }
+    tc_fence_before();
+    if (epi >= 0) epilogue(epi);
+    epilogue(NU - 1);
+  } else {
+    for (int v = 0; v < NU; ++v) epilogue(v);
+  }
+
+  __syncthreads();
+  if (warp == 0) {
+    tc_fence_after();
+    tmem_dealloc(*tmem_base_p, kWG * kColsPerWG);
+  }
+}
+
 int ilog2(int v) {
   int l = 0;
   while ((1 << (l + 1)) <= v) ++l;
@@ -599,10 +959,36 @@ cudaError_t launch_tt(const FfnParams& p, int seg, int grid, int smem, cudaStrea
   return launch_k<MODE, 32, TT>(p, grid, smem, stream);
 }
 
+int smem_needed8(int K, int TT) {
+  const size_t b = make_layout8(K, TT).bytes;
+  return (int)(b > 120 * 1024 ? b : 120 * 1024);
+}
+
+template <int TT>
+cudaError_t launch_gateup_e4m3(const FfnParams& p, int grid, int smem, cudaStream_t stream) {
+  cudaError_t err = ensure_smem_limit(reinterpret_cast<const void*>(ffn_gateup_e4m3_kernel<TT>), smem);
+  if (err != cudaSuccess) return err;
+  ffn_gateup_e4m3_kernel<TT><<<grid, kThreads, smem, stream>>>(p);
+  return cudaGetLastError();
+}
+
 template <int MODE>
 cudaError_t launch_mode(const FfnParams& base, long long units, cudaStream_t stream) {
   FfnParams p = base;
   const int sms = device_sm_count();
+  if (MODE == 0 && p.G == SK8) {
+    // gate/up with FP8 weights in tensor memory: whole-group stages in every K slice
+    p.kq = pick_kq(p.K, p.G);
+    const int TT = p.T == 1 ? 1 : kTok;
+    const int smem = smem_needed8(p.K, TT);
+    if ((p.K / p.kq) % SK8 == 0 && smem <= device_max_smem_optin()) {
+      p.lgG = ilog2(p.G);
+      p.nB = 1;
+      const int grid = (int)(units < sms ? units : sms);
+      if (TT == 1) return launch_gateup_e4m3<1>(p, grid, smem, stream);
+      return launch_gateup_e4m3<kTok>(p, grid, smem, stream);
+    }
+  }
   p.kq = pick_kq(p.K, p.G);
   const int Kq = p.K / p.kq;
   p.lgG = ilog2(p.G);

@@ -114,6 +114,22 @@ __device__ __forceinline__ void umma_f16_tmem_a(uint32_t d_tmem, uint32_t a_tmem
       : "memory");
 }
 
+// kind::f8f6f4 with E4M3 A and B (format code 0) and an f32 accumulator: the
+// same descriptor bits as f16 A and B; each MMA consumes K = 32.
+__device__ __forceinline__ uint32_t umma_idesc_e4m3(int M, int N) { return umma_idesc_f16(M, N); }
+
+// D(tmem) (+)= A(tmem) * B(smem)^T with E4M3 operands: A is M lanes x 8 columns
+// (32 bytes of a lane per MMA).
+__device__ __forceinline__ void umma_e4m3_tmem_a(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
+                                                 uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
 // Arrives on `bar` once every tcgen05 MMA issued so far by this thread completed.
 __device__ __forceinline__ void umma_commit(uint64_t* bar) {
   asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(

@@ -172,24 +172,14 @@ __device__ __forceinline__ void decode_nibbles(uint32_t w, uint32_t (&p)[4]) {
   p[3] = h2_as_u32(__hfma2(u32_as_h2((w8 & hi_mask) | magic), k1_16, km72));
 }
 
-// Decodes the eight nibbles u0..u7 of one 32-bit word (u_i at bits 4i..4i+3)
-// into the FP8 E4M3 codes of the unsigned values u (0..15, all exact in E4M3),
-// in nibble order: lo = bytes of u0..u3, hi = bytes of u4..u7.  Each byte is a
-// table lookup (byte permute): nibbles 0-7 index the codes of 0..7 directly;
-// nibbles 8-15 have bit 3 set, which makes the same lookup return the sign of
-// a code (0x00), while the lookup with bit 3 flipped returns the codes of 8..15
-// for them and 0x00 for the others, so an OR of the two lookups is the code.
-__device__ __forceinline__ uint32_t byte_perm(uint32_t a, uint32_t b, uint32_t sel) {
-  uint32_t d;
-  asm("prmt.b32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(sel));
-  return d;
-}
-__device__ __forceinline__ void decode_nibbles_e4m3(uint32_t w, uint32_t& lo, uint32_t& hi) {
-  constexpr uint32_t kLow0 = 0x44403800u, kLow1 = 0x4E4C4A48u;     // E4M3 of 0, 1, ..., 7
-  constexpr uint32_t kHigh0 = 0x53525150u, kHigh1 = 0x57565554u;   // E4M3 of 8, 9, ..., 15
-  const uint32_t wx = w ^ 0x88888888u;
-  lo = byte_perm(kLow0, kLow1, w) | byte_perm(kHigh0, kHigh1, wx);
-  hi = byte_perm(kLow0, kLow1, w >> 16) | byte_perm(kHigh0, kHigh1, wx >> 16);
+// The nibbles u of a packed word as E4M3 codes, the code byte being the nibble
+// itself: exponent field u >> 3 and mantissa u & 7 make u < 8 the subnormal
+// u * 2^-9 and u >= 8 the normal (1 + (u & 7) / 8) * 2^-6 = u * 2^-9, so every
+// code is worth exactly u * 2^-9.  lo holds the low nibbles of the four bytes
+// (even reduction indices), hi the high ones (odd indices).
+__device__ __forceinline__ void split_nibbles_e4m3(uint32_t w, uint32_t& lo, uint32_t& hi) {
+  lo = w & 0x0F0F0F0Fu;
+  hi = (w >> 4) & 0x0F0F0F0Fu;
 }
 
 __device__ __forceinline__ float bf16_bits_to_float(uint32_t b) { return __uint_as_float(b << 16); }

@@ -567,14 +567,18 @@ __global__ void __launch_bounds__(kThreads, 1) ffn_decode_kernel(const FfnParams
 // ---------------------------------------------------------------- gate/up with FP8 weights in tensor memory
 //
 // For G = 128 the gate/up phase can hold the weights in tensor memory as FP8
-// E4M3 codes of the unsigned nibbles u = q + 8 (0..15, all exact in E4M3): one
-// byte per weight instead of two, so half the tcgen05.st traffic and half the
-// MMAs (kind::f8f6f4 consumes K = 32), and a 128-element stage (one whole
-// group) per synchronisation.  The tokens enter as E4M3 too: for each token
+// E4M3 codes of the unsigned nibbles u = q + 8: the code byte is the nibble
+// itself, worth u * 2^-9 (split_nibbles_e4m3), so the decode is a mask and a
+// shift.  One byte per weight instead of two, so half the tcgen05.st traffic
+// and half the MMAs (kind::f8f6f4 consumes K = 32), and a 128-element stage
+// (one whole group) per synchronisation.  A packed 32-bit word (reduction
+// indices 8w .. 8w + 7) becomes two TMEM columns, the even indices then the
+// odd ones, and the B operand is filled in that same order: physical position
+// 8w + 4h + i of a stage holds reduction index 8w + 2i + h.  The tokens enter as E4M3 too: for each token
 // and group, x * 2^e (e puts the group's largest |x| in [128, 256)) is written
 // as the sum of three E4M3 terms, which holds a bf16 value exactly unless it is
 // more than ~2^9 below the group's largest.  The group's dot product is then
-//   sum_k q_k x_k = 2^-e * sum_k u_k (t1 + t2 + t3)_k - 8 * sum_k x_k,
+//   sum_k q_k x_k = 2^(9-e) * sum_k (u_k 2^-9) (t1 + t2 + t3)_k - 8 * sum_k x_k,
 // with the first sum from the tensor core (products exact, fp32 accumulation)
 // and the correction precomputed per token and group from the same terms.
 // B rows: 3n + j = term j of token n (N = 16 for one token, 32 for eight).
@@ -683,12 +687,14 @@ __global__ void __launch_bounds__(kThreads, 1) ffn_gateup_e4m3_kernel(const FfnP
     tmem_alloc(tmem_base_p, kWG * kColsPerWG);
     tmem_relinquish();
   }
-  // B: per (token, group) one warp; lane l handles elements 4l .. 4l + 3 of the group
+  // B: per (token, group) one warp; lane l fills physical positions 4l .. 4l + 3
+  // of the group, i.e. reduction indices 8(l >> 1) + (l & 1) + 2i, i = 0..3
   for (int tg = warp; tg < p.T * KG; tg += kThreads / 32) {
     const int n = tg / KG, g = tg - n * KG;
-    const uint2 raw = __ldg(reinterpret_cast<const uint2*>(p.x + (size_t)n * p.H + g * SK8 + 4 * lane));
-    float v[4] = {bf16_bits_to_float(raw.x & 0xFFFFu), bf16_bits_to_float(raw.x >> 16),
-                  bf16_bits_to_float(raw.y & 0xFFFFu), bf16_bits_to_float(raw.y >> 16)};
+    const uint4 raw = __ldg(reinterpret_cast<const uint4*>(p.x + (size_t)n * p.H + g * SK8 + 8 * (lane >> 1)));
+    const int sh = 16 * (lane & 1);
+    float v[4] = {bf16_bits_to_float((raw.x >> sh) & 0xFFFFu), bf16_bits_to_float((raw.y >> sh) & 0xFFFFu),
+                  bf16_bits_to_float((raw.z >> sh) & 0xFFFFu), bf16_bits_to_float((raw.w >> sh) & 0xFFFFu)};
     float m = fmaxf(fmaxf(fabsf(v[0]), fabsf(v[1])), fmaxf(fabsf(v[2]), fabsf(v[3])));
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
@@ -717,7 +723,7 @@ __global__ void __launch_bounds__(kThreads, 1) ffn_gateup_e4m3_kernel(const FfnP
     for (int j = 0; j < 3; ++j)
       *reinterpret_cast<uint32_t*>(Bs + b8_offset(3 * n + j, g * SK8 + 4 * lane, BN8)) = t[j];
     if (lane == 0) {
-      Et[n * KG + g] = down;
+      Et[n * KG + g] = 512.0f * down;   // the codes carry 2^-9
       Ct[n * KG + g] = 8.0f * back * down;
     }
   }
@@ -851,14 +857,14 @@ __global__ void __launch_bounds__(kThreads, 1) ffn_gateup_e4m3_kernel(const FfnP
             __syncwarp();
             tc_fence_after();
           }
-          // (2) decode 128 nibbles of this row into 128 E4M3 codes, store them in TMEM
+          // (2) split 128 nibbles of this row into 128 E4M3 codes, store them in TMEM
           {
             uint32_t av[32];
 #pragma unroll
             for (int c = 0; c < 4; ++c) {
               const uint32_t wd[4] = {ring[j][c].x, ring[j][c].y, ring[j][c].z, ring[j][c].w};
 #pragma unroll
-              for (int w = 0; w < 4; ++w) decode_nibbles_e4m3(wd[w], av[8 * c + 2 * w], av[8 * c + 2 * w + 1]);
+              for (int w = 0; w < 4; ++w) split_nibbles_e4m3(wd[w], av[8 * c + 2 * w], av[8 * c + 2 * w + 1]);
             }
             tmem_st_32x32b_x32(tlane + tmem_wg + ab * kA8, av);
           }

@@ -566,7 +566,7 @@ __global__ void __launch_bounds__(kThreads, 1) ffn_decode_kernel(const FfnParams
 
 // ---------------------------------------------------------------- gate/up with FP8 weights in tensor memory
 //
-// For G = 128 the gate/up phase can hold the weights in tensor memory as FP8
+// For G = 128 both decode phases hold the weights in tensor memory as FP8
 // E4M3 codes of the unsigned nibbles u = q + 8: the code byte is the nibble
 // itself, worth u * 2^-9 (split_nibbles_e4m3), so the decode is a mask and a
 // shift.  One byte per weight instead of two, so half the tcgen05.st traffic
@@ -574,19 +574,30 @@ __global__ void __launch_bounds__(kThreads, 1) ffn_decode_kernel(const FfnParams
 // (one whole group) per synchronisation.  A packed 32-bit word (reduction
 // indices 8w .. 8w + 7) becomes two TMEM columns, the even indices then the
 // odd ones, and the B operand is filled in that same order: physical position
-// 8w + 4h + i of a stage holds reduction index 8w + 2i + h.  The tokens enter as E4M3 too: for each token
-// and group, x * 2^e (e puts the group's largest |x| in [128, 256)) is written
-// as the sum of three E4M3 terms, which holds a bf16 value exactly unless it is
-// more than ~2^9 below the group's largest.  The group's dot product is then
-//   sum_k q_k x_k = 2^(9-e) * sum_k (u_k 2^-9) (t1 + t2 + t3)_k - 8 * sum_k x_k,
+// 8w + 4h + i of a stage holds reduction index 8w + 2i + h.
+// The activations (x for gate/up, h for down) enter as E4M3 too: for each
+// token and group, v = x * 2^e (e puts the group's largest |x| in [128, 256))
+// is written as four terms, t_j = 2^-4j * E4M3(2^4j * r_j) with r_0 = v and
+// r_(j+1) = r_j - t_j, so every term is rounded in the normal E4M3 range and
+// the four keep about 16 significant bits of each element.  Term j is B row
+// 4n + j of token n (N = 16 for one token, 32 for eight), holding the code of
+// 2^4j * t_j; the readback adds the four accumulator columns with weights
+// 2^-4j.  The group's dot product is then
+//   sum_k q_k x_k = 2^(9-e) * sum_k (u_k 2^-9) (t_0 + .. + t_3)_k - 8 * sum_k x_k,
 // with the first sum from the tensor core (products exact, fp32 accumulation)
 // and the correction precomputed per token and group from the same terms.
-// B rows: 3n + j = term j of token n (N = 16 for one token, 32 for eight).
 // Pipeline as in the 64-element kernel with segment = stage: two A buffers, two
 // D buffers, item g read back during iteration g + 2, issued during g + 1 by
 // warp g mod 4.
 constexpr int SK8 = 128;                   // reduction elements per stage (one group)
 constexpr int kA8 = SK8 / 4;               // TMEM columns of one A buffer (4 codes per column)
+constexpr int kTerms = 4;                  // E4M3 terms per activation element
+
+// Accumulator columns of the four terms of one token, term j weighted 2^-4j.
+__device__ __forceinline__ float add_terms(uint32_t c0, uint32_t c1, uint32_t c2, uint32_t c3) {
+  const float s = 0.0625f;
+  return fmaf(fmaf(fmaf(__uint_as_float(c3), s, __uint_as_float(c2)), s, __uint_as_float(c1)), s, __uint_as_float(c0));
+}
 
 __host__ __device__ inline int bn8(int TT) { return TT == 1 ? 16 : 32; }
 
@@ -595,11 +606,11 @@ struct Layout8 {
   size_t bytes;
 };
 
-__host__ __device__ inline Layout8 make_layout8(int K, int TT) {
+__host__ __device__ inline Layout8 make_layout8(int K, int nB, int TT) {
   Layout8 L;
-  L.b_off = 0;                                          // bn8 rows x K bytes, swizzled (1024-aligned)
-  L.ec_off = L.b_off + bn8(TT) * K;                     // E[TT][K/128], C[TT][K/128] fp32
-  L.red_off = L.ec_off + 2 * TT * (K / SK8) * 4;        // 2 x kWG x BM x TT fp32
+  L.b_off = 0;                                          // nB x (bn8 rows x K bytes, swizzled; 1024-aligned)
+  L.ec_off = L.b_off + nB * bn8(TT) * K;                // nB x (E[TT][K/128], C[TT][K/128]) fp32
+  L.red_off = L.ec_off + nB * 2 * TT * (K / SK8) * 4;   // 2 x kWG x BM x TT fp32
   L.bar_off = L.red_off + 2 * kWG * BM * TT * 4;
   L.grp_off = L.bar_off + (kWG * 6 + 4) * 8;
   L.misc_off = L.grp_off + kMaxGroups * (int)sizeof(Group);
@@ -614,8 +625,8 @@ __device__ __forceinline__ uint32_t b8_offset(int n, int l, int rows) {
                     (byte & 15));
 }
 
-template <int TT>
-__global__ void __launch_bounds__(kThreads, 1) ffn_gateup_e4m3_kernel(const FfnParams p) {
+template <int MODE, int TT>
+__global__ void __launch_bounds__(kThreads, 1) ffn_e4m3_kernel(const FfnParams p) {
   constexpr int R = 2;                     // ring depth = unroll (2 x 64 bytes per thread in flight)
   constexpr int NA = 2;                    // A buffers (and D buffers) per warpgroup
   constexpr int BN8 = TT == 1 ? 16 : 32;   // MMA N
@@ -623,10 +634,10 @@ __global__ void __launch_bounds__(kThreads, 1) ffn_gateup_e4m3_kernel(const FfnP
   static_assert(kD0 + NA * BN8 <= kColsPerWG, "TMEM columns per warpgroup");
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
-  const Layout8 L = make_layout8(p.K, TT);
-  uint8_t* Bs = smem + L.b_off;
-  float* Et = reinterpret_cast<float*>(smem + L.ec_off);          // [TT][KG]: 2^-e
-  float* Ct = Et + TT * (p.K / SK8);                               // [TT][KG]: 8 * sum x
+  const Layout8 L = make_layout8(p.K, p.nB, TT);
+  uint8_t* Bs = smem + L.b_off;                                    // buffer j at j * b_bytes
+  float* Et = reinterpret_cast<float*>(smem + L.ec_off);          // buffer j at j * 2 * TT * KG: [TT][KG] 2^(9-e),
+                                                                   // then [TT][KG] 8 * sum of the represented values
   float* red = reinterpret_cast<float*>(smem + L.red_off);
   uint64_t* a_full = reinterpret_cast<uint64_t*>(smem + L.bar_off);
   uint64_t* done = a_full + kWG * 3;
@@ -649,6 +660,8 @@ __global__ void __launch_bounds__(kThreads, 1) ffn_gateup_e4m3_kernel(const FfnP
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int wg = tid >> 7, r = tid & 127, wq = warp & 3;
   const int KG = p.K / SK8;
+  const uint32_t b_bytes = (uint32_t)BN8 * p.K;
+  const int a_first = ub / upe, a_last = (ue - 1) / upe;
 
   for (int a = tid; a < ngroups; a += blockDim.x) {
     const int e = a < n_act ? (a == tid ? a_spec : __ldg(p.active + a)) : p.E;
@@ -657,18 +670,25 @@ __global__ void __launch_bounds__(kThreads, 1) ffn_gateup_e4m3_kernel(const FfnP
     int flags = 0;
     if (e >= 0 && e <= p.E) {
       const qre_slot* sl = p.slots + e;
-      w = sl->w_gate_up;
-      sc = sl->s_gate_up;
+      w = MODE == 0 ? sl->w_gate_up : sl->w_down;
+      sc = MODE == 0 ? sl->s_gate_up : sl->s_down;
       flags = (w && sc && ((reinterpret_cast<uintptr_t>(w) | reinterpret_cast<uintptr_t>(sc)) & 15) == 0) ? 1 : 0;
     }
-    if (!flags && a >= ub / upe && a <= (ue - 1) / upe) set_status(p.status, QRE_DEV_NULL_SLOT);
+    if (!flags && a >= a_first && a <= a_last) set_status(p.status, QRE_DEV_NULL_SLOT);
     Group& dst = groups[a];
     dst.w = w;
     dst.s = sc;
     dst.e = e;
     dst.flags = flags;
 #pragma unroll
-    for (int n = 0; n < kTok; ++n) dst.outq[n] = -1;
+    for (int n = 0; n < kTok; ++n) dst.outq[n] = (MODE == 1 && a == n_act && n < p.T) ? p.T * p.k + n : -1;
+    if (MODE == 1 && a < n_act && flags) {
+      const int lo = __ldg(p.offsets + e), hi = __ldg(p.offsets + e + 1);
+      for (int q = lo; q < hi && q < lo + kTok; ++q) {
+        const int tk = __ldg(p.perm + q) / p.k;
+        if (tk >= 0 && tk < kTok) dst.outq[tk] = q;
+      }
+    }
   }
   if (tid == 0) {
     for (int i = 0; i < kWG * 3; ++i) {
@@ -687,14 +707,40 @@ __global__ void __launch_bounds__(kThreads, 1) ffn_gateup_e4m3_kernel(const FfnP
     tmem_alloc(tmem_base_p, kWG * kColsPerWG);
     tmem_relinquish();
   }
-  // B: per (token, group) one warp; lane l fills physical positions 4l .. 4l + 3
-  // of the group, i.e. reduction indices 8(l >> 1) + (l & 1) + 2i, i = 0..3
-  for (int tg = warp; tg < p.T * KG; tg += kThreads / 32) {
+  // B: gate/up one buffer of the tokens, down one buffer of h per expert of the
+  // range (at most nB, by the launch).  Per (buffer, token, group) one warp;
+  // lane l fills physical positions 4l .. 4l + 3 of the group, i.e. reduction
+  // indices 8(l >> 1) + (l & 1) + 2i, i = 0..3.
+  const int nbuf = MODE == 0 ? 1 : (a_last - a_first + 1 < p.nB ? a_last - a_first + 1 : p.nB);
+  if (MODE == 1 && a_last - a_first >= p.nB && tid == 0) set_status(p.status, QRE_DEV_BAD_INDEX);
+  for (int job = warp; job < nbuf * p.T * KG; job += kThreads / 32) {
+    const int jb = job / (p.T * KG), tg = job - jb * (p.T * KG);
     const int n = tg / KG, g = tg - n * KG;
-    const uint4 raw = __ldg(reinterpret_cast<const uint4*>(p.x + (size_t)n * p.H + g * SK8 + 8 * (lane >> 1)));
-    const int sh = 16 * (lane & 1);
-    float v[4] = {bf16_bits_to_float((raw.x >> sh) & 0xFFFFu), bf16_bits_to_float((raw.y >> sh) & 0xFFFFu),
-                  bf16_bits_to_float((raw.z >> sh) & 0xFFFFu), bf16_bits_to_float((raw.w >> sh) & 0xFFFFu)};
+    const int hsel = lane & 1;
+    float v[4];
+    if constexpr (MODE == 0) {
+      const uint4 raw = __ldg(reinterpret_cast<const uint4*>(p.x + (size_t)n * p.H + g * SK8 + 8 * (lane >> 1)));
+      const int sh = 16 * hsel;
+      v[0] = bf16_bits_to_float((raw.x >> sh) & 0xFFFFu);
+      v[1] = bf16_bits_to_float((raw.y >> sh) & 0xFFFFu);
+      v[2] = bf16_bits_to_float((raw.z >> sh) & 0xFFFFu);
+      v[3] = bf16_bits_to_float((raw.w >> sh) & 0xFFFFu);
+    } else {
+      // h rows of the gate/up epilogue: high part and remainder, feature m of
+      // each 8-group at position 2 (m & 3) + (m >> 2); this lane's m = hsel + 2i
+      // sit in words hsel and hsel + 2: low halves (i = 0, 1), then high halves
+      const __half* hb = p.hbuf + ((size_t)(a_first + jb) * 2 * kTok + 2 * n) * p.I + g * SK8 + 8 * (lane >> 1);
+      const uint4 hv = *reinterpret_cast<const uint4*>(hb);
+      const uint4 lv = *reinterpret_cast<const uint4*>(hb + p.I);
+      const uint32_t ha = hsel ? hv.y : hv.x, hc = hsel ? hv.w : hv.z;
+      const uint32_t la = hsel ? lv.y : lv.x, lc = hsel ? lv.w : lv.z;
+      const float2 fha = __half22float2(u32_as_h2(ha)), fhc = __half22float2(u32_as_h2(hc));
+      const float2 fla = __half22float2(u32_as_h2(la)), flc = __half22float2(u32_as_h2(lc));
+      v[0] = fha.x + fla.x;
+      v[1] = fhc.x + flc.x;
+      v[2] = fha.y + fla.y;
+      v[3] = fhc.y + flc.y;
+    }
     float m = fmaxf(fmaxf(fabsf(v[0]), fabsf(v[1])), fmaxf(fabsf(v[2]), fabsf(v[3])));
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
@@ -702,15 +748,16 @@ __global__ void __launch_bounds__(kThreads, 1) ffn_gateup_e4m3_kernel(const FfnP
     int ex = m > 0.f ? 7 - (int)((__float_as_uint(m) >> 23) & 0xFF) + 127 : 0;
     ex = ex < -100 ? -100 : (ex > 100 ? 100 : ex);
     const float up = __uint_as_float((uint32_t)(127 + ex) << 23), down = __uint_as_float((uint32_t)(127 - ex) << 23);
-    uint32_t t[3] = {0u, 0u, 0u};   // 4 codes of each term
-    float back = 0.f;               // sum of the represented values of this lane's 4 elements
+    uint32_t t[kTerms] = {0u, 0u, 0u, 0u};   // 4 codes of each term
+    float back = 0.f;                        // sum of the represented values of this lane's 4 elements
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
       float rem = v[i] * up, rep = 0.f;
 #pragma unroll
-      for (int j = 0; j < 3; ++j) {
-        const __nv_fp8_storage_t c = __nv_cvt_float_to_fp8(rem, __NV_SATFINITE, __NV_E4M3);
-        const float cv = __half2float(__half(__nv_cvt_fp8_to_halfraw(c, __NV_E4M3)));
+      for (int j = 0; j < kTerms; ++j) {
+        const float lift = (float)(1 << (4 * j)), drop = 1.0f / lift;   // powers of two: exact
+        const __nv_fp8_storage_t c = __nv_cvt_float_to_fp8(rem * lift, __NV_SATFINITE, __NV_E4M3);
+        const float cv = __half2float(__half(__nv_cvt_fp8_to_halfraw(c, __NV_E4M3))) * drop;
         t[j] |= (uint32_t)c << (8 * i);
         rem -= cv;
         rep += cv;
@@ -720,11 +767,12 @@ __global__ void __launch_bounds__(kThreads, 1) ffn_gateup_e4m3_kernel(const FfnP
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) back += __shfl_xor_sync(0xffffffffu, back, o);
 #pragma unroll
-    for (int j = 0; j < 3; ++j)
-      *reinterpret_cast<uint32_t*>(Bs + b8_offset(3 * n + j, g * SK8 + 4 * lane, BN8)) = t[j];
+    for (int j = 0; j < kTerms; ++j)
+      *reinterpret_cast<uint32_t*>(Bs + jb * b_bytes + b8_offset(kTerms * n + j, g * SK8 + 4 * lane, BN8)) = t[j];
     if (lane == 0) {
-      Et[n * KG + g] = 512.0f * down;   // the codes carry 2^-9
-      Ct[n * KG + g] = 8.0f * back * down;
+      float* ec = Et + jb * 2 * TT * KG;
+      ec[n * KG + g] = 512.0f * down;   // the codes carry 2^-9
+      ec[TT * KG + n * KG + g] = 8.0f * back * down;
     }
   }
   fence_proxy_async_smem();
@@ -740,8 +788,8 @@ __global__ void __launch_bounds__(kThreads, 1) ffn_gateup_e4m3_kernel(const FfnP
   const int g0 = k0 / SK8;           // first group of this warpgroup's slice
 
   auto epilogue = [&](int v) {
-    finish_unit<0, TT>(v, ub, upe, groups, red, red_full, red_empty, p.kq, p.T, p.I, p.H, p.hbuf, p.expert_out,
-                       abort_flag, p.status);
+    finish_unit<MODE, TT>(v, ub, upe, groups, red, red_full, red_empty, p.kq, p.T, p.I, p.H, p.hbuf, p.expert_out,
+                          abort_flag, p.status);
   };
   int epi = -1;
 
@@ -797,22 +845,23 @@ __global__ void __launch_bounds__(kThreads, 1) ffn_gateup_e4m3_kernel(const FfnP
     auto readback = [&](int est, int eul, int db, uint32_t sp) {
       const float sc = __half2float(__ushort_as_half((unsigned short)sp));
       const int g = g0 + est;
+      const float* ec = MODE == 0 ? Et : Et + ((ub + eul) / upe - a_first) * 2 * TT * KG;
       if constexpr (TT == 1) {
         uint32_t dv[4];
         asm volatile("tcgen05.ld.sync.aligned.32x32b.x4.b32 {%0,%1,%2,%3}, [%4];"
                      : "=r"(dv[0]), "=r"(dv[1]), "=r"(dv[2]), "=r"(dv[3])
                      : "r"(tlane + tmem_wg + kD0 + BN8 * db));
         tmem_ld_wait();
-        const float d = __uint_as_float(dv[0]) + __uint_as_float(dv[1]) + __uint_as_float(dv[2]);
-        acc[0] = fmaf(sc, fmaf(d, Et[g], -Ct[g]), acc[0]);
+        const float d = add_terms(dv[0], dv[1], dv[2], dv[3]);
+        acc[0] = fmaf(sc, fmaf(d, ec[g], -ec[KG + g]), acc[0]);
       } else {
         uint32_t dv[32];
         tmem_ld_32x32b_x32(tlane + tmem_wg + kD0 + BN8 * db, dv);
         tmem_ld_wait();
 #pragma unroll
         for (int n = 0; n < TT; ++n) {
-          const float d = __uint_as_float(dv[3 * n]) + __uint_as_float(dv[3 * n + 1]) + __uint_as_float(dv[3 * n + 2]);
-          acc[n] = fmaf(sc, fmaf(d, Et[n * KG + g], -Ct[n * KG + g]), acc[n]);
+          const float d = add_terms(dv[4 * n], dv[4 * n + 1], dv[4 * n + 2], dv[4 * n + 3]);
+          acc[n] = fmaf(sc, fmaf(d, ec[n * KG + g], -ec[(TT + n) * KG + g]), acc[n]);
         }
       }
       if (est == nst - 1) {
@@ -831,12 +880,14 @@ __global__ void __launch_bounds__(kThreads, 1) ffn_gateup_e4m3_kernel(const FfnP
         if (eul >= 1) epi = eul - 1;
       }
     };
-    // lane 0 of warp (stage mod 4): the 4 MMAs of global stage i (stage ist of its unit), A/D buffer i & 1
-    auto issue = [&](int i, int ist) {
+    // lane 0 of warp (stage mod 4): the 4 MMAs of global stage i (stage ist of
+    // local unit iul), A/D buffer i & 1
+    auto issue = [&](int i, int ist, int iul) {
       const int ib = i & 1;
       mbar_wait_bounded(&a_full[wg * 3 + ib], (i >> 1) & 1, abort_flag, p.status);
       tc_fence_after();
-      const uint32_t bstage = bbase + (uint32_t)((g0 + ist) * (BN8 * 128));
+      const uint32_t bbuf = MODE == 0 ? 0u : (uint32_t)((ub + iul) / upe - a_first) * b_bytes;
+      const uint32_t bstage = bbase + bbuf + (uint32_t)((g0 + ist) * (BN8 * 128));
 #pragma unroll
       for (int q = 0; q < 4; ++q)
         umma_e4m3_tmem_a(tmem_wg + kD0 + BN8 * ib, tmem_wg + ib * kA8 + 8 * q, umma_desc_sw128(bstage + 32 * q), idesc,
@@ -887,7 +938,7 @@ __global__ void __launch_bounds__(kThreads, 1) ffn_gateup_e4m3_kernel(const FfnP
           __syncwarp();
           if (lane == 0) mbar_arrive(&a_full[wg * 3 + ab]);
           // (5) issue stage gs - 1 if it is this warp's turn
-          if (gs >= 1 && ((gs - 1) & 3) == wq && lane == 0) issue(gs - 1, st > 0 ? st - 1 : nst - 1);
+          if (gs >= 1 && ((gs - 1) & 3) == wq && lane == 0) issue(gs - 1, st > 0 ? st - 1 : nst - 1, st > 0 ? ul : ul - 1);
           __syncwarp();
           if (++st == nst) {
             st = 0;
@@ -900,7 +951,7 @@ __global__ void __launch_bounds__(kThreads, 1) ffn_gateup_e4m3_kernel(const FfnP
         epi = -1;
       }
     }
-    if (((NS - 1) & 3) == wq && lane == 0) issue(NS - 1, st > 0 ? st - 1 : nst - 1);
+    if (((NS - 1) & 3) == wq && lane == 0) issue(NS - 1, st > 0 ? st - 1 : nst - 1, st > 0 ? ul : ul - 1);
     __syncwarp();
     for (int back = NS < 2 ? NS : 2; back >= 1; --back) {
       const int e = NS - back;
@@ -965,50 +1016,53 @@ cudaError_t launch_tt(const FfnParams& p, int seg, int grid, int smem, cudaStrea
   return launch_k<MODE, 32, TT>(p, grid, smem, stream);
 }
 
-int smem_needed8(int K, int TT) {
-  const size_t b = make_layout8(K, TT).bytes;
+int smem_needed8(int K, int nB, int TT) {
+  const size_t b = make_layout8(K, nB, TT).bytes;
   return (int)(b > 120 * 1024 ? b : 120 * 1024);
 }
 
-template <int TT>
-cudaError_t launch_gateup_e4m3(const FfnParams& p, int grid, int smem, cudaStream_t stream) {
-  cudaError_t err = ensure_smem_limit(reinterpret_cast<const void*>(ffn_gateup_e4m3_kernel<TT>), smem);
+template <int MODE, int TT>
+cudaError_t launch_e4m3(const FfnParams& p, int grid, int smem, cudaStream_t stream) {
+  cudaError_t err = ensure_smem_limit(reinterpret_cast<const void*>(ffn_e4m3_kernel<MODE, TT>), smem);
   if (err != cudaSuccess) return err;
-  ffn_gateup_e4m3_kernel<TT><<<grid, kThreads, smem, stream>>>(p);
+  ffn_e4m3_kernel<MODE, TT><<<grid, kThreads, smem, stream>>>(p);
   return cudaGetLastError();
+}
+
+// One CTA per SM.  The down kernels hold the B operand (h) of every expert of
+// their range in shared memory, so their ranges span at most nB experts: with
+// two buffers at least one CTA per group (ranges of at most one expert's
+// units), with one buffer one unit per CTA.
+long long decode_grid(int MODE, int nB, long long units, int amax, int sms) {
+  long long grid = units < sms ? units : sms;
+  if (MODE == 1) grid = nB == 2 ? (grid > amax + 1 ? grid : amax + 1) : units;
+  return grid;
 }
 
 template <int MODE>
 cudaError_t launch_mode(const FfnParams& base, long long units, cudaStream_t stream) {
   FfnParams p = base;
   const int sms = device_sm_count();
-  if (MODE == 0 && p.G == SK8) {
-    // gate/up with FP8 weights in tensor memory: whole-group stages in every K slice
+  const int budget = device_max_smem_optin();
+  const int TT = p.T == 1 ? 1 : kTok;
+  p.lgG = ilog2(p.G);
+  if (p.G == SK8) {
+    // FP8 weights in tensor memory: whole-group stages in every K slice
     p.kq = pick_kq(p.K, p.G);
-    const int TT = p.T == 1 ? 1 : kTok;
-    const int smem = smem_needed8(p.K, TT);
-    if ((p.K / p.kq) % SK8 == 0 && smem <= device_max_smem_optin()) {
-      p.lgG = ilog2(p.G);
-      p.nB = 1;
-      const int grid = (int)(units < sms ? units : sms);
-      if (TT == 1) return launch_gateup_e4m3<1>(p, grid, smem, stream);
-      return launch_gateup_e4m3<kTok>(p, grid, smem, stream);
+    p.nB = (MODE == 1 && smem_needed8(p.K, 2, TT) <= budget) ? 2 : 1;
+    const int smem = smem_needed8(p.K, p.nB, TT);
+    if (p.kq > 0 && (p.K / p.kq) % SK8 == 0 && smem <= budget) {
+      const int grid = (int)decode_grid(MODE, p.nB, units, p.amax, sms);
+      if (TT == 1) return launch_e4m3<MODE, 1>(p, grid, smem, stream);
+      return launch_e4m3<MODE, kTok>(p, grid, smem, stream);
     }
   }
   p.kq = pick_kq(p.K, p.G);
   const int Kq = p.K / p.kq;
-  p.lgG = ilog2(p.G);
   const int seg = Kq < p.G ? Kq : p.G;
-  const int TT = p.T == 1 ? 1 : kTok;
-  const int budget = device_max_smem_optin();
   p.nB = (MODE == 1 && smem_needed(p.K, 2, TT) <= budget) ? 2 : 1;
   const int smem = smem_needed(p.K, p.nB, TT);
-  // one CTA per SM; the down kernel holds h of every expert of its range in
-  // shared memory, so its ranges span at most nB experts: with two buffers at
-  // least one CTA per group (ranges of at most one expert's units), with one
-  // buffer one unit per CTA
-  long long grid = units < sms ? units : sms;
-  if (MODE == 1) grid = p.nB == 2 ? (grid > p.amax + 1 ? grid : p.amax + 1) : units;
+  const long long grid = decode_grid(MODE, p.nB, units, p.amax, sms);
   if (TT == 1) return launch_tt<MODE, 1>(p, seg, (int)grid, smem, stream);
   return launch_tt<MODE, kTok>(p, seg, (int)grid, smem, stream);
 }

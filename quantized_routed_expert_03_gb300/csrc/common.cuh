@@ -67,8 +67,10 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
 // from the first failed poll.  Gives up early when *abort is set by another
 // warp; on expiry sets *abort and QRE_DEV_TIMEOUT.  Returns true when the phase
 // completed.
-__device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity, volatile int* abort, int* status) {
-  if (mbar_try_wait(bar, parity)) return true;
+// The polling loop is out of line: the hot loops that wait on barriers keep
+// only the first poll and a call, which keeps their code small enough for the
+// instruction cache.
+static __device__ __noinline__ bool mbar_wait_slow(uint64_t* bar, uint32_t parity, volatile int* abort, int* status) {
   const uint64_t deadline = global_timer_ns() + kWaitLimitNs;
   uint32_t spins = 0;
   while (!mbar_try_wait(bar, parity)) {
@@ -80,6 +82,10 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity
     }
   }
   return true;
+}
+__device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity, volatile int* abort, int* status) {
+  if (mbar_try_wait(bar, parity)) return true;
+  return mbar_wait_slow(bar, parity, abort, status);
 }
 
 // ---------------------------------------------------------------- bulk copy
@@ -104,6 +110,13 @@ __device__ __forceinline__ void cp_async_arrive(uint64_t* bar) {
   asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(smem_addr(bar)) : "memory");
 }
 __device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
+// Closes this thread's current group of cp.async copies (an empty group if it
+// issued none), and waits until at most N of its groups are still in flight.
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait_group() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
 
 // Returns its argument through a volatile instruction: shared-memory loads whose
 // address depends on the result stay after every earlier volatile asm (such as
@@ -180,6 +193,14 @@ __device__ __forceinline__ void decode_nibbles(uint32_t w, uint32_t (&p)[4]) {
 __device__ __forceinline__ void split_nibbles_e4m3(uint32_t w, uint32_t& lo, uint32_t& hi) {
   lo = w & 0x0F0F0F0Fu;
   hi = (w >> 4) & 0x0F0F0F0Fu;
+}
+
+// 16-byte read-only load that stays where it is written (volatile asm is not
+// moved across other volatile asm, such as later cp.async copies).
+__device__ __forceinline__ uint4 ldg_v4_early(const void* p) {
+  uint4 v;
+  asm volatile("ld.global.nc.v4.u32 {%0,%1,%2,%3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "l"(p));
+  return v;
 }
 
 __device__ __forceinline__ float bf16_bits_to_float(uint32_t b) { return __uint_as_float(b << 16); }

@@ -132,10 +132,12 @@ __device__ __forceinline__ void load_h(uint8_t* dst, const __half* hbuf, int a, 
 // A unit's epilogue (local unit v of the CTA's range starting at unit ub).
 // TT = 8: thread (wg, r) finishes row r for tokens 2wg and 2wg + 1; TT = 1:
 // warpgroup 0 finishes token 0.  Gate/up: h = silu(gate) * up of each row pair
-// (gate row in lanes 0-15, its up row 16 lanes above) into hbuf as fp16 high
-// part and remainder; down: the expert's output rows.  Whole warps call it;
-// every thread of the CTA arrives on red_empty.
-template <int MODE, int TT>
+// (gate row in lanes 0-15, its up row 16 lanes above) into hbuf, for the fp16
+// down kernel as fp16 high part and remainder (rows 2n, 2n + 1 of the group),
+// for the FP8 one (H32) as fp32 (row n) with each 8-feature block in the FP8
+// B operand's order (feature 2i + h at 4h + i); down: the expert's output
+// rows.  Whole warps call it; every thread of the CTA arrives on red_empty.
+template <int MODE, int TT, bool H32 = false>
 __device__ __noinline__ void finish_unit(int v, int ub, int upe, const Group* groups, const float* red,
                                          uint64_t* red_full, uint64_t* red_empty, int kq, int T, int I, int H,
                                          __half* hbuf, float* expert_out, volatile int* abort_flag, int* status) {
@@ -154,7 +156,16 @@ __device__ __noinline__ void finish_unit(int v, int ub, int upe, const Group* gr
 #pragma unroll
       for (int t = 0; t < NT; ++t) vv[t] += rr[t];
     }
-    if constexpr (MODE == 0) {
+    if constexpr (MODE == 0 && H32) {
+      const int f = m0 / 2 + 16 * (r >> 5) + (r & 15);
+      const int pos = (f & ~7) | ((f & 1) << 2) | ((f >> 1) & 3);
+      float* hb = reinterpret_cast<float*>(hbuf) + (size_t)a * kTok * I;
+#pragma unroll
+      for (int t = 0; t < NT; ++t) {
+        const float up = __shfl_down_sync(0xffffffffu, vv[t], 16);
+        if ((lane & 16) == 0 && n0 + t < T) hb[(size_t)(n0 + t) * I + pos] = silu_f32(vv[t]) * up;
+      }
+    } else if constexpr (MODE == 0) {
       const int f = m0 / 2 + 16 * (r >> 5) + (r & 15);
       const int pos = (f & ~7) | (((f & 3) << 1) | ((f >> 2) & 1));
       __half* hb = hbuf + (size_t)a * 2 * kTok * I;
@@ -577,13 +588,16 @@ __global__ void __launch_bounds__(kThreads, 1) ffn_decode_kernel(const FfnParams
 // 8w + 4h + i of a stage holds reduction index 8w + 2i + h.
 // The activations (x for gate/up, h for down) enter as E4M3 too: for each
 // token and group, v = x * 2^e (e puts the group's largest |x| in [128, 256))
-// is written as four terms, t_j = 2^-4j * E4M3(2^4j * r_j) with r_0 = v and
-// r_(j+1) = r_j - t_j, so every term is rounded in the normal E4M3 range and
-// the four keep about 16 significant bits of each element.  Term j is B row
-// 4n + j of token n (N = 16 for one token, 32 for eight), holding the code of
-// 2^4j * t_j; the readback adds the four accumulator columns with weights
-// 2^-4j.  The group's dot product is then
-//   sum_k q_k x_k = 2^(9-e) * sum_k (u_k 2^-9) (t_0 + .. + t_3)_k - 8 * sum_k x_k,
+// is written as terms t_j = 2^-4j * E4M3(2^4j * r_j) with r_0 = v and
+// r_(j+1) = r_j - t_j, so every term is rounded in the normal E4M3 range.  Two
+// terms hold a bf16 x exactly (its 8 significant bits split 4 + 4, the second
+// residual fitting 4 bits after round-to-nearest) unless the element is below
+// 2^-13 of its group's largest; h, an fp32 value, takes four (about 16
+// significant bits).  Term j of token n is B row NT n + j (NT terms; N = 16,
+// or 32 for eight tokens of h), holding the code of 2^4j * t_j; the readback
+// adds the NT accumulator columns with weights 2^-4j.  The group's dot product
+// is then
+//   sum_k q_k x_k = 2^(9-e) * sum_k (u_k 2^-9) (t_0 + .. + t_(NT-1))_k - 8 * sum_k x_k,
 // with the first sum from the tensor core (products exact, fp32 accumulation)
 // and the correction precomputed per token and group from the same terms.
 // Pipeline as in the 64-element kernel with segment = stage: two A buffers, two
@@ -591,26 +605,41 @@ __global__ void __launch_bounds__(kThreads, 1) ffn_decode_kernel(const FfnParams
 // warp g mod 4.
 constexpr int SK8 = 128;                   // reduction elements per stage (one group)
 constexpr int kA8 = SK8 / 4;               // TMEM columns of one A buffer (4 codes per column)
-constexpr int kTerms = 4;                  // E4M3 terms per activation element
+// E4M3 terms per activation element: x (bf16) two, h (fp32) four.
+__host__ __device__ constexpr int n_terms(int MODE) { return MODE == 0 ? 2 : 4; }
 
-// Accumulator columns of the four terms of one token, term j weighted 2^-4j.
-__device__ __forceinline__ float add_terms(uint32_t c0, uint32_t c1, uint32_t c2, uint32_t c3) {
-  const float s = 0.0625f;
-  return fmaf(fmaf(fmaf(__uint_as_float(c3), s, __uint_as_float(c2)), s, __uint_as_float(c1)), s, __uint_as_float(c0));
+// Accumulator columns of the NT terms of one token, term j weighted 2^-4j.
+template <int NT>
+__device__ __forceinline__ float add_terms(const uint32_t* c) {
+  float d = __uint_as_float(c[NT - 1]);
+#pragma unroll
+  for (int j = NT - 2; j >= 0; --j) d = fmaf(d, 0.0625f, __uint_as_float(c[j]));
+  return d;
 }
 
-__host__ __device__ inline int bn8(int TT) { return TT == 1 ? 16 : 32; }
+// MMA N (B rows) of the FP8 kernel: NT terms per token, at least 16.
+__host__ __device__ constexpr int bn8(int MODE, int TT) { return n_terms(MODE) * TT <= 16 ? 16 : 32; }
+
+// Where shared memory allows, the weights stream through a ring of stages
+// that every thread fills with cp.async (its own 4 x 16 bytes per stage, read
+// back by itself, so only cp.async groups order them): kStages8 stages in
+// flight without holding registers.  The down kernel for eight tokens keeps a
+// register ring (two experts' h take 128 KB).
+constexpr int kStages8 = 2;
+constexpr int kStageBytes8 = BM * SK8 / 2;   // one warpgroup's stage: 128 rows x 128 nibbles
+__host__ __device__ constexpr int ring8_stages(int MODE, int TT) { return (TT == 1 || MODE == 0) ? kStages8 : 0; }
 
 struct Layout8 {
-  int b_off, ec_off, red_off, bar_off, grp_off, misc_off;
+  int b_off, ec_off, ring_off, red_off, bar_off, grp_off, misc_off;
   size_t bytes;
 };
 
-__host__ __device__ inline Layout8 make_layout8(int K, int nB, int TT) {
+__host__ __device__ inline Layout8 make_layout8(int MODE, int K, int nB, int TT) {
   Layout8 L;
   L.b_off = 0;                                          // nB x (bn8 rows x K bytes, swizzled; 1024-aligned)
-  L.ec_off = L.b_off + nB * bn8(TT) * K;                // nB x (E[TT][K/128], C[TT][K/128]) fp32
-  L.red_off = L.ec_off + nB * 2 * TT * (K / SK8) * 4;   // 2 x kWG x BM x TT fp32
+  L.ec_off = L.b_off + nB * bn8(MODE, TT) * K;          // nB x (E[TT][K/128], C[TT][K/128]) fp32
+  L.ring_off = (L.ec_off + nB * 2 * TT * (K / SK8) * 4 + 127) & ~127;   // [stage][kWG] x 8 KB
+  L.red_off = L.ring_off + ring8_stages(MODE, TT) * kWG * kStageBytes8;   // 2 x kWG x BM x TT fp32
   L.bar_off = L.red_off + 2 * kWG * BM * TT * 4;
   L.grp_off = L.bar_off + (kWG * 6 + 4) * 8;
   L.misc_off = L.grp_off + kMaxGroups * (int)sizeof(Group);
@@ -625,16 +654,82 @@ __device__ __forceinline__ uint32_t b8_offset(int n, int l, int rows) {
                     (byte & 15));
 }
 
+// One B operand job of the FP8 kernel: (buffer jb, token n, group g) of job
+// index `job`, whose raw activations are `raw` (gate/up: 8 bf16 of which this
+// lane takes the even or odd ones; down: 4 fp32 h in B order).  Lane l writes
+// physical positions 4l .. 4l + 3 of the group's four term rows, and lane 0 the
+// group's 2^(9-e) and offset entries.  Out of line: one copy of the code for
+// all jobs.
+template <int MODE, int TT, int BN8, int NT>
+__device__ __noinline__ void e4m3_b_job(int job, const uint4 raw, int T, int KG, uint8_t* Bs, float* Et,
+                                        uint32_t b_bytes) {
+  const int lane = threadIdx.x & 31;
+  const int jb = job >= T * KG ? 1 : 0, tg = job - jb * (T * KG);   // at most two buffers
+  const int n = tg / KG, g = tg - n * KG;
+  float v[4];
+  if constexpr (MODE == 0) {
+    const int sh = 16 * (lane & 1);
+    v[0] = bf16_bits_to_float((raw.x >> sh) & 0xFFFFu);
+    v[1] = bf16_bits_to_float((raw.y >> sh) & 0xFFFFu);
+    v[2] = bf16_bits_to_float((raw.z >> sh) & 0xFFFFu);
+    v[3] = bf16_bits_to_float((raw.w >> sh) & 0xFFFFu);
+  } else {
+    v[0] = __uint_as_float(raw.x);   // h is stored in this order (H32 epilogue)
+    v[1] = __uint_as_float(raw.y);
+    v[2] = __uint_as_float(raw.z);
+    v[3] = __uint_as_float(raw.w);
+  }
+  float m = fmaxf(fmaxf(fabsf(v[0]), fabsf(v[1])), fmaxf(fabsf(v[2]), fabsf(v[3])));
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+  // 2^e with m * 2^e in [128, 256): from the exponent field of m
+  int ex = m > 0.f ? 7 - (int)((__float_as_uint(m) >> 23) & 0xFF) + 127 : 0;
+  ex = ex < -100 ? -100 : (ex > 100 ? 100 : ex);
+  const float up = __uint_as_float((uint32_t)(127 + ex) << 23), down = __uint_as_float((uint32_t)(127 - ex) << 23);
+  uint32_t t[NT];    // 4 codes of each term
+  float back = 0.f;  // sum of the represented values of this lane's 4 elements
+#pragma unroll
+  for (int j = 0; j < NT; ++j) t[j] = 0u;
+#pragma unroll
+  for (int k = 0; k < 2; ++k) {   // elements 2k, 2k + 1, converted as a pair
+    float2 rem = make_float2(v[2 * k] * up, v[2 * k + 1] * up);
+#pragma unroll
+    for (int j = 0; j < NT; ++j) {
+      const float lift = (float)(1 << (4 * j)), drop = 1.0f / lift;   // powers of two: exact
+      const __nv_fp8x2_storage_t c = __nv_cvt_float2_to_fp8x2(make_float2(rem.x * lift, rem.y * lift),
+                                                              __NV_SATFINITE, __NV_E4M3);
+      const __half2_raw hr = __nv_cvt_fp8x2_to_halfraw2(c, __NV_E4M3);
+      const float2 cv = __half22float2(__half2(hr));
+      t[j] |= (uint32_t)c << (16 * k);   // element 2k in the low byte
+      rem.x -= cv.x * drop;
+      rem.y -= cv.y * drop;
+      back += (cv.x + cv.y) * drop;
+    }
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) back += __shfl_xor_sync(0xffffffffu, back, o);
+#pragma unroll
+  for (int j = 0; j < NT; ++j)
+    *reinterpret_cast<uint32_t*>(Bs + jb * b_bytes + b8_offset(NT * n + j, g * SK8 + 4 * lane, BN8)) = t[j];
+  if (lane == 0) {
+    float* ec = Et + jb * 2 * TT * KG;
+    ec[n * KG + g] = 512.0f * down;   // the codes carry 2^-9
+    ec[TT * KG + n * KG + g] = 8.0f * back * down;
+  }
+}
+
 template <int MODE, int TT>
 __global__ void __launch_bounds__(kThreads, 1) ffn_e4m3_kernel(const FfnParams p) {
-  constexpr int R = 2;                     // ring depth = unroll (2 x 64 bytes per thread in flight)
+  constexpr int kStages = ring8_stages(MODE, TT);   // shared-memory ring depth (0: register ring)
+  constexpr int R = kStages ? kStages : 2;          // ring depth = unroll
   constexpr int NA = 2;                    // A buffers (and D buffers) per warpgroup
-  constexpr int BN8 = TT == 1 ? 16 : 32;   // MMA N
+  constexpr int NT = n_terms(MODE);
+  constexpr int BN8 = bn8(MODE, TT);       // MMA N
   constexpr int kD0 = NA * kA8;            // first D column
   static_assert(kD0 + NA * BN8 <= kColsPerWG, "TMEM columns per warpgroup");
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
-  const Layout8 L = make_layout8(p.K, p.nB, TT);
+  const Layout8 L = make_layout8(MODE, p.K, p.nB, TT);
   uint8_t* Bs = smem + L.b_off;                                    // buffer j at j * b_bytes
   float* Et = reinterpret_cast<float*>(smem + L.ec_off);          // buffer j at j * 2 * TT * KG: [TT][KG] 2^(9-e),
                                                                    // then [TT][KG] 8 * sum of the represented values
@@ -647,6 +742,32 @@ __global__ void __launch_bounds__(kThreads, 1) ffn_e4m3_kernel(const FfnParams p
   uint32_t* tmem_base_p = reinterpret_cast<uint32_t*>(smem + L.misc_off);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L.misc_off + 4);
 
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int KG = p.K / SK8;
+  // B operand jobs: (buffer jb, token n, group g), one warp each, lane l
+  // holding physical positions 4l .. 4l + 3 of the group (reduction indices
+  // 8(l >> 1) + (l & 1) + 2i).  A warp's first kJB jobs have their loads in
+  // flight before the group table: the tokens do not depend on the routing,
+  // h only on the range.
+  constexpr int kJB = 8;
+  const float* hb32 = reinterpret_cast<const float*>(p.hbuf);
+  // jobs of one buffer are (n, g) row-major, i.e. consecutive 128-element
+  // blocks of the activation rows (x rows of H = KG * 128, h rows of I)
+  const int tjobs = p.T * KG;   // jobs per buffer; at most two buffers
+  auto job_load = [&](int job, int a0) -> uint4 {
+    const int jb = job >= tjobs ? 1 : 0, rem = job - jb * tjobs;
+    if constexpr (MODE == 0)
+      return ldg_v4_early(p.x + (size_t)rem * SK8 + 8 * (lane >> 1));
+    else
+      return ldg_v4_early(hb32 + (size_t)(a0 + jb) * kTok * p.I + (size_t)rem * SK8 + 4 * lane);
+  };
+  uint4 pre[kJB];
+  if constexpr (MODE == 0) {
+#pragma unroll
+    for (int b = 0; b < kJB; ++b)
+      if (warp + 16 * b < p.T * KG) pre[b] = job_load(warp + 16 * b, 0);
+  }
+
   const int a_spec = threadIdx.x < p.amax ? __ldg(p.active + threadIdx.x) : p.E;
   int n_act = *p.n_active;
   n_act = n_act < 0 ? 0 : (n_act > p.amax ? p.amax : n_act);
@@ -657,14 +778,24 @@ __global__ void __launch_bounds__(kThreads, 1) ffn_e4m3_kernel(const FfnParams p
   const int ue = (int)((long long)(blockIdx.x + 1) * U / gridDim.x);
   if (ub >= ue) return;
 
-  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int wg = tid >> 7, r = tid & 127, wq = warp & 3;
-  const int KG = p.K / SK8;
   const uint32_t b_bytes = (uint32_t)BN8 * p.K;
   const int a_first = ub / upe, a_last = (ue - 1) / upe;
+  const int nbuf = MODE == 0 ? 1 : (a_last - a_first + 1 < p.nB ? a_last - a_first + 1 : p.nB);
+  const int njobs = nbuf * p.T * KG;
+  if constexpr (MODE == 1) {
+#pragma unroll
+    for (int b = 0; b < kJB; ++b)
+      if (warp + 16 * b < njobs) pre[b] = job_load(warp + 16 * b, a_first);
+  }
 
+  int olo = 0, ohi = 0;   // down: the dispatch range of this thread's group (tid < n_act)
   for (int a = tid; a < ngroups; a += blockDim.x) {
     const int e = a < n_act ? (a == tid ? a_spec : __ldg(p.active + a)) : p.E;
+    if (MODE == 1 && a < n_act && a == tid && e >= 0 && e < p.E) {
+      olo = __ldg(p.offsets + e);   // in flight with the slot entry
+      ohi = __ldg(p.offsets + e + 1);
+    }
     const uint8_t* w = nullptr;
     const uint16_t* sc = nullptr;
     int flags = 0;
@@ -673,6 +804,7 @@ __global__ void __launch_bounds__(kThreads, 1) ffn_e4m3_kernel(const FfnParams p
       w = MODE == 0 ? sl->w_gate_up : sl->w_down;
       sc = MODE == 0 ? sl->s_gate_up : sl->s_down;
       flags = (w && sc && ((reinterpret_cast<uintptr_t>(w) | reinterpret_cast<uintptr_t>(sc)) & 15) == 0) ? 1 : 0;
+      if (flags && sl->tier != 0) flags |= 2;   // host-mapped: plain loads only
     }
     if (!flags && a >= a_first && a <= a_last) set_status(p.status, QRE_DEV_NULL_SLOT);
     Group& dst = groups[a];
@@ -682,13 +814,6 @@ __global__ void __launch_bounds__(kThreads, 1) ffn_e4m3_kernel(const FfnParams p
     dst.flags = flags;
 #pragma unroll
     for (int n = 0; n < kTok; ++n) dst.outq[n] = (MODE == 1 && a == n_act && n < p.T) ? p.T * p.k + n : -1;
-    if (MODE == 1 && a < n_act && flags) {
-      const int lo = __ldg(p.offsets + e), hi = __ldg(p.offsets + e + 1);
-      for (int q = lo; q < hi && q < lo + kTok; ++q) {
-        const int tk = __ldg(p.perm + q) / p.k;
-        if (tk >= 0 && tk < kTok) dst.outq[tk] = q;
-      }
-    }
   }
   if (tid == 0) {
     for (int i = 0; i < kWG * 3; ++i) {
@@ -707,136 +832,132 @@ __global__ void __launch_bounds__(kThreads, 1) ffn_e4m3_kernel(const FfnParams p
     tmem_alloc(tmem_base_p, kWG * kColsPerWG);
     tmem_relinquish();
   }
-  // B: gate/up one buffer of the tokens, down one buffer of h per expert of the
-  // range (at most nB, by the launch).  Per (buffer, token, group) one warp;
-  // lane l fills physical positions 4l .. 4l + 3 of the group, i.e. reduction
-  // indices 8(l >> 1) + (l & 1) + 2i, i = 0..3.
-  const int nbuf = MODE == 0 ? 1 : (a_last - a_first + 1 < p.nB ? a_last - a_first + 1 : p.nB);
-  if (MODE == 1 && a_last - a_first >= p.nB && tid == 0) set_status(p.status, QRE_DEV_BAD_INDEX);
-  for (int job = warp; job < nbuf * p.T * KG; job += kThreads / 32) {
-    const int jb = job / (p.T * KG), tg = job - jb * (p.T * KG);
-    const int n = tg / KG, g = tg - n * KG;
-    const int hsel = lane & 1;
-    float v[4];
-    if constexpr (MODE == 0) {
-      const uint4 raw = __ldg(reinterpret_cast<const uint4*>(p.x + (size_t)n * p.H + g * SK8 + 8 * (lane >> 1)));
-      const int sh = 16 * hsel;
-      v[0] = bf16_bits_to_float((raw.x >> sh) & 0xFFFFu);
-      v[1] = bf16_bits_to_float((raw.y >> sh) & 0xFFFFu);
-      v[2] = bf16_bits_to_float((raw.z >> sh) & 0xFFFFu);
-      v[3] = bf16_bits_to_float((raw.w >> sh) & 0xFFFFu);
-    } else {
-      // h rows of the gate/up epilogue: high part and remainder, feature m of
-      // each 8-group at position 2 (m & 3) + (m >> 2); this lane's m = hsel + 2i
-      // sit in words hsel and hsel + 2: low halves (i = 0, 1), then high halves
-      const __half* hb = p.hbuf + ((size_t)(a_first + jb) * 2 * kTok + 2 * n) * p.I + g * SK8 + 8 * (lane >> 1);
-      const uint4 hv = *reinterpret_cast<const uint4*>(hb);
-      const uint4 lv = *reinterpret_cast<const uint4*>(hb + p.I);
-      const uint32_t ha = hsel ? hv.y : hv.x, hc = hsel ? hv.w : hv.z;
-      const uint32_t la = hsel ? lv.y : lv.x, lc = hsel ? lv.w : lv.z;
-      const float2 fha = __half22float2(u32_as_h2(ha)), fhc = __half22float2(u32_as_h2(hc));
-      const float2 fla = __half22float2(u32_as_h2(la)), flc = __half22float2(u32_as_h2(lc));
-      v[0] = fha.x + fla.x;
-      v[1] = fhc.x + flc.x;
-      v[2] = fha.y + fla.y;
-      v[3] = fhc.y + flc.y;
-    }
-    float m = fmaxf(fmaxf(fabsf(v[0]), fabsf(v[1])), fmaxf(fabsf(v[2]), fabsf(v[3])));
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
-    // 2^e with m * 2^e in [128, 256): from the exponent field of m
-    int ex = m > 0.f ? 7 - (int)((__float_as_uint(m) >> 23) & 0xFF) + 127 : 0;
-    ex = ex < -100 ? -100 : (ex > 100 ? 100 : ex);
-    const float up = __uint_as_float((uint32_t)(127 + ex) << 23), down = __uint_as_float((uint32_t)(127 - ex) << 23);
-    uint32_t t[kTerms] = {0u, 0u, 0u, 0u};   // 4 codes of each term
-    float back = 0.f;                        // sum of the represented values of this lane's 4 elements
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      float rem = v[i] * up, rep = 0.f;
-#pragma unroll
-      for (int j = 0; j < kTerms; ++j) {
-        const float lift = (float)(1 << (4 * j)), drop = 1.0f / lift;   // powers of two: exact
-        const __nv_fp8_storage_t c = __nv_cvt_float_to_fp8(rem * lift, __NV_SATFINITE, __NV_E4M3);
-        const float cv = __half2float(__half(__nv_cvt_fp8_to_halfraw(c, __NV_E4M3))) * drop;
-        t[j] |= (uint32_t)c << (8 * i);
-        rem -= cv;
-        rep += cv;
-      }
-      back += rep;
-    }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) back += __shfl_xor_sync(0xffffffffu, back, o);
-#pragma unroll
-    for (int j = 0; j < kTerms; ++j)
-      *reinterpret_cast<uint32_t*>(Bs + jb * b_bytes + b8_offset(kTerms * n + j, g * SK8 + 4 * lane, BN8)) = t[j];
-    if (lane == 0) {
-      float* ec = Et + jb * 2 * TT * KG;
-      ec[n * KG + g] = 512.0f * down;   // the codes carry 2^-9
-      ec[TT * KG + n * KG + g] = 8.0f * back * down;
-    }
-  }
-  fence_proxy_async_smem();
-  tc_fence_before();
+  // The weight stream does not depend on the activations: with the group
+  // table in place every warpgroup puts its first ring stages in flight, and
+  // the B operand is built while they travel.
   __syncthreads();
-  tc_fence_after();
-
   const int NU = ue - ub;
   const int Kq = p.K / p.kq;
   const int nst = Kq / SK8;
   const int NS = NU * nst;
   const int k0 = wg * Kq;
   const int g0 = k0 / SK8;           // first group of this warpgroup's slice
+  const int KS = p.K / SK;           // 64-element chunks per row block
+
+  int lu = ub, lst = 0;
+  const uint4* lptr = nullptr;
+  const unsigned short* lsp = nullptr;
+  bool lhost = false;
+  auto cursor_unit = [&](int u) {
+    const int a = u / upe, m0 = (u - a * upe) * BM;
+    const Group& gr = groups[a];
+    if (gr.flags & 1) {
+      lptr = reinterpret_cast<const uint4*>(gr.w + ((size_t)(m0 / BM) * KS + k0 / SK) * kChunk) + r;
+      lsp = reinterpret_cast<const unsigned short*>(gr.s) + ((size_t)(m0 / BM) * KG + g0) * BM + r;
+      lhost = (gr.flags & 2) != 0;
+    } else {
+      lptr = nullptr;
+      lsp = nullptr;
+    }
+  };
+  cursor_unit(lu);
+  uint4 ring[kStages ? 1 : R][4];   // register ring (no shared-memory ring)
+  uint32_t sring[R];                // weight scales of the stages in flight
+  // shared-memory ring: this thread's 16 bytes of each quarter
+  // of slot 0; slot j, quarter c at + j * kWG * kStageBytes8 + c * 2048
+  uint8_t* const sbuf = smem + L.ring_off + wg * kStageBytes8 + r * 16;
+  constexpr uint32_t kQuarter = kChunk / 2;   // bytes between a thread's four 16-byte pieces of a stage
+  // ring slot j <- the next stage of this warpgroup's slice
+  auto load_next = [&](int j) {
+    if (lptr) {
+      const uint4* c = lptr + (size_t)lst * (2 * kChunk / 16);   // chunks 2*lst and 2*lst + 1 of the slice
+      if constexpr (kStages) {
+        uint8_t* d = sbuf + j * (kWG * kStageBytes8);
+        if (lhost) {
+#pragma unroll
+          for (int q = 0; q < 4; ++q) *reinterpret_cast<uint4*>(d + q * kQuarter) = __ldg(c + q * (kQuarter / 16));
+        } else {
+#pragma unroll
+          for (int q = 0; q < 4; ++q) cp_async_16(d + q * kQuarter, c + q * (kQuarter / 16));
+        }
+      } else {
+#pragma unroll
+        for (int q = 0; q < 4; ++q) ring[j][q] = __ldg(c + q * (kQuarter / 16));
+      }
+      sring[j] = __ldg(lsp + (size_t)lst * BM);
+    } else {
+      const uint4 z = make_uint4(0x88888888u, 0x88888888u, 0x88888888u, 0x88888888u);
+      if constexpr (kStages) {
+#pragma unroll
+        for (int q = 0; q < 4; ++q) *reinterpret_cast<uint4*>(sbuf + j * (kWG * kStageBytes8) + q * kQuarter) = z;
+      } else {
+#pragma unroll
+        for (int q = 0; q < 4; ++q) ring[j][q] = z;
+      }
+      sring[j] = 0;
+    }
+    if constexpr (kStages) cp_async_commit();
+    if (++lst == nst) {
+      lst = 0;
+      if (++lu < ue) cursor_unit(lu);
+    }
+  };
+  if (wg < p.kq) {
+#pragma unroll
+    for (int j = 0; j < R; ++j) {
+      if (j < NS) {
+        load_next(j);
+      } else if constexpr (kStages) {
+        cp_async_commit();   // one group per ring slot, loaded or not
+      }
+    }
+  }
+
+  // down: the expert_out rows of each routed group's tokens (read by the
+  // epilogues only, so after the first weights are on their way)
+  if constexpr (MODE == 1) {
+    for (int a = tid; a < n_act; a += blockDim.x) {
+      Group& dst = groups[a];
+      if (!(dst.flags & 1)) continue;
+      const bool mine = a == tid;   // always, as n_act < blockDim.x
+      const int lo = mine ? olo : __ldg(p.offsets + dst.e), hi = mine ? ohi : __ldg(p.offsets + dst.e + 1);
+      for (int q = lo; q < hi && q < lo + kTok; ++q) {
+        const int tk = __ldg(p.perm + q) / p.k;
+        if (tk >= 0 && tk < kTok) dst.outq[tk] = q;
+      }
+    }
+  }
+  // B: gate/up one buffer of the tokens, down one buffer of h per expert of the
+  // range (at most nB, by the launch).
+  if (MODE == 1 && a_last - a_first >= p.nB && tid == 0) set_status(p.status, QRE_DEV_BAD_INDEX);
+  for (int b0 = 0; warp + 16 * b0 < njobs; b0 += kJB) {
+    if (b0 > 0) {
+#pragma unroll
+      for (int b = 0; b < kJB; ++b)
+        if (warp + 16 * (b0 + b) < njobs) pre[b] = job_load(warp + 16 * (b0 + b), a_first);
+    }
+#pragma unroll
+    for (int b = 0; b < kJB; ++b)
+      if (warp + 16 * (b0 + b) < njobs)
+        e4m3_b_job<MODE, TT, BN8, NT>(warp + 16 * (b0 + b), pre[b], p.T, KG, Bs, Et, b_bytes);
+  }
+  fence_proxy_async_smem();
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+
 
   auto epilogue = [&](int v) {
-    finish_unit<MODE, TT>(v, ub, upe, groups, red, red_full, red_empty, p.kq, p.T, p.I, p.H, p.hbuf, p.expert_out,
-                          abort_flag, p.status);
+    finish_unit<MODE, TT, true>(v, ub, upe, groups, red, red_full, red_empty, p.kq, p.T, p.I, p.H, p.hbuf,
+                                p.expert_out, abort_flag, p.status);
   };
   int epi = -1;
 
   if (wg < p.kq) {
     const uint32_t tmem_wg = *tmem_base_p + wg * kColsPerWG;
     const uint32_t tlane = (uint32_t)(32 * wq) << 16;
-    const int KS = p.K / SK;                       // 64-element chunks per row block
     const uint32_t idesc = umma_idesc_e4m3(BM, BN8);
     const uint32_t bbase = smem_addr(Bs);
-
-    int lu = ub, lst = 0;
-    const uint4* lptr = nullptr;
-    const unsigned short* lsp = nullptr;
-    auto cursor_unit = [&](int u) {
-      const int a = u / upe, m0 = (u - a * upe) * BM;
-      const Group& gr = groups[a];
-      if (gr.flags & 1) {
-        lptr = reinterpret_cast<const uint4*>(gr.w + ((size_t)(m0 / BM) * KS + k0 / SK) * kChunk) + r;
-        lsp = reinterpret_cast<const unsigned short*>(gr.s) + ((size_t)(m0 / BM) * KG + g0) * BM + r;
-      } else {
-        lptr = nullptr;
-        lsp = nullptr;
-      }
-    };
-    cursor_unit(lu);
-    uint4 ring[R][4];
-    uint32_t sring[R];
-    auto load_next = [&](uint4 (&dst)[4], uint32_t& sdst) {
-      if (lptr) {
-        const uint4* c = lptr + (size_t)lst * (2 * kChunk / 16);   // chunks 2*lst and 2*lst + 1 of the slice
-        dst[0] = __ldg(c);
-        dst[1] = __ldg(c + kChunk / 32);
-        dst[2] = __ldg(c + kChunk / 16);
-        dst[3] = __ldg(c + kChunk / 16 + kChunk / 32);
-        sdst = __ldg(lsp + (size_t)lst * BM);
-      } else {
-        dst[0] = dst[1] = dst[2] = dst[3] = make_uint4(0x88888888u, 0x88888888u, 0x88888888u, 0x88888888u);
-        sdst = 0;
-      }
-      if (++lst == nst) {
-        lst = 0;
-        if (++lu < ue) cursor_unit(lu);
-      }
-    };
-#pragma unroll
-    for (int j = 0; j < R; ++j)
-      if (j < NS) load_next(ring[j], sring[j]);
 
     float acc[TT];
 #pragma unroll
@@ -852,15 +973,18 @@ __global__ void __launch_bounds__(kThreads, 1) ffn_e4m3_kernel(const FfnParams p
                      : "=r"(dv[0]), "=r"(dv[1]), "=r"(dv[2]), "=r"(dv[3])
                      : "r"(tlane + tmem_wg + kD0 + BN8 * db));
         tmem_ld_wait();
-        const float d = add_terms(dv[0], dv[1], dv[2], dv[3]);
+        const float d = add_terms<NT>(dv);
         acc[0] = fmaf(sc, fmaf(d, ec[g], -ec[KG + g]), acc[0]);
       } else {
-        uint32_t dv[32];
-        tmem_ld_32x32b_x32(tlane + tmem_wg + kD0 + BN8 * db, dv);
+        uint32_t dv[BN8];
+        if constexpr (BN8 == 32)
+          tmem_ld_32x32b_x32(tlane + tmem_wg + kD0 + BN8 * db, dv);
+        else
+          tmem_ld_32x32b_x16(tlane + tmem_wg + kD0 + BN8 * db, dv);
         tmem_ld_wait();
 #pragma unroll
         for (int n = 0; n < TT; ++n) {
-          const float d = add_terms(dv[4 * n], dv[4 * n + 1], dv[4 * n + 2], dv[4 * n + 3]);
+          const float d = add_terms<NT>(dv + NT * n);
           acc[n] = fmaf(sc, fmaf(d, ec[n * KG + g], -ec[(TT + n) * KG + g]), acc[n]);
         }
       }
@@ -900,7 +1024,7 @@ __global__ void __launch_bounds__(kThreads, 1) ffn_e4m3_kernel(const FfnParams p
     for (int gs0 = 0; gs0 < NS; gs0 += R) {
 #pragma unroll
       for (int j = 0; j < R; ++j) {
-        const int gs = gs0 + j, ab = j & 1;   // gs0 is a multiple of R = 2: buffer = gs & 1 = j & 1
+        const int gs = gs0 + j, ab = j & 1;   // gs0 is a multiple of R (even): buffer = gs & 1 = j & 1
         if (gs < NS) {
           // (1) stage gs - 2 completed: A buffer ab is free, its D readable
           if (gs >= 2) {
@@ -910,17 +1034,31 @@ __global__ void __launch_bounds__(kThreads, 1) ffn_e4m3_kernel(const FfnParams p
           }
           // (2) split 128 nibbles of this row into 128 E4M3 codes, store them in TMEM
           {
+            uint4 cur[4];
+            if constexpr (kStages) {
+              cp_async_wait_group<kStages - 1>();   // slot j's group (the oldest in flight) has landed
+#pragma unroll
+              for (int q = 0; q < 4; ++q)
+                cur[q] = *reinterpret_cast<const uint4*>(sbuf + j * (kWG * kStageBytes8) + q * kQuarter);
+            } else {
+#pragma unroll
+              for (int q = 0; q < 4; ++q) cur[q] = ring[j][q];
+            }
             uint32_t av[32];
 #pragma unroll
             for (int c = 0; c < 4; ++c) {
-              const uint32_t wd[4] = {ring[j][c].x, ring[j][c].y, ring[j][c].z, ring[j][c].w};
+              const uint32_t wd[4] = {cur[c].x, cur[c].y, cur[c].z, cur[c].w};
 #pragma unroll
               for (int w = 0; w < 4; ++w) split_nibbles_e4m3(wd[w], av[8 * c + 2 * w], av[8 * c + 2 * w + 1]);
             }
             tmem_st_32x32b_x32(tlane + tmem_wg + ab * kA8, av);
           }
           const uint32_t sp = sring[j];
-          if (gs + R < NS) load_next(ring[j], sring[j]);
+          if (gs + R < NS) {
+            load_next(j);
+          } else if constexpr (kStages) {
+            cp_async_commit();   // keeps the group count in step with the stages
+          }
           // (3) while the store drains: read back stage gs - 2
           if (gs >= 2) {
             int est = st - 2, eul = ul;
@@ -1016,8 +1154,8 @@ cudaError_t launch_tt(const FfnParams& p, int seg, int grid, int smem, cudaStrea
   return launch_k<MODE, 32, TT>(p, grid, smem, stream);
 }
 
-int smem_needed8(int K, int nB, int TT) {
-  const size_t b = make_layout8(K, nB, TT).bytes;
+int smem_needed8(int MODE, int K, int nB, int TT) {
+  const size_t b = make_layout8(MODE, K, nB, TT).bytes;
   return (int)(b > 120 * 1024 ? b : 120 * 1024);
 }
 
@@ -1039,19 +1177,30 @@ long long decode_grid(int MODE, int nB, long long units, int amax, int sms) {
   return grid;
 }
 
+// FP8 weights in tensor memory need G = 128 (whole-group stages in every K
+// slice) and the B operand in shared memory; shared-memory bytes and buffers.
+bool e4m3_plan(int MODE, int K, int G, int TT, int* nB, int* smem) {
+  const int budget = device_max_smem_optin();
+  const int kq = pick_kq(K, G);
+  if (G != SK8 || kq == 0 || (K / kq) % SK8 != 0) return false;
+  *nB = (MODE == 1 && smem_needed8(MODE, K, 2, TT) <= budget) ? 2 : 1;
+  *smem = smem_needed8(MODE, K, *nB, TT);
+  return *smem <= budget;
+}
+
+// fp8: both phases take the FP8 kernel (they share the h layout), else both
+// the fp16 one.
 template <int MODE>
-cudaError_t launch_mode(const FfnParams& base, long long units, cudaStream_t stream) {
+cudaError_t launch_mode(const FfnParams& base, long long units, bool fp8, cudaStream_t stream) {
   FfnParams p = base;
   const int sms = device_sm_count();
   const int budget = device_max_smem_optin();
   const int TT = p.T == 1 ? 1 : kTok;
   p.lgG = ilog2(p.G);
-  if (p.G == SK8) {
-    // FP8 weights in tensor memory: whole-group stages in every K slice
-    p.kq = pick_kq(p.K, p.G);
-    p.nB = (MODE == 1 && smem_needed8(p.K, 2, TT) <= budget) ? 2 : 1;
-    const int smem = smem_needed8(p.K, p.nB, TT);
-    if (p.kq > 0 && (p.K / p.kq) % SK8 == 0 && smem <= budget) {
+  if (fp8) {
+    int smem = 0;
+    if (e4m3_plan(MODE, p.K, p.G, TT, &p.nB, &smem)) {
+      p.kq = pick_kq(p.K, p.G);
       const int grid = (int)decode_grid(MODE, p.nB, units, p.amax, sms);
       if (TT == 1) return launch_e4m3<MODE, 1>(p, grid, smem, stream);
       return launch_e4m3<MODE, kTok>(p, grid, smem, stream);
@@ -1107,12 +1256,15 @@ cudaError_t launch_ffn_decode(const qre_layer_shape& s, int T, const uint16_t* x
   p.amax = (int)(pk < s.n_experts ? pk : s.n_experts);
   p.K = s.hidden;
   p.n_out = 2 * s.inter;
-  cudaError_t err = launch_mode<0>(p, (long long)(p.amax + 1) * (p.n_out / BM), stream);
+  const int TT = T == 1 ? 1 : kTok;
+  int nb = 0, sm = 0;
+  const bool fp8 = e4m3_plan(0, s.hidden, s.group, TT, &nb, &sm) && e4m3_plan(1, s.inter, s.group, TT, &nb, &sm);
+  cudaError_t err = launch_mode<0>(p, (long long)(p.amax + 1) * (p.n_out / BM), fp8, stream);
   if (err != cudaSuccess) return err;
 
   p.K = s.inter;
   p.n_out = s.hidden;
-  return launch_mode<1>(p, (long long)(p.amax + 1) * (p.n_out / BM), stream);
+  return launch_mode<1>(p, (long long)(p.amax + 1) * (p.n_out / BM), fp8, stream);
 }
 
 }  // namespace qre

@@ -9,6 +9,11 @@ namespace {
 // (ascending expert id), the shared term last.  Summing the expert partials in
 // fp32 after the experts follows the glm53-flash-offload README ("CPU tier"
 // bullet).  y_bf16 (optional) is round-to-nearest-even of y.
+// KMAX > 0: top_k <= KMAX, and every weight, row index and expert row of the
+// thread is loaded before the first sum (one round of memory latency instead
+// of k dependent ones); KMAX == 0: any top_k, one pick at a time.  Same sums,
+// same order, same bits either way.
+template <int KMAX>
 __global__ void __launch_bounds__(256) combine_kernel(int T, int H, int k, const float* __restrict__ eo,
                                                       const float* __restrict__ w, const int32_t* __restrict__ inv_perm,
                                                       float* __restrict__ y, uint16_t* __restrict__ ybf) {
@@ -16,16 +21,36 @@ __global__ void __launch_bounds__(256) combine_kernel(int T, int H, int k, const
   const int h = (blockIdx.x * blockDim.x + threadIdx.x) * 4;
   if (t >= T || h >= H) return;
   float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-  for (int j = 0; j < k; ++j) {
-    const float wj = __ldg(w + (size_t)t * k + j);
-    const int q = __ldg(inv_perm + (size_t)t * k + j);
-    const float4 v = __ldg(reinterpret_cast<const float4*>(eo + (size_t)q * H + h));
+  auto add = [&](float wj, const float4 v) {
     acc.x = fmaf(wj, v.x, acc.x);
     acc.y = fmaf(wj, v.y, acc.y);
     acc.z = fmaf(wj, v.z, acc.z);
     acc.w = fmaf(wj, v.w, acc.w);
-  }
+  };
   const float4 sh = __ldg(reinterpret_cast<const float4*>(eo + ((size_t)T * k + t) * H + h));
+  if constexpr (KMAX > 0) {
+    float wj[KMAX];
+    int qj[KMAX];
+#pragma unroll
+    for (int j = 0; j < KMAX; ++j)
+      if (j < k) {
+        wj[j] = __ldg(w + (size_t)t * k + j);
+        qj[j] = __ldg(inv_perm + (size_t)t * k + j);
+      }
+    float4 v[KMAX];
+#pragma unroll
+    for (int j = 0; j < KMAX; ++j)
+      if (j < k) v[j] = __ldg(reinterpret_cast<const float4*>(eo + (size_t)qj[j] * H + h));
+#pragma unroll
+    for (int j = 0; j < KMAX; ++j)
+      if (j < k) add(wj[j], v[j]);
+  } else {
+    for (int j = 0; j < k; ++j) {
+      const float wj = __ldg(w + (size_t)t * k + j);
+      const int q = __ldg(inv_perm + (size_t)t * k + j);
+      add(wj, __ldg(reinterpret_cast<const float4*>(eo + (size_t)q * H + h)));
+    }
+  }
   acc.x += sh.x;
   acc.y += sh.y;
   acc.z += sh.z;
@@ -123,7 +148,12 @@ cudaError_t launch_combine(const qre_layer_shape& s, int T, const float* expert_
   const int H = s.hidden;
   const int threads = T <= 8 ? 64 : 256;   // small batches: spread over more SMs
   dim3 grid((H / 4 + threads - 1) / threads, T);
-  combine_kernel<<<grid, threads, 0, stream>>>(T, H, s.top_k, expert_out, topk_w, inv_perm, y_f32, y_bf16);
+  if (s.top_k <= 8)
+    combine_kernel<8><<<grid, threads, 0, stream>>>(T, H, s.top_k, expert_out, topk_w, inv_perm, y_f32, y_bf16);
+  else if (s.top_k <= 16)
+    combine_kernel<16><<<grid, threads, 0, stream>>>(T, H, s.top_k, expert_out, topk_w, inv_perm, y_f32, y_bf16);
+  else
+    combine_kernel<0><<<grid, threads, 0, stream>>>(T, H, s.top_k, expert_out, topk_w, inv_perm, y_f32, y_bf16);
   return cudaGetLastError();
 }
 

@@ -15,39 +15,12 @@
 //     expert), then placement per chunk from the chunk's base offsets.
 #include "common.cuh"
 #include "internal.h"
+#include "routing.cuh"
 
 namespace qre {
 namespace {
 
 constexpr int kChunk = 1024;
-
-// Block-wide exclusive scan of one value per thread (blockDim.x <= 1024).
-__device__ int block_exclusive_scan(int v, int* warp_tot, int* total) {
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = (blockDim.x + 31) >> 5;
-  int inc = v;
-#pragma unroll
-  for (int o = 1; o < 32; o <<= 1) {
-    const int y = __shfl_up_sync(0xffffffffu, inc, o);
-    if (lane >= o) inc += y;
-  }
-  if (lane == 31) warp_tot[warp] = inc;
-  __syncthreads();
-  if (warp == 0) {
-    int w = lane < nw ? warp_tot[lane] : 0;
-    int wi = w;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const int y = __shfl_up_sync(0xffffffffu, wi, o);
-      if (lane >= o) wi += y;
-    }
-    if (lane < nw) warp_tot[lane] = wi - w;
-    if (lane == nw - 1) *total = wi;
-  }
-  __syncthreads();
-  const int r = warp_tot[warp] + inc - v;
-  __syncthreads();
-  return r;
-}
 
 __device__ __forceinline__ int load_pick(const int32_t* idx, int p, int E, int* status) {
   const int e = idx[p];
@@ -56,20 +29,6 @@ __device__ __forceinline__ int load_pick(const int32_t* idx, int p, int E, int* 
     return -1;
   }
   return e;
-}
-
-// Places the picks of one chunk: thread e walks the chunk in pick order.
-__device__ void place_chunk(const int* s_idx, int p0, int n, int E, int base_e, int32_t* perm, int32_t* inv_perm) {
-  const int e = threadIdx.x;
-  if (e >= E) return;
-  int pos = base_e;
-  for (int i = 0; i < n; ++i) {
-    if (s_idx[i] == e) {
-      perm[pos] = p0 + i;
-      inv_perm[p0 + i] = pos;
-      ++pos;
-    }
-  }
 }
 
 // Single CTA: the whole pick list is one chunk.  blockDim.x = max(E, 32) rounded up to a warp.
@@ -81,27 +40,9 @@ __global__ void __launch_bounds__(1024) dispatch_single(int P, int E, const int3
   __shared__ int s_cnt[1024];
   __shared__ int warp_tot[32];
   __shared__ int total;
-  for (int e = threadIdx.x; e < E; e += blockDim.x) s_cnt[e] = 0;
+  for (int p = threadIdx.x; p < P; p += blockDim.x) s_idx[p] = load_pick(idx, p, E, status);
   __syncthreads();
-  for (int p = threadIdx.x; p < P; p += blockDim.x) {
-    const int e = load_pick(idx, p, E, status);
-    s_idx[p] = e;
-    if (e >= 0) atomicAdd(&s_cnt[e], 1);
-  }
-  __syncthreads();
-  const int e = threadIdx.x;
-  const int c = e < E ? s_cnt[e] : 0;
-  const int off = block_exclusive_scan(c, warp_tot, &total);
-  const int flag = c > 0 ? 1 : 0;
-  const int apos = block_exclusive_scan(flag, warp_tot, &total);
-  if (e < E) {
-    counts[e] = c;
-    offsets[e] = off;
-    if (flag) active[apos] = e;
-  }
-  if (threadIdx.x == 0) n_active[0] = total;
-  if (e == E - 1) offsets[E] = off + c;
-  place_chunk(s_idx, 0, P, E, off, perm, inv_perm);
+  dispatch_block(P, E, s_idx, counts, offsets, perm, inv_perm, active, n_active, s_cnt, warp_tot, &total);
 }
 
 // Multi-chunk, step 1: per-chunk counts -> ccount[chunk][E].

@@ -15,6 +15,7 @@
 // give the same bits (same fp32 scores, same exact order, same summation).
 #include "common.cuh"
 #include "internal.h"
+#include "routing.cuh"
 
 namespace qre {
 namespace {
@@ -25,56 +26,7 @@ template <int TMAX>
 __global__ void __launch_bounds__(256) route_logits_gemv(int T, int H, int E, const uint16_t* __restrict__ x,
                                                          const float* __restrict__ W, float* __restrict__ logits) {
   __shared__ float part[2][4][TMAX];
-  const int row = threadIdx.x >> 7;        // expert row within the CTA
-  const int c = threadIdx.x & 127;         // column slot
-  const int warp_in_row = (threadIdx.x >> 5) & 3, lane = threadIdx.x & 31;
-  const int e = blockIdx.x * 2 + row;
-  float acc[TMAX];
-#pragma unroll
-  for (int t = 0; t < TMAX; ++t) acc[t] = 0.f;
-  if (e < E) {
-    const float* w = W + (size_t)e * H;
-    float4 wbuf[8];
-#pragma unroll
-    for (int m = 0; m < 8; ++m) {   // all of this thread's weights in flight at once
-      const int j = c * 4 + m * 512;
-      wbuf[m] = j < H ? __ldg(reinterpret_cast<const float4*>(w + j)) : make_float4(0.f, 0.f, 0.f, 0.f);
-    }
-#pragma unroll
-    for (int m = 0; m < 8; ++m) {
-      const int j = c * 4 + m * 512;
-      if (j >= H) break;
-      const float4 wv = wbuf[m];
-#pragma unroll
-      for (int t = 0; t < TMAX; ++t) {
-        if (t < T) {
-          const uint2 xv = __ldg(reinterpret_cast<const uint2*>(x + (size_t)t * H + j));
-          float a = acc[t];
-          a = fmaf(bf16_bits_to_float(xv.x & 0xFFFFu), wv.x, a);
-          a = fmaf(bf16_bits_to_float(xv.x >> 16), wv.y, a);
-          a = fmaf(bf16_bits_to_float(xv.y & 0xFFFFu), wv.z, a);
-          a = fmaf(bf16_bits_to_float(xv.y >> 16), wv.w, a);
-          acc[t] = a;
-        }
-      }
-    }
-  }
-#pragma unroll
-  for (int t = 0; t < TMAX; ++t) {
-    float v = acc[t];
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-    if (lane == 0) part[row][warp_in_row][t] = v;
-  }
-  __syncthreads();
-  if (threadIdx.x < 2 * TMAX) {
-    const int r = threadIdx.x / TMAX, t = threadIdx.x % TMAX;
-    const int ee = blockIdx.x * 2 + r;
-    if (ee < E && t < T) {
-      const float v = ((part[r][0][t] + part[r][1][t]) + part[r][2][t]) + part[r][3][t];
-      logits[(size_t)t * E + ee] = v;
-    }
-  }
+  logits_gemv_pair<TMAX>(blockIdx.x * 2, T, H, E, x, W, logits, part);
 }
 
 // logits[T][E] = X[T][H] (bf16) * W[E][H]^T (fp32), fp32 CUDA-core GEMM.
@@ -138,97 +90,20 @@ __global__ void __launch_bounds__(256) route_logits_gemm(int T, int H, int E, co
   }
 }
 
-struct Cand {
-  float v;
-  int id;
-};
-__device__ __forceinline__ bool better(const Cand& a, const Cand& b) {
-  return a.v > b.v || (a.v == b.v && a.id < b.id);
-}
-
-// One warp per token: sigmoid, selection score, k rounds of warp arg-max (ties
-// to the lower id), ascending-id output, weights s / sum(s) summed in ascending
-// id order.
+// One warp per token (select_token_warp).
 constexpr int kSelWarps = 8;
 __global__ void __launch_bounds__(kSelWarps * 32) route_select(int T, int E, int k, const float* __restrict__ logits,
                                                                const float* __restrict__ bias, int32_t* __restrict__ idx,
                                                                float* __restrict__ wout) {
   __shared__ int sid[kSelWarps][16];
   __shared__ float ssc[kSelWarps][16];
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int warp = threadIdx.x >> 5;
   const int t = blockIdx.x * kSelWarps + warp;
   if (t >= T) return;
-  const float* lg = logits + (size_t)t * E;
-  float s[32], sel[32];
-  uint32_t taken = 0;
-#pragma unroll
-  for (int i = 0; i < 32; ++i) {
-    const int e = i * 32 + lane;
-    if (e < E) {
-      const float sc = 1.0f / (1.0f + expf(-lg[e]));
-      s[i] = sc;
-      sel[i] = bias ? sc + bias[e] : sc;
-    } else {
-      s[i] = 0.f;
-      sel[i] = -INFINITY;
-      taken |= 1u << i;
-    }
-  }
-  int my_id = -1;
-  float my_s = 0.f;
-  for (int r = 0; r < k; ++r) {
-    Cand best{-INFINITY, 0x7fffffff};
-    int best_i = -1;
-#pragma unroll
-    for (int i = 0; i < 32; ++i) {
-      if (!(taken >> i & 1u)) {
-        const Cand c{sel[i], i * 32 + lane};
-        if (best_i < 0 || better(c, best)) {
-          best = c;
-          best_i = i;
-        }
-      }
-    }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-      Cand other{__shfl_xor_sync(0xffffffffu, best.v, o), __shfl_xor_sync(0xffffffffu, best.id, o)};
-      if (better(other, best)) best = other;
-    }
-    const int owner = best.id & 31, slot = best.id >> 5;
-    float sw = 0.f;
-    if (lane == owner) {
-#pragma unroll
-      for (int i = 0; i < 32; ++i)
-        if (i == slot) {
-          taken |= 1u << i;
-          sw = s[i];
-        }
-    }
-    sw = __shfl_sync(0xffffffffu, sw, owner);
-    if (lane == r) {
-      my_id = best.id;
-      my_s = sw;
-    }
-  }
-  // rank = number of picks with a smaller id
-  int rank = 0;
-  for (int j = 0; j < k; ++j) {
-    const int other = __shfl_sync(0xffffffffu, my_id, j);
-    if (lane < k && other < my_id) ++rank;
-  }
-  if (lane < k) {
-    sid[warp][rank] = my_id;
-    ssc[warp][rank] = my_s;
-  }
-  __syncwarp();
-  if (lane == 0) {
-    float tot = 0.f;
-    for (int j = 0; j < k; ++j) tot += ssc[warp][j];
-    for (int j = 0; j < k; ++j) {
-      idx[(size_t)t * k + j] = sid[warp][j];
-      wout[(size_t)t * k + j] = ssc[warp][j] / tot;
-    }
-  }
+  if (E <= 320)
+    select_token_warp<10>(t, E, k, logits + (size_t)t * E, bias, idx, wout, sid[warp], ssc[warp], nullptr);
+  else
+    select_token_warp<32>(t, E, k, logits + (size_t)t * E, bias, idx, wout, sid[warp], ssc[warp], nullptr);
 }
 
 // One CTA per token (small T): every expert computes its rank in the order

@@ -208,6 +208,8 @@ __device__ __noinline__ void finish_unit(int v, int ub, int upe, const Group* gr
 // are the ones read back.
 template <int MODE, int SEG, int TT>
 __global__ void __launch_bounds__(kThreads, 1) ffn_decode_kernel(const FfnParams p) {
+  if constexpr (MODE == 1) grid_dependency_wait();   // h of the gate/up grid
+  if constexpr (MODE == 0) grid_dependents_launch();
   constexpr int R = 4;                    // register ring depth = unroll
   constexpr int NA = SEG == 128 ? 3 : 2;  // A buffers per warpgroup
   constexpr int ND = SEG == 128 ? 2 : 4;  // D buffers per warpgroup
@@ -744,6 +746,9 @@ __global__ void __launch_bounds__(kThreads, 1) ffn_e4m3_kernel(const FfnParams p
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int KG = p.K / SK8;
+  // gate/up: the down kernel (launched as its programmatic dependent) may take
+  // each SM this CTA leaves; it waits for this grid before it reads h
+  if constexpr (MODE == 0) grid_dependents_launch();
   // B operand jobs: (buffer jb, token n, group g), one warp each, lane l
   // holding physical positions 4l .. 4l + 3 of the group (reduction indices
   // 8(l >> 1) + (l & 1) + 2i).  A warp's first kJB jobs have their loads in
@@ -783,11 +788,6 @@ __global__ void __launch_bounds__(kThreads, 1) ffn_e4m3_kernel(const FfnParams p
   const int a_first = ub / upe, a_last = (ue - 1) / upe;
   const int nbuf = MODE == 0 ? 1 : (a_last - a_first + 1 < p.nB ? a_last - a_first + 1 : p.nB);
   const int njobs = nbuf * p.T * KG;
-  if constexpr (MODE == 1) {
-#pragma unroll
-    for (int b = 0; b < kJB; ++b)
-      if (warp + 16 * b < njobs) pre[b] = job_load(warp + 16 * b, a_first);
-  }
 
   int olo = 0, ohi = 0;   // down: the dispatch range of this thread's group (tid < n_act)
   for (int a = tid; a < ngroups; a += blockDim.x) {
@@ -926,6 +926,14 @@ __global__ void __launch_bounds__(kThreads, 1) ffn_e4m3_kernel(const FfnParams p
         if (tk >= 0 && tk < kTok) dst.outq[tk] = q;
       }
     }
+  }
+  // down: everything above (group table, first weight stages) overlaps the end
+  // of the gate/up grid; h is read only once that grid has completed
+  if constexpr (MODE == 1) {
+    grid_dependency_wait();
+#pragma unroll
+    for (int b = 0; b < kJB; ++b)
+      if (warp + 16 * b < njobs) pre[b] = job_load(warp + 16 * b, a_first);
   }
   // B: gate/up one buffer of the tokens, down one buffer of h per expert of the
   // range (at most nB, by the launch).
@@ -1139,12 +1147,31 @@ int smem_needed(int K, int nB, int TT) {
   return (int)(b > 120 * 1024 ? b : 120 * 1024);
 }
 
+// The down kernel is launched as a programmatic dependent of the gate/up
+// kernel: its CTAs start on the SMs the gate/up CTAs leave, and it waits for
+// the gate/up grid (griddepcontrol.wait) before reading h.
+template <typename Kernel>
+cudaError_t launch_decode(Kernel kernel, bool dependent, const FfnParams& p, int grid, int smem,
+                          cudaStream_t stream) {
+  cudaError_t err = ensure_smem_limit(reinterpret_cast<const void*>(kernel), smem);
+  if (err != cudaSuccess) return err;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = dependent ? 1 : 0;
+  err = cudaLaunchKernelEx(&cfg, kernel, p);
+  return err != cudaSuccess ? err : cudaGetLastError();
+}
+
 template <int MODE, int SEG, int TT>
 cudaError_t launch_k(const FfnParams& p, int grid, int smem, cudaStream_t stream) {
-  cudaError_t err = ensure_smem_limit(reinterpret_cast<const void*>(ffn_decode_kernel<MODE, SEG, TT>), smem);
-  if (err != cudaSuccess) return err;
-  ffn_decode_kernel<MODE, SEG, TT><<<grid, kThreads, smem, stream>>>(p);
-  return cudaGetLastError();
+  return launch_decode(ffn_decode_kernel<MODE, SEG, TT>, MODE == 1, p, grid, smem, stream);
 }
 
 template <int MODE, int TT>
@@ -1161,10 +1188,7 @@ int smem_needed8(int MODE, int K, int nB, int TT) {
 
 template <int MODE, int TT>
 cudaError_t launch_e4m3(const FfnParams& p, int grid, int smem, cudaStream_t stream) {
-  cudaError_t err = ensure_smem_limit(reinterpret_cast<const void*>(ffn_e4m3_kernel<MODE, TT>), smem);
-  if (err != cudaSuccess) return err;
-  ffn_e4m3_kernel<MODE, TT><<<grid, kThreads, smem, stream>>>(p);
-  return cudaGetLastError();
+  return launch_decode(ffn_e4m3_kernel<MODE, TT>, MODE == 1, p, grid, smem, stream);
 }
 
 // One CTA per SM.  The down kernels hold the B operand (h) of every expert of

@@ -17,6 +17,8 @@ template <int KMAX>
 __global__ void __launch_bounds__(256) combine_kernel(int T, int H, int k, const float* __restrict__ eo,
                                                       const float* __restrict__ w, const int32_t* __restrict__ inv_perm,
                                                       float* __restrict__ y, uint16_t* __restrict__ ybf) {
+  grid_dependency_wait();
+  grid_dependents_launch();
   const int t = blockIdx.y;
   const int h = (blockIdx.x * blockDim.x + threadIdx.x) * 4;
   if (t >= T || h >= H) return;
@@ -148,13 +150,9 @@ cudaError_t launch_combine(const qre_layer_shape& s, int T, const float* expert_
   const int H = s.hidden;
   const int threads = T <= 8 ? 64 : 256;   // small batches: spread over more SMs
   dim3 grid((H / 4 + threads - 1) / threads, T);
-  if (s.top_k <= 8)
-    combine_kernel<8><<<grid, threads, 0, stream>>>(T, H, s.top_k, expert_out, topk_w, inv_perm, y_f32, y_bf16);
-  else if (s.top_k <= 16)
-    combine_kernel<16><<<grid, threads, 0, stream>>>(T, H, s.top_k, expert_out, topk_w, inv_perm, y_f32, y_bf16);
-  else
-    combine_kernel<0><<<grid, threads, 0, stream>>>(T, H, s.top_k, expert_out, topk_w, inv_perm, y_f32, y_bf16);
-  return cudaGetLastError();
+  auto kernel = s.top_k <= 8 ? combine_kernel<8> : (s.top_k <= 16 ? combine_kernel<16> : combine_kernel<0>);
+  return launch_dependent(kernel, grid, dim3(threads), 0, stream, T, H, s.top_k, expert_out, topk_w, inv_perm, y_f32,
+                          y_bf16);
 }
 
 cudaError_t launch_quantize(int n_rows, int k_dim, int group, const float* w, const float* w2, uint8_t* packed,

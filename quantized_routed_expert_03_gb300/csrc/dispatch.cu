@@ -36,6 +36,8 @@ __global__ void __launch_bounds__(1024) dispatch_single(int P, int E, const int3
                                                          int32_t* counts, int32_t* offsets, int32_t* perm,
                                                          int32_t* inv_perm, int32_t* active, int32_t* n_active,
                                                          int* status) {
+  grid_dependency_wait();
+  grid_dependents_launch();
   __shared__ int s_idx[kChunk];
   __shared__ int s_cnt[1024];
   __shared__ int warp_tot[32];
@@ -48,6 +50,8 @@ __global__ void __launch_bounds__(1024) dispatch_single(int P, int E, const int3
 // Multi-chunk, step 1: per-chunk counts -> ccount[chunk][E].
 __global__ void __launch_bounds__(1024) dispatch_count(int P, int E, const int32_t* __restrict__ idx, int* ccount,
                                                         int* status) {
+  grid_dependency_wait();
+  grid_dependents_launch();
   __shared__ int s_cnt[1024];
   for (int e = threadIdx.x; e < E; e += blockDim.x) s_cnt[e] = 0;
   __syncthreads();
@@ -65,6 +69,8 @@ __global__ void __launch_bounds__(1024) dispatch_count(int P, int E, const int32
 // each chunk's base position per expert.
 __global__ void __launch_bounds__(1024) dispatch_scan(int nchunk, int E, int* ccount, int32_t* counts,
                                                        int32_t* offsets, int32_t* active, int32_t* n_active) {
+  grid_dependency_wait();
+  grid_dependents_launch();
   __shared__ int warp_tot[32];
   __shared__ int total;
   const int e = threadIdx.x;
@@ -91,6 +97,8 @@ __global__ void __launch_bounds__(1024) dispatch_scan(int nchunk, int E, int* cc
 // Multi-chunk, step 3: placement per chunk.
 __global__ void __launch_bounds__(1024) dispatch_place(int P, int E, const int32_t* __restrict__ idx,
                                                         const int* ccount, int32_t* perm, int32_t* inv_perm) {
+  grid_dependency_wait();
+  grid_dependents_launch();
   __shared__ int s_idx[kChunk];
   const int p0 = blockIdx.x * kChunk;
   const int n = min(kChunk, P - p0);
@@ -118,16 +126,18 @@ cudaError_t launch_dispatch(const qre_layer_shape& s, int T, const int32_t* topk
   const int P = T * s.top_k, E = s.n_experts;
   const int threads = ((E + 31) / 32) * 32;
   if (P <= kChunk) {
-    dispatch_single<<<1, threads, 0, stream>>>(P, E, topk_idx, counts, offsets, perm, inv_perm, active, n_active,
-                                               status);
-    return cudaGetLastError();
+    return launch_dependent(dispatch_single, dim3(1), dim3(threads), 0, stream, P, E, topk_idx, counts, offsets, perm,
+                            inv_perm, active, n_active, status);
   }
   const int nchunk = (P + kChunk - 1) / kChunk;
   int* ccount = static_cast<int*>(ws);
-  dispatch_count<<<nchunk, 1024, 0, stream>>>(P, E, topk_idx, ccount, status);
-  dispatch_scan<<<1, threads, 0, stream>>>(nchunk, E, ccount, counts, offsets, active, n_active);
-  dispatch_place<<<nchunk, threads, 0, stream>>>(P, E, topk_idx, ccount, perm, inv_perm);
-  return cudaGetLastError();
+  cudaError_t err = launch_dependent(dispatch_count, dim3(nchunk), dim3(1024), 0, stream, P, E, topk_idx, ccount, status);
+  if (err != cudaSuccess) return err;
+  err = launch_dependent(dispatch_scan, dim3(1), dim3(threads), 0, stream, nchunk, E, ccount, counts, offsets, active,
+                         n_active);
+  if (err != cudaSuccess) return err;
+  return launch_dependent(dispatch_place, dim3(nchunk), dim3(threads), 0, stream, P, E, topk_idx, ccount, perm,
+                          inv_perm);
 }
 
 }  // namespace qre

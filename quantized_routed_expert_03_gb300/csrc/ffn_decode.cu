@@ -208,8 +208,8 @@ __device__ __noinline__ void finish_unit(int v, int ub, int upe, const Group* gr
 // are the ones read back.
 template <int MODE, int SEG, int TT>
 __global__ void __launch_bounds__(kThreads, 1) ffn_decode_kernel(const FfnParams p) {
-  if constexpr (MODE == 1) grid_dependency_wait();   // h of the gate/up grid
-  if constexpr (MODE == 0) grid_dependents_launch();
+  grid_dependency_wait();   // everything the kernels before it wrote (down: h of the gate/up grid)
+  grid_dependents_launch();
   constexpr int R = 4;                    // register ring depth = unroll
   constexpr int NA = SEG == 128 ? 3 : 2;  // A buffers per warpgroup
   constexpr int ND = SEG == 128 ? 2 : 4;  // D buffers per warpgroup
@@ -746,9 +746,15 @@ __global__ void __launch_bounds__(kThreads, 1) ffn_e4m3_kernel(const FfnParams p
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int KG = p.K / SK8;
-  // gate/up: the down kernel (launched as its programmatic dependent) may take
-  // each SM this CTA leaves; it waits for this grid before it reads h
-  if constexpr (MODE == 0) grid_dependents_launch();
+  // Both kernels are programmatic dependents (launch_dependent).  gate/up
+  // waits for the dispatch before anything else and then lets the down kernel
+  // be scheduled: down CTAs take the SMs that gate/up CTAs leave, build their
+  // group table and fill their weight ring (dispatch outputs and weights, all
+  // complete by then), and wait for the gate/up grid only before reading h.
+  if constexpr (MODE == 0) {
+    grid_dependency_wait();
+    grid_dependents_launch();
+  }
   // B operand jobs: (buffer jb, token n, group g), one warp each, lane l
   // holding physical positions 4l .. 4l + 3 of the group (reduction indices
   // 8(l >> 1) + (l & 1) + 2i).  A warp's first kJB jobs have their loads in
@@ -931,6 +937,7 @@ __global__ void __launch_bounds__(kThreads, 1) ffn_e4m3_kernel(const FfnParams p
   // of the gate/up grid; h is read only once that grid has completed
   if constexpr (MODE == 1) {
     grid_dependency_wait();
+    grid_dependents_launch();
 #pragma unroll
     for (int b = 0; b < kJB; ++b)
       if (warp + 16 * b < njobs) pre[b] = job_load(warp + 16 * b, a_first);
@@ -1147,31 +1154,11 @@ int smem_needed(int K, int nB, int TT) {
   return (int)(b > 120 * 1024 ? b : 120 * 1024);
 }
 
-// The down kernel is launched as a programmatic dependent of the gate/up
-// kernel: its CTAs start on the SMs the gate/up CTAs leave, and it waits for
-// the gate/up grid (griddepcontrol.wait) before reading h.
-template <typename Kernel>
-cudaError_t launch_decode(Kernel kernel, bool dependent, const FfnParams& p, int grid, int smem,
-                          cudaStream_t stream) {
-  cudaError_t err = ensure_smem_limit(reinterpret_cast<const void*>(kernel), smem);
-  if (err != cudaSuccess) return err;
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(grid);
-  cfg.blockDim = dim3(kThreads);
-  cfg.dynamicSmemBytes = smem;
-  cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = dependent ? 1 : 0;
-  err = cudaLaunchKernelEx(&cfg, kernel, p);
-  return err != cudaSuccess ? err : cudaGetLastError();
-}
-
 template <int MODE, int SEG, int TT>
 cudaError_t launch_k(const FfnParams& p, int grid, int smem, cudaStream_t stream) {
-  return launch_decode(ffn_decode_kernel<MODE, SEG, TT>, MODE == 1, p, grid, smem, stream);
+  const cudaError_t err = ensure_smem_limit(reinterpret_cast<const void*>(ffn_decode_kernel<MODE, SEG, TT>), smem);
+  if (err != cudaSuccess) return err;
+  return launch_dependent(ffn_decode_kernel<MODE, SEG, TT>, dim3(grid), dim3(kThreads), smem, stream, p);
 }
 
 template <int MODE, int TT>
@@ -1188,7 +1175,9 @@ int smem_needed8(int MODE, int K, int nB, int TT) {
 
 template <int MODE, int TT>
 cudaError_t launch_e4m3(const FfnParams& p, int grid, int smem, cudaStream_t stream) {
-  return launch_decode(ffn_e4m3_kernel<MODE, TT>, MODE == 1, p, grid, smem, stream);
+  const cudaError_t err = ensure_smem_limit(reinterpret_cast<const void*>(ffn_e4m3_kernel<MODE, TT>), smem);
+  if (err != cudaSuccess) return err;
+  return launch_dependent(ffn_e4m3_kernel<MODE, TT>, dim3(grid), dim3(kThreads), smem, stream, p);
 }
 
 // One CTA per SM.  The down kernels hold the B operand (h) of every expert of

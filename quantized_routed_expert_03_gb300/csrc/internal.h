@@ -31,6 +31,29 @@ int* device_status_word();   // address of the current device's status word
 // current device (cached, so repeated launches and graph captures skip it).
 cudaError_t ensure_smem_limit(const void* kernel, int bytes);
 
+// Launches `kernel` as a programmatic dependent of the kernel before it in the
+// stream (it may be scheduled while that kernel finishes).  Every kernel so
+// launched executes griddepcontrol.wait before it reads or writes global
+// memory that an earlier kernel touches, and lets its own dependent start
+// (griddepcontrol.launch_dependents) only after that wait, so a dependent's
+// early part never overlaps anything but its direct predecessor.
+template <typename... Params, typename... Args>
+cudaError_t launch_dependent(void (*kernel)(Params...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
+                             Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  const cudaError_t err = cudaLaunchKernelEx(&cfg, kernel, static_cast<Params>(args)...);
+  return err != cudaSuccess ? err : cudaGetLastError();
+}
+
 // Kernel launchers (return the launch error, cudaSuccess otherwise).
 // w2 == nullptr: plain matrix of n_rows rows.  Otherwise the gate/up pair:
 // n_rows = 2I output rows interleaved in blocks of 16 from w (gate) and w2 (up).

@@ -26,6 +26,8 @@ template <int TMAX>
 __global__ void __launch_bounds__(256) route_logits_gemv(int T, int H, int E, const uint16_t* __restrict__ x,
                                                          const float* __restrict__ W, float* __restrict__ logits) {
   __shared__ float part[2][4][TMAX];
+  grid_dependency_wait();
+  grid_dependents_launch();
   logits_gemv_pair<TMAX>(blockIdx.x * 2, T, H, E, x, W, logits, part);
 }
 
@@ -35,6 +37,8 @@ __global__ void __launch_bounds__(256) route_logits_gemm(int T, int H, int E, co
                                                          const float* __restrict__ W, float* __restrict__ logits) {
   __shared__ float xs[BK][BM + 4];
   __shared__ float ws[BK][BN + 4];
+  grid_dependency_wait();
+  grid_dependents_launch();
   const int tm = blockIdx.y * BM, en = blockIdx.x * BN;
   const int tx = threadIdx.x & 15, ty = threadIdx.x >> 4;   // 16 x 16 threads, 4 x 4 outputs each
   float acc[4][4] = {};
@@ -97,6 +101,8 @@ __global__ void __launch_bounds__(kSelWarps * 32) route_select(int T, int E, int
                                                                float* __restrict__ wout) {
   __shared__ int sid[kSelWarps][16];
   __shared__ float ssc[kSelWarps][16];
+  grid_dependency_wait();
+  grid_dependents_launch();
   const int warp = threadIdx.x >> 5;
   const int t = blockIdx.x * kSelWarps + warp;
   if (t >= T) return;
@@ -116,6 +122,8 @@ __global__ void __launch_bounds__(1024) route_select_rank(int T, int E, int k, c
   __shared__ int wcount[32];
   __shared__ int chosen[16];
   __shared__ float chosen_s[16];
+  grid_dependency_wait();
+  grid_dependents_launch();
   const int t = blockIdx.x, e = threadIdx.x, lane = e & 31, warp = e >> 5;
   float sc = 0.f, my = -INFINITY;
   if (e < E) {
@@ -162,23 +170,23 @@ cudaError_t launch_route(const qre_layer_shape& s, int T, const uint16_t* x, con
                          const float* bias, int32_t* topk_idx, float* topk_w, void* ws, cudaStream_t stream) {
   float* logits = static_cast<float*>(ws);
   const int H = s.hidden, E = s.n_experts;
+  cudaError_t err;
   if (T <= 8) {
-    route_logits_gemv<8><<<(E + 1) / 2, 256, 0, stream>>>(T, H, E, x, w_router, logits);
+    err = launch_dependent(route_logits_gemv<8>, dim3((E + 1) / 2), dim3(256), 0, stream, T, H, E, x, w_router,
+                           logits);
   } else if (T <= kGemvTMax) {
-    route_logits_gemv<kGemvTMax><<<(E + 1) / 2, 256, 0, stream>>>(T, H, E, x, w_router, logits);
+    err = launch_dependent(route_logits_gemv<kGemvTMax>, dim3((E + 1) / 2), dim3(256), 0, stream, T, H, E, x,
+                           w_router, logits);
   } else {
     dim3 grid((E + BN - 1) / BN, (T + BM - 1) / BM);
-    route_logits_gemm<<<grid, 256, 0, stream>>>(T, H, E, x, w_router, logits);
+    err = launch_dependent(route_logits_gemm, grid, dim3(256), 0, stream, T, H, E, x, w_router, logits);
   }
-  cudaError_t err = cudaGetLastError();
   if (err != cudaSuccess) return err;
-  if (T <= 64) {
-    route_select_rank<<<T, ((E + 31) / 32) * 32, 0, stream>>>(T, E, s.top_k, logits, bias, topk_idx, topk_w);
-  } else {
-    route_select<<<(T + kSelWarps - 1) / kSelWarps, kSelWarps * 32, 0, stream>>>(T, E, s.top_k, logits, bias,
-                                                                                topk_idx, topk_w);
-  }
-  return cudaGetLastError();
+  if (T <= 64)
+    return launch_dependent(route_select_rank, dim3(T), dim3(((E + 31) / 32) * 32), 0, stream, T, E, s.top_k,
+                            (const float*)logits, bias, topk_idx, topk_w);
+  return launch_dependent(route_select, dim3((T + kSelWarps - 1) / kSelWarps), dim3(kSelWarps * 32), 0, stream, T, E,
+                          s.top_k, (const float*)logits, bias, topk_idx, topk_w);
 }
 
 }  // namespace qre

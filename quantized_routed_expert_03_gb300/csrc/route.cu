@@ -24,11 +24,13 @@ constexpr int kGemvTMax = 16;
 
 template <int TMAX>
 __global__ void __launch_bounds__(256) route_logits_gemv(int T, int H, int E, const uint16_t* __restrict__ x,
-                                                         const float* __restrict__ W, float* __restrict__ logits) {
+                                                         const float* __restrict__ W, float* __restrict__ logits,
+                                                         int stage) {
   __shared__ float part[2][4][TMAX];
+  extern __shared__ uint4 xs_dyn[];   // T * H bf16 when staged (dynamic size > 0)
   grid_dependency_wait();
   grid_dependents_launch();
-  logits_gemv_pair<TMAX>(blockIdx.x * 2, T, H, E, x, W, logits, part);
+  logits_gemv_pair<TMAX>(blockIdx.x * 2, T, H, E, x, W, logits, part, stage ? xs_dyn : nullptr);
 }
 
 // logits[T][E] = X[T][H] (bf16) * W[E][H]^T (fp32), fp32 CUDA-core GEMM.
@@ -171,12 +173,17 @@ cudaError_t launch_route(const qre_layer_shape& s, int T, const uint16_t* x, con
   float* logits = static_cast<float*>(ws);
   const int H = s.hidden, E = s.n_experts;
   cudaError_t err;
-  if (T <= 8) {
-    err = launch_dependent(route_logits_gemv<8>, dim3((E + 1) / 2), dim3(256), 0, stream, T, H, E, x, w_router,
-                           logits);
-  } else if (T <= kGemvTMax) {
-    err = launch_dependent(route_logits_gemv<kGemvTMax>, dim3((E + 1) / 2), dim3(256), 0, stream, T, H, E, x,
-                           w_router, logits);
+  // the tokens go through shared memory when they fit (64 KB)
+  const size_t xs_bytes = (size_t)T * H * 2;
+  const int stage = xs_bytes <= 64 * 1024 ? 1 : 0;
+  const size_t dyn = stage ? xs_bytes : 0;
+  if (T <= kGemvTMax) {
+    auto kernel = T <= 8 ? route_logits_gemv<8> : route_logits_gemv<kGemvTMax>;
+    if (stage) {
+      err = ensure_smem_limit(reinterpret_cast<const void*>(kernel), (int)dyn);
+      if (err != cudaSuccess) return err;
+    }
+    err = launch_dependent(kernel, dim3((E + 1) / 2), dim3(256), dyn, stream, T, H, E, x, w_router, logits, stage);
   } else {
     dim3 grid((E + BN - 1) / BN, (T + BM - 1) / BM);
     err = launch_dependent(route_logits_gemm, grid, dim3(256), 0, stream, T, H, E, x, w_router, logits);

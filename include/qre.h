@@ -113,9 +113,10 @@ typedef struct {
   const uint16_t* s_gate_up;  /* 2I x H/G fp16 scales, device or host-mapped      */
   const uint8_t*  w_down;     /* H x I packed (H*I/2 bytes), device or host-mapped */
   const uint16_t* s_down;     /* H x I/G fp16 scales, device or host-mapped       */
-  uint32_t tier;              /* 0 = device memory, 1 = host-mapped (read with
-                                 direct loads over the host link); both are read
-                                 the same way, the tier is informational         */
+  uint32_t tier;              /* 0 = device memory (the decode kernels stage it
+                                 through shared memory with cp.async), 1 =
+                                 host-mapped (read with direct 16-byte loads over
+                                 the host link); results are identical        */
   uint32_t reserved;          /* must be 0                                      */
 } qre_slot;
 
@@ -238,9 +239,12 @@ QRE_API qre_status qre_dispatch(const qre_layer_shape* shape, int32_t T, const i
  *   expert_out  [T*k + T][H] fp32, device (written): row q < T*k is the output
  *               of pick perm[q] (unweighted), row T*k + t the shared expert's
  *               output for token t.
- * T <= 8 runs the bandwidth-bound decode kernels (fp32-exact products, fp32
- * accumulation); larger T runs the grouped-GEMM path (fp16 operands, fp32
- * accumulation).
+ * T <= 8 runs the bandwidth-bound decode kernels: for group 128 the weights as
+ * exact FP8 codes and the activations as sums of FP8 terms (x: two, exact for
+ * bf16 unless an element is below 2^-13 of its 128-group's largest; h: four,
+ * about 16 significant bits), exact products, fp32 accumulation; for groups 32
+ * and 64 exact fp16 codes times x split into two fp16 parts.  Larger T runs
+ * the grouped-GEMM path (fp16 operands, fp32 accumulation).
  */
 QRE_API qre_status qre_expert_ffn(const qre_layer_shape* shape, int32_t T, const uint16_t* x_bf16,
                           const qre_slot* slots, const int32_t* offsets, const int32_t* perm,

@@ -7,6 +7,13 @@
 // bandwidth, so the packed weights must stream at full rate while everything
 // else stays under that.
 //
+// Two kernels share the structure below: ffn_e4m3_kernel for group 128 (every
+// full-size configuration: weights as FP8 E4M3 codes, 128-element stages, see
+// the comment above it) and ffn_decode_kernel for groups 32 and 64 (weights as
+// fp16 codes, 64-element stages).  Both launch as programmatic dependents
+// (launch_dependent): gate/up waits for the dispatch, down's CTAs take the SMs
+// gate/up CTAs leave and wait for the gate/up grid only before reading h.
+//
 // Layout of the work (5th-generation tensor cores, weights in tensor memory)
 //   * A unit is 128 consecutive rows of one expert's matrix (UMMA M = 128; for
 //     gate/up four blocks of 16 gate rows, each followed by its 16 up rows).
@@ -15,33 +22,32 @@
 //   * The four warpgroups of a CTA split the reduction length K.  Thread r of a
 //     warpgroup owns weight row r of the unit and tensor-memory lane r.  The
 //     packed weights are stored in 4 KB chunks of 128 rows x 64 reduction
-//     elements, so each warp's 16-byte loads cover 512 contiguous bytes; they are
-//     prefetched up to four stages ahead, across unit boundaries (host-resident
-//     experts are read the same way, zero-copy).  Each thread decodes its 64
-//     nibbles per stage into fp16 pairs of exact integer codes and writes them
-//     into its lane with tcgen05.st.
-//   * One tcgen05.mma (A from tensor memory, B from shared memory, M=128, N=16,
-//     K=16) is cheap for the tensor core but takes a warp on the order of a
-//     hundred cycles to issue, while issues from different warps overlap.  So
-//     every warp issues: the stages of a warpgroup are issued in turn by its
-//     four warps, one stage late, once all four warps have arrived on the
-//     stage's mbarrier, and complete on one commit per stage.
-//   * B holds the tokens (T <= 8) in shared memory, 128-byte swizzled: row 2n
-//     the fp16 high part of token n, row 2n + 1 the fp16 remainder (x - high),
-//     so the products stay accurate to about fp32.  The weights are exact codes,
-//     so the only rounding is the fp32 accumulation.
+//     elements, so each warp's 16-byte loads cover 512 contiguous bytes; they
+//     run a few stages ahead, across unit boundaries (FP8 kernel: through a
+//     cp.async ring in shared memory; host-resident experts are read the same
+//     way with direct loads, zero-copy).  Each thread decodes its nibbles into
+//     exact codes and writes them into its lane with tcgen05.st.
+//   * One tcgen05.mma (A from tensor memory, B from shared memory) is cheap for
+//     the tensor core but takes a warp on the order of a hundred cycles to
+//     issue, while issues from different warps overlap.  So every warp issues:
+//     the stages of a warpgroup are issued in turn by its four warps, one stage
+//     late, once all four warps have arrived on the stage's mbarrier, and
+//     complete on one commit per stage.
+//   * B holds the tokens (T <= 8) in shared memory, 128-byte swizzled: fp16
+//     kernel, row 2n the fp16 high part of token n and row 2n + 1 the remainder
+//     (x - high); FP8 kernel, E4M3 terms per token and group.  The weights are
+//     exact codes, so the only rounding is that of the activations' split and
+//     the fp32 accumulation.
 //   * Every quantization group accumulates into its own buffer; a few stages
-//     later the owning threads read it back (tcgen05.ld; two columns for a
-//     single token, sixteen for eight), add the two halves and apply the
-//     group's fp16 scale in fp32.
+//     later the owning threads read it back (tcgen05.ld), combine the columns
+//     of each token and apply the group's fp16 scale in fp32.
 //   * The warpgroups' partial rows are added in fixed order (deterministic), one
 //     unit after they were handed over: gate/up pairs each gate row with its up
-//     row (16 lanes apart, a shuffle) and stores h = silu(g) * u as fp16 high
-//     part and remainder for the down kernel; down writes the expert's output
-//     rows.
-//   * Inside every group of 8 reduction elements the tokens and h are stored in
-//     the order the nibble decode yields weight pairs (0,4,1,5,2,6,3,7), which
-//     leaves every dot product unchanged.
+//     row (16 lanes apart, a shuffle) and stores h for the down kernel; down
+//     writes the expert's output rows.
+//   * fp16 kernel: inside every group of 8 reduction elements the tokens and h
+//     are stored in the order the nibble decode yields weight pairs
+//     (0,4,1,5,2,6,3,7), which leaves every dot product unchanged.
 #include "common.cuh"
 #include "internal.h"
 #include "tc.cuh"

@@ -33,64 +33,98 @@ __global__ void __launch_bounds__(256) route_logits_gemv(int T, int H, int E, co
   logits_gemv_pair<TMAX>(blockIdx.x * 2, T, H, E, x, W, logits, part, stage ? xs_dyn : nullptr);
 }
 
-// logits[T][E] = X[T][H] (bf16) * W[E][H]^T (fp32), fp32 CUDA-core GEMM.
-constexpr int BM = 64, BN = 64, BK = 32;
+// logits[T][E] = X[T][H] (bf16) * W[E][H]^T (fp32), fp32 CUDA-core GEMM for
+// T > 16.  A CTA computes 128 tokens x 96 experts, each thread 8 x 6 outputs
+// from 16-deep k slices held in shared memory (double-buffered: the next
+// slice's global loads are in flight while the current one is consumed).  Every
+// output is one fp32 FMA chain over k in ascending order, so the result does
+// not depend on the tiling.
+constexpr int BM = 128, BN = 96, BK = 16;
+constexpr int TM = 8, TN = 6;   // outputs per thread: tokens x experts
 __global__ void __launch_bounds__(256) route_logits_gemm(int T, int H, int E, const uint16_t* __restrict__ x,
                                                          const float* __restrict__ W, float* __restrict__ logits) {
-  __shared__ float xs[BK][BM + 4];
-  __shared__ float ws[BK][BN + 4];
+  __shared__ __align__(16) float xs[2][BK][BM + 4];
+  __shared__ __align__(16) float ws[2][BK][BN + 4];
   grid_dependency_wait();
   grid_dependents_launch();
   const int tm = blockIdx.y * BM, en = blockIdx.x * BN;
-  const int tx = threadIdx.x & 15, ty = threadIdx.x >> 4;   // 16 x 16 threads, 4 x 4 outputs each
-  float acc[4][4] = {};
-  for (int k0 = 0; k0 < H; k0 += BK) {
-    // load 64 x 32 of X and of W; 256 threads, 8 elements each
-    for (int i = threadIdx.x; i < BM * BK / 4; i += 256) {
-      const int r = i / (BK / 4), cc = (i % (BK / 4)) * 4;
-      const int tok = tm + r;
-      if (tok < T) {
-        const uint2 v = __ldg(reinterpret_cast<const uint2*>(x + (size_t)tok * H + k0 + cc));
-        xs[cc + 0][r] = bf16_bits_to_float(v.x & 0xFFFFu);
-        xs[cc + 1][r] = bf16_bits_to_float(v.x >> 16);
-        xs[cc + 2][r] = bf16_bits_to_float(v.y & 0xFFFFu);
-        xs[cc + 3][r] = bf16_bits_to_float(v.y >> 16);
-      } else {
-        xs[cc + 0][r] = xs[cc + 1][r] = xs[cc + 2][r] = xs[cc + 3][r] = 0.f;
-      }
-      const int ex = en + r;
-      if (ex < E) {
-        const float4 v = __ldg(reinterpret_cast<const float4*>(W + (size_t)ex * H + k0 + cc));
-        ws[cc + 0][r] = v.x;
-        ws[cc + 1][r] = v.y;
-        ws[cc + 2][r] = v.z;
-        ws[cc + 3][r] = v.w;
-      } else {
-        ws[cc + 0][r] = ws[cc + 1][r] = ws[cc + 2][r] = ws[cc + 3][r] = 0.f;
+  const int tid = threadIdx.x;
+  const int tx = tid & 15, ty = tid >> 4;   // 16 x 16 threads: experts tx*6.., tokens ty*8..
+  // global -> register staging of one k slice: X 128 rows x 16 (one uint4 of 8
+  // bf16 per thread), W 96 rows x 16 (384 float4: threads 0..255, then 0..127)
+  const int xr = tid >> 1, xk = (tid & 1) * 8;
+  uint4 xv;
+  float4 wv[2];
+  auto load_slice = [&](int k0) {
+    const int tok = tm + xr;
+    xv = tok < T ? __ldg(reinterpret_cast<const uint4*>(x + (size_t)tok * H + k0 + xk)) : make_uint4(0u, 0u, 0u, 0u);
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+      const int f = tid + 256 * i;   // float4 index in the 96 x 4 slice
+      const int er = f >> 2, kq = (f & 3) * 4;
+      wv[i] = (f < BN * BK / 4 && en + er < E)
+                  ? __ldg(reinterpret_cast<const float4*>(W + (size_t)(en + er) * H + k0 + kq))
+                  : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+  };
+  auto store_slice = [&](int buf) {
+    const uint32_t v[4] = {xv.x, xv.y, xv.z, xv.w};
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      xs[buf][xk + 2 * j][xr] = bf16_bits_to_float(v[j] & 0xFFFFu);
+      xs[buf][xk + 2 * j + 1][xr] = bf16_bits_to_float(v[j] >> 16);
+    }
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+      const int f = tid + 256 * i;
+      if (f < BN * BK / 4) {
+        const int er = f >> 2, kq = (f & 3) * 4;
+        ws[buf][kq + 0][er] = wv[i].x;
+        ws[buf][kq + 1][er] = wv[i].y;
+        ws[buf][kq + 2][er] = wv[i].z;
+        ws[buf][kq + 3][er] = wv[i].w;
       }
     }
-    __syncthreads();
-#pragma unroll 8
+  };
+  float acc[TM][TN];
+#pragma unroll
+  for (int i = 0; i < TM; ++i)
+#pragma unroll
+    for (int j = 0; j < TN; ++j) acc[i][j] = 0.f;
+  load_slice(0);
+  store_slice(0);
+  __syncthreads();
+  const int nk = H / BK;
+  for (int ks = 0; ks < nk; ++ks) {
+    const int buf = ks & 1;
+    if (ks + 1 < nk) load_slice((ks + 1) * BK);
+#pragma unroll
     for (int kk = 0; kk < BK; ++kk) {
-      float a[4], b[4];
+      const float4 a0 = *reinterpret_cast<const float4*>(&xs[buf][kk][ty * TM]);
+      const float4 a1 = *reinterpret_cast<const float4*>(&xs[buf][kk][ty * TM + 4]);
+      const float a[TM] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
+      float bv[TN];
 #pragma unroll
-      for (int i = 0; i < 4; ++i) a[i] = xs[kk][ty * 4 + i];
+      for (int j = 0; j < TN; j += 2) {
+        const float2 b2 = *reinterpret_cast<const float2*>(&ws[buf][kk][tx * TN + j]);
+        bv[j] = b2.x;
+        bv[j + 1] = b2.y;
+      }
 #pragma unroll
-      for (int j = 0; j < 4; ++j) b[j] = ws[kk][tx * 4 + j];
+      for (int i = 0; i < TM; ++i)
 #pragma unroll
-      for (int i = 0; i < 4; ++i)
-#pragma unroll
-        for (int j = 0; j < 4; ++j) acc[i][j] = fmaf(a[i], b[j], acc[i][j]);
+        for (int j = 0; j < TN; ++j) acc[i][j] = fmaf(a[i], bv[j], acc[i][j]);
     }
+    if (ks + 1 < nk) store_slice(buf ^ 1);
     __syncthreads();
   }
 #pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    const int tok = tm + ty * 4 + i;
+  for (int i = 0; i < TM; ++i) {
+    const int tok = tm + ty * TM + i;
     if (tok >= T) continue;
 #pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      const int ex = en + tx * 4 + j;
+    for (int j = 0; j < TN; ++j) {
+      const int ex = en + tx * TN + j;
       if (ex < E) logits[(size_t)tok * E + ex] = acc[i][j];
     }
   }

@@ -88,28 +88,12 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity
   return mbar_wait_slow(bar, parity, abort, status);
 }
 
-// ---------------------------------------------------------------- bulk copy
+// ---------------------------------------------------------------- async copies
 
-// 1-D bulk copy global -> shared, completing `bytes` transaction bytes on `bar`.
-// dst, src 16-byte aligned; bytes a multiple of 16.
-__device__ __forceinline__ void bulk_copy_g2s(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
-  asm volatile(
-      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
-          smem_addr(dst)),
-      "l"(src), "r"(bytes), "r"(smem_addr(bar))
-      : "memory");
-}
-
-// 16-byte asynchronous copy global -> shared (L2 only), and the arrival on an
-// mbarrier once all of this thread's earlier cp.async copies have completed
-// (the barrier's expected count must include this arrival).
+// 16-byte asynchronous copy global -> shared (cached in L2 only).
 __device__ __forceinline__ void cp_async_16(void* dst, const void* src) {
   asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_addr(dst)), "l"(src) : "memory");
 }
-__device__ __forceinline__ void cp_async_arrive(uint64_t* bar) {
-  asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(smem_addr(bar)) : "memory");
-}
-__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
 // Closes this thread's current group of cp.async copies (an empty group if it
 // issued none), and waits until at most N of its groups are still in flight.
 __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
@@ -118,29 +102,10 @@ __device__ __forceinline__ void cp_async_wait_group() {
   asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
 }
 
-// Returns its argument through a volatile instruction: shared-memory loads whose
-// address depends on the result stay after every earlier volatile asm (such as
-// an mbarrier wait) while remaining free to be reordered among themselves.
-__device__ __forceinline__ uint32_t after_wait(uint32_t v) {
-  uint32_t r;
-  asm volatile("mov.b32 %0, %1;" : "=r"(r) : "r"(v));
-  return r;
-}
-__device__ __forceinline__ uint32_t lds32(uint32_t addr) {
-  uint32_t v;
-  asm("ld.shared.u32 %0, [%1];" : "=r"(v) : "r"(addr));
-  return v;
-}
 __device__ __forceinline__ unsigned short lds16(uint32_t addr) {
   unsigned short v;
   asm("ld.shared.u16 %0, [%1];" : "=h"(v) : "r"(addr));
   return v;
-}
-
-// ---------------------------------------------------------------- named barrier
-
-__device__ __forceinline__ void named_barrier_sync(int id, int nthreads) {
-  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
 }
 
 // ---------------------------------------------------------------- PDL
@@ -148,18 +113,6 @@ __device__ __forceinline__ void named_barrier_sync(int id, int nthreads) {
 __device__ __forceinline__ void grid_dependency_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 __device__ __forceinline__ void grid_dependents_launch() {
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-}
-
-// ---------------------------------------------------------------- tensor-core MMA
-
-// D[16x8] += A[16x16] * B[16x8]; f16 operands, f32 accumulators.
-__device__ __forceinline__ void mma_f16_16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
-                                              uint32_t b0, uint32_t b1) {
-  asm(
-      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
-      "{%0,%1,%2,%3};"
-      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 
 // ---------------------------------------------------------------- 4-bit decode
@@ -205,8 +158,5 @@ __device__ __forceinline__ uint4 ldg_v4_early(const void* p) {
 
 __device__ __forceinline__ float bf16_bits_to_float(uint32_t b) { return __uint_as_float(b << 16); }
 
-__device__ __forceinline__ uint32_t pack_half2(float lo, float hi) {
-  return h2_as_u32(__floats2half2_rn(lo, hi));
-}
 
 }  // namespace qre

@@ -34,13 +34,13 @@ __global__ void __launch_bounds__(256) route_logits_gemv(int T, int H, int E, co
 }
 
 // logits[T][E] = X[T][H] (bf16) * W[E][H]^T (fp32), fp32 CUDA-core GEMM for
-// T > 16.  A CTA computes 128 tokens x 96 experts, each thread 8 x 6 outputs
+// T > 16.  A CTA computes 64 tokens x 96 experts, each thread 4 x 6 outputs
 // from 16-deep k slices held in shared memory (double-buffered: the next
 // slice's global loads are in flight while the current one is consumed).  Every
 // output is one fp32 FMA chain over k in ascending order, so the result does
 // not depend on the tiling.
-constexpr int BM = 128, BN = 96, BK = 16;
-constexpr int TM = 8, TN = 6;   // outputs per thread: tokens x experts
+constexpr int TM = 4, TN = 6;   // outputs per thread: tokens x experts
+constexpr int BM = 16 * TM, BN = 16 * TN, BK = 16;
 __global__ void __launch_bounds__(256) route_logits_gemm(int T, int H, int E, const uint16_t* __restrict__ x,
                                                          const float* __restrict__ W, float* __restrict__ logits) {
   __shared__ __align__(16) float xs[2][BK][BM + 4];
@@ -49,15 +49,18 @@ __global__ void __launch_bounds__(256) route_logits_gemm(int T, int H, int E, co
   grid_dependents_launch();
   const int tm = blockIdx.y * BM, en = blockIdx.x * BN;
   const int tid = threadIdx.x;
-  const int tx = tid & 15, ty = tid >> 4;   // 16 x 16 threads: experts tx*6.., tokens ty*8..
-  // global -> register staging of one k slice: X 128 rows x 16 (one uint4 of 8
-  // bf16 per thread), W 96 rows x 16 (384 float4: threads 0..255, then 0..127)
-  const int xr = tid >> 1, xk = (tid & 1) * 8;
+  const int tx = tid & 15, ty = tid >> 4;   // 16 x 16 threads: experts tx*TN.., tokens ty*TM..
+  // global -> register staging of one k slice: X BM rows x 16 (one uint4 of 8
+  // bf16 per thread, threads below 2 BM), W 96 rows x 16 (384 float4: threads
+  // 0..255, then 0..127)
+  const bool xl = tid < 2 * BM;
+  const int xr = xl ? tid >> 1 : 0, xk = (tid & 1) * 8;
   uint4 xv;
   float4 wv[2];
   auto load_slice = [&](int k0) {
     const int tok = tm + xr;
-    xv = tok < T ? __ldg(reinterpret_cast<const uint4*>(x + (size_t)tok * H + k0 + xk)) : make_uint4(0u, 0u, 0u, 0u);
+    xv = (xl && tok < T) ? __ldg(reinterpret_cast<const uint4*>(x + (size_t)tok * H + k0 + xk))
+                         : make_uint4(0u, 0u, 0u, 0u);
 #pragma unroll
     for (int i = 0; i < 2; ++i) {
       const int f = tid + 256 * i;   // float4 index in the 96 x 4 slice
@@ -69,10 +72,12 @@ __global__ void __launch_bounds__(256) route_logits_gemm(int T, int H, int E, co
   };
   auto store_slice = [&](int buf) {
     const uint32_t v[4] = {xv.x, xv.y, xv.z, xv.w};
+    if (xl) {
 #pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      xs[buf][xk + 2 * j][xr] = bf16_bits_to_float(v[j] & 0xFFFFu);
-      xs[buf][xk + 2 * j + 1][xr] = bf16_bits_to_float(v[j] >> 16);
+      for (int j = 0; j < 4; ++j) {
+        xs[buf][xk + 2 * j][xr] = bf16_bits_to_float(v[j] & 0xFFFFu);
+        xs[buf][xk + 2 * j + 1][xr] = bf16_bits_to_float(v[j] >> 16);
+      }
     }
 #pragma unroll
     for (int i = 0; i < 2; ++i) {
@@ -100,9 +105,15 @@ __global__ void __launch_bounds__(256) route_logits_gemm(int T, int H, int E, co
     if (ks + 1 < nk) load_slice((ks + 1) * BK);
 #pragma unroll
     for (int kk = 0; kk < BK; ++kk) {
-      const float4 a0 = *reinterpret_cast<const float4*>(&xs[buf][kk][ty * TM]);
-      const float4 a1 = *reinterpret_cast<const float4*>(&xs[buf][kk][ty * TM + 4]);
-      const float a[TM] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
+      float a[TM];
+#pragma unroll
+      for (int i = 0; i < TM; i += 4) {
+        const float4 a4 = *reinterpret_cast<const float4*>(&xs[buf][kk][ty * TM + i]);
+        a[i] = a4.x;
+        a[i + 1] = a4.y;
+        a[i + 2] = a4.z;
+        a[i + 3] = a4.w;
+      }
       float bv[TN];
 #pragma unroll
       for (int j = 0; j < TN; j += 2) {

@@ -77,6 +77,26 @@ def ffn_source_hash():
     return h.hexdigest()[:16]
 
 
+def max_over_ranks(value: float, world: int) -> float:
+    """The largest of one number per rank (the slowest replica sets the time);
+    the number itself when there is one rank.  Works on an NCCL or a gloo group."""
+    if world <= 1:
+        return float(value)
+    import torch
+    import torch.distributed as dist
+    on_gpu = dist.get_backend() == "nccl"
+    dev = torch.device("cuda", torch.cuda.current_device()) if on_gpu else torch.device("cpu")
+    t = torch.tensor([float(value)], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput(world: int, tokens_per_step: int, steps: int, ms: float) -> float:
+    """Whole-job tokens/s: every rank runs `steps` steps of `tokens_per_step`
+    tokens in (at most) `ms` milliseconds."""
+    return world * tokens_per_step * steps / (ms / 1e3)
+
+
 def load_peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(path):
@@ -281,11 +301,7 @@ def run_ours(args, rank, local_rank, world):
     if world > 1:
         torch.distributed.barrier()
     t_wall1 = time.time()
-    ms = start.elapsed_time(end)
-    if world > 1:
-        t = torch.tensor([ms], device=device)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = max_over_ranks(start.elapsed_time(end), world)
     sampler.stop()
     clocks = sampler.summary(t_wall0, t_wall1)
 
@@ -324,7 +340,7 @@ def run_ours(args, rank, local_rank, world):
             host_bytes.append(n_host_act * wl.expert_payload)
 
     tokens_per_step = T * wl.layers_per_step
-    value = world * tokens_per_step * K / (ms / 1e3)
+    value = job_throughput(world, tokens_per_step, K, ms)
     peaks, peak_src = load_peaks()
     roofline = None
     if ffn_ms and not prefill:
@@ -450,8 +466,8 @@ def run_e2e(args, wl, xs, stream, device, tokens_per_step, world):
             one(j)
         s1.record(stream)
         torch.cuda.synchronize()
-    ms = s0.elapsed_time(s1)
-    return {"value": round(world * tokens_per_step * K / (ms / 1e3), 2), "unit": UNIT, "steps": K,
+    ms = max_over_ranks(s0.elapsed_time(s1), world)
+    return {"value": round(job_throughput(world, tokens_per_step, K, ms), 2), "unit": UNIT, "steps": K,
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
             "api": "MoELayer.forward captured in a CUDA graph; per step: pinned H2D input copy, replay, "
                    "pinned D2H of the bf16 output, stream synchronize"}

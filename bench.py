@@ -13,24 +13,34 @@ Workloads (``--workload``):
   decode1           H4096 I2048 E288 top-8 + shared, T = 1, all 289 experts in HBM
   decode8_zipf_x42  T = 8, Zipf(1.1) routing bias, 42 distinct layers
   cache4_x42        T = 4, Zipf(1.1), 42 layers, 100 experts/layer in pinned host memory
+  prefill8192       T = 8192 tokens through one layer (tcgen05 grouped GEMM)
   tiny              H256 I128 E16 top-4 + shared, T = 4
-``--impl reference`` times the fp64 CPU oracle (the only reference this build
-has) on a bounded sample of the same workload.
+The line's top level is the ``--workload`` (decode1 by default); the workloads
+named by ``--also`` (prefill8192 by default) are measured in the same run, each
+with its own steps, roofline, clocks, e2e and oracle baseline, under
+``workloads``.  ``--impl reference`` times the fp64 CPU oracle (the only
+reference this build has) on a bounded sample of the same workload.
 """
 
 from __future__ import annotations
 
-import argparse
-import hashlib
-import json
-import math
 import os
-import subprocess
-import sys
-import threading
-import time
 
-import numpy as np
+# The oracle legs use numpy's BLAS; give it every core of this process explicitly
+# (before numpy is imported, which reads these once).
+_NCPU = len(os.sched_getaffinity(0))
+for _v in ("OPENBLAS_NUM_THREADS", "OMP_NUM_THREADS", "MKL_NUM_THREADS"):
+    os.environ.setdefault(_v, str(_NCPU))
+
+import argparse  # noqa: E402
+import hashlib  # noqa: E402
+import json  # noqa: E402
+import subprocess  # noqa: E402
+import sys  # noqa: E402
+import threading  # noqa: E402
+import time  # noqa: E402
+
+import numpy as np  # noqa: E402
 
 ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
@@ -40,6 +50,10 @@ import synthetic  # noqa: E402
 METRIC = "MoE-layer tokens/s at 1 GB300 and achieved HBM GB/s vs roofline (decode); prefill TFLOP/s"
 UNIT = "tokens/s"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+DTYPE_DECODE = ("e4m3 x e4m3, fp32 accumulate (4-bit weights as exact E4M3 codes; x as 2 E4M3 terms, exact "
+                "for bf16; h as 4 E4M3 terms, ~16 significant bits)")
+DTYPE_DECODE_FP16 = "fp16 x fp16 (exact 4-bit codes; x and h as fp16 high part + remainder), fp32 accumulate"
+DTYPE_PREFILL = "fp16 x fp16 (dequantized weights and h rounded to fp16; bf16 x exact), fp32 accumulate"
 
 
 # ------------------------------------------------------------------ helpers
@@ -49,8 +63,8 @@ def dist_env():
             int(os.environ.get("WORLD_SIZE", 1)))
 
 
-# DRAM bytes per expert-FFN call (both kernels) measured with ncu on the decode1
-# workload, for the FFN kernel code with the given hash (ffn_source_hash).  Reported only
+# DRAM bytes per expert-FFN call (both kernels) measured with ncu on a workload,
+# for the FFN kernel code with the given hash (ffn_source_hash).  Reported only
 # while the sources still hash to that value; a changed kernel reports null.
 MEASURED_TRAFFIC = {"decode1": (117405568, "7a5a27b151322a8e")}
 FFN_SOURCES = ("ffn_decode.cu", "common.cuh", "tc.cuh", "internal.h")
@@ -97,6 +111,11 @@ def job_throughput(world: int, tokens_per_step: int, steps: int, ms: float) -> f
     return world * tokens_per_step * steps / (ms / 1e3)
 
 
+def split_steps(K: int, per_graph: int):
+    """(full replays of a per_graph-step graph, remaining steps) that make exactly K steps."""
+    return K // per_graph, K % per_graph
+
+
 def load_peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(path):
@@ -104,6 +123,35 @@ def load_peaks():
             d = json.load(f)
         return d, "measured"
     return dict(FALLBACK_PEAKS), "fallback"
+
+
+def default_sets(cfg) -> int:
+    """Distinct layer weight sets the steps rotate over: a stack has its own
+    layers; one decode layer is repeated in 8 copies (30 GB, far more than L2); a
+    prefill step streams far more than L2 by itself."""
+    if cfg.layers > 1:
+        return cfg.layers
+    if cfg.tokens > 8:
+        return 1
+    return 8 if cfg.hidden >= 4096 else 2
+
+
+def expert_payload(cfg) -> int:
+    """Packed bytes of one expert (weights + scales), the library's format."""
+    H, I, G = cfg.hidden, cfg.inter, cfg.group
+    return 2 * I * H // 2 + 2 * I * (H // G) * 2 + H * I // 2 + H * (I // G) * 2
+
+
+def workload_config(name: str, n_sets: int, world: int) -> dict:
+    """The ``config`` object of a workload's line (the same for both arms)."""
+    cfg = synthetic.CONFIGS[name]
+    return {"workload": name, "note": cfg.note, "tokens_per_step": cfg.tokens, "layers_per_step": cfg.layers,
+            "hidden": cfg.hidden, "inter": cfg.inter, "experts": cfg.n_experts, "top_k": cfg.top_k,
+            "group": cfg.group,
+            "l2": f"inputs larger than L2: {n_sets} distinct layer weight set(s) rotated "
+                  f"({n_sets * (cfg.n_experts + 1) * expert_payload(cfg) / 1e9:.1f} GB of packed experts)",
+            "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+            "launch": "CUDA graph of captured steps"}
 
 
 class ClockSampler:
@@ -167,14 +215,7 @@ class Workload:
         H, I, E, k, G, T = cfg.hidden, cfg.inter, cfg.n_experts, cfg.top_k, cfg.group, cfg.tokens
         self.T = T
         self.layers_per_step = cfg.layers
-        if n_sets is None:
-            if cfg.layers > 1:
-                n_sets = cfg.layers
-            elif T > 8:
-                n_sets = 1          # a prefill step streams far more than L2 on its own
-            else:
-                n_sets = 8 if H >= 4096 else 2
-        self.n_sets = n_sets
+        self.n_sets = n_sets = default_sets(cfg) if n_sets is None else n_sets
         t0 = time.time()
         self.sets = []
         staging = None
@@ -204,11 +245,11 @@ class Workload:
             self.sets.append({"layer": L, "dev": dev, "host": harena, "wr": wr, "bias": bias, "n_host": n_host,
                               "host_mask": host})
             if (r + 1) % 8 == 0:
-                log(f"[bench] built {r + 1}/{n_sets} layers ({time.time() - t0:.0f} s)")
+                log(f"[bench] {name}: built {r + 1}/{n_sets} layers ({time.time() - t0:.0f} s)")
         torch.cuda.synchronize()
         self.expert_payload = self.sets[0]["dev"].layout["payload"]
-        self.host_ranks = None
-        log(f"[bench] weights ready: {n_sets} layer(s), {time.time() - t0:.1f} s")
+        self.build_s = time.time() - t0
+        log(f"[bench] {name}: weights ready, {n_sets} layer set(s), {self.build_s:.1f} s")
 
     def x_pool(self, n, device):
         """n distinct activation batches per layer set, [n_sets][n][T,H] bf16 on device."""
@@ -221,17 +262,10 @@ class Workload:
         return out
 
 
-def run_ours(args, rank, local_rank, world):
+def measure_workload(name, args, K, W, rank, local_rank, world, device, log, cpu_leg=True):
+    """Times K steps of one workload (after W warm-up steps) and returns its record."""
     import torch
-    device = torch.device(f"cuda:{local_rank}")
-    torch.cuda.set_device(device)
-    from quantized_routed_expert_03_gb300 import build as qbuild
-    qbuild.build()
-    import quantized_routed_expert_03_gb300 as qre
-    qre.load_library()
-
-    log = (lambda *a: print(*a, file=sys.stderr, flush=True)) if rank == 0 else (lambda *a: None)
-    wl = Workload(args.workload, device, n_sets=args.sets, log=log)
+    wl = Workload(name, device, n_sets=args.sets if name == args.workload else None, log=log)
     cfg, T, H, k = wl.cfg, wl.T, wl.cfg.hidden, wl.cfg.top_k
     stream = torch.cuda.Stream(device)
 
@@ -242,7 +276,6 @@ def run_ours(args, rank, local_rank, world):
     per_graph = 1 if (stack or prefill) else wl.n_sets * 4
     n_x = 4 if stack else (2 if prefill else per_graph // wl.n_sets)
     xs = wl.x_pool(n_x, device)
-    K, W = args.steps, args.warmup
 
     def one_layer(s, x):
         L = s["layer"]
@@ -261,7 +294,7 @@ def run_ours(args, rank, local_rank, world):
 
     # eager warm-up (sets kernel attributes, loads modules) then capture
     with torch.cuda.stream(stream):
-        for j in range(min(W, per_graph) if W else 1):
+        for j in range(min(W, per_graph)):
             step_fn(j)
     stream.synchronize()
 
@@ -272,14 +305,19 @@ def run_ours(args, rank, local_rank, world):
                 step_fn(j)
         return g
 
-    g_full = capture(per_graph)
-    rem = K % per_graph
+    n_full, rem = split_steps(K, per_graph)
+    g_full = capture(per_graph) if n_full else None
     g_rem = capture(rem) if rem else None
-    n_full = K // per_graph
 
-    # warm-up replays
-    for _ in range(max(1, math.ceil(W / per_graph))):
-        g_full.replay()
+    # warm-up replays: at least W steps, and every graph the timed region replays has run before
+    warm = 0
+    while warm < W or (g_full is not None and warm == 0):
+        if g_full is not None:
+            g_full.replay()
+            warm += per_graph
+        if g_rem is not None:
+            g_rem.replay()
+            warm += rem
     torch.cuda.synchronize()
 
     sampler = ClockSampler(local_rank)
@@ -308,110 +346,139 @@ def run_ours(args, rank, local_rank, world):
     # FFN stage: the expert FFN alone, back to back over the layer sets (each
     # with the routing its last timed step left), in a graph of its own on the
     # same stream, timed with CUDA events around whole replays.
-    ffn_ms, ffn_bytes, n_act, host_bytes = [], [], [], []
     I = cfg.inter
     ffn_flops = 2.0 * 3 * H * I * (T * k + T)        # gate, up, down for every pick and the shared expert
-    if n_full > 0:
-        ffn_calls = [(r, wl.sets[r]) for r in range(len(wl.sets))] * (1 if stack else 4)
-        g_ffn = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(g_ffn, stream=stream):
-            for r, sset in ffn_calls:
-                sset["layer"].expert_ffn(xs[r][0], T)
-        for _ in range(3):
-            g_ffn.replay()
-        torch.cuda.synchronize()
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        reps = max(3, min(50, int(0.05 / max(ms / K / 1e3, 1e-6) / len(ffn_calls) * wl.layers_per_step) + 1))
-        with torch.cuda.stream(stream):
-            e0.record(stream)
-            for _ in range(reps):
-                g_ffn.replay()
-            e1.record(stream)
-        torch.cuda.synchronize()
-        per_call_ms = e0.elapsed_time(e1) / (reps * len(ffn_calls))
+    ffn_calls = [(r, wl.sets[r]) for r in range(len(wl.sets))] * (1 if (stack or prefill) else 4)
+    g_ffn = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g_ffn, stream=stream):
         for r, sset in ffn_calls:
-            L = sset["layer"]
-            a = int(L.n_active[0].item())
-            ids = L.active[:a].cpu().numpy()
-            ffn_ms.append(per_call_ms)
-            n_act.append(a)
-            ffn_bytes.append((a + 1) * wl.expert_payload + T * H * 2 + (T * k + T) * H * 4)
-            n_host_act = int(sset["host_mask"][ids].sum()) if sset["n_host"] else 0
-            host_bytes.append(n_host_act * wl.expert_payload)
+            sset["layer"].expert_ffn(xs[r][0], T)
+    for _ in range(3):
+        g_ffn.replay()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    reps = max(3, min(50, int(0.05 / max(ms / K / 1e3, 1e-6) / len(ffn_calls) * wl.layers_per_step) + 1))
+    with torch.cuda.stream(stream):
+        e0.record(stream)
+        for _ in range(reps):
+            g_ffn.replay()
+        e1.record(stream)
+    torch.cuda.synchronize()
+    ffn_ms_call = max_over_ranks(e0.elapsed_time(e1), world) / (reps * len(ffn_calls))
+    ffn_bytes, n_act, host_bytes = [], [], []
+    for r, sset in ffn_calls:
+        L = sset["layer"]
+        a = int(L.n_active[0].item())
+        ids = L.active[:a].cpu().numpy()
+        n_act.append(a)
+        ffn_bytes.append((a + 1) * wl.expert_payload + T * H * 2 + (T * k + T) * H * 4)
+        n_host_act = int(sset["host_mask"][ids].sum()) if sset["n_host"] else 0
+        host_bytes.append(n_host_act * wl.expert_payload)
+    del g_ffn
 
     tokens_per_step = T * wl.layers_per_step
     value = job_throughput(world, tokens_per_step, K, ms)
     peaks, peak_src = load_peaks()
-    roofline = None
-    if ffn_ms and not prefill:
-        achieved = float(np.mean(ffn_bytes)) / (float(np.mean(ffn_ms)) / 1e3) / 1e9
+    fp8 = cfg.group == 128
+    if not prefill:
+        achieved = float(np.mean(ffn_bytes)) / (ffn_ms_call / 1e3) / 1e9
         peak = float(peaks["hbm_gbs"])
-        traffic = args.traffic if args.traffic is not None else recorded_traffic(args.workload)
+        traffic = (args.traffic if (args.traffic is not None and name == args.workload)
+                   else recorded_traffic(name))
         roofline = {"bound": "hbm", "kernel": "qre_expert_ffn (gate/up + down dequant-GEMV kernels)",
                     "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                     "frac": round(achieved / peak, 4), "traffic": traffic,
                     "traffic_unit": "bytes per FFN call (ncu dram read + write)",
                     "peak_source": "of measured (MEASURED_PEAKS.json hbm_gbs)" if peak_src == "measured" else
                     "of fallback 6.8 TB/s",
-                    "ffn_us_mean": round(float(np.mean(ffn_ms)) * 1e3, 2),
+                    "ffn_us_mean": round(ffn_ms_call * 1e3, 2),
                     "ffn_bytes_mean": int(np.mean(ffn_bytes)),
                     "unique_experts_mean": round(float(np.mean(n_act)) + 1, 2),
-                    "timed_region": "CUDA events around replays of a graph of expert-FFN calls over the layer sets (mean per call)"}
+                    "timed_region": "CUDA events around replays of a graph of expert-FFN calls over the "
+                                    "layer sets (mean per call, slowest rank)"}
         if any(host_bytes):
             # experts read over the host link (pinned host memory, zero-copy) vs from HBM
             hb = float(np.mean(host_bytes))
             roofline["host_bytes_mean"] = int(hb)
             roofline["hbm_bytes_mean"] = int(float(np.mean(ffn_bytes)) - hb)
-            roofline["hbm_gbs"] = round((float(np.mean(ffn_bytes)) - hb) / (float(np.mean(ffn_ms)) / 1e3) / 1e9, 1)
-            roofline["host_link_gbs"] = round(hb / (float(np.mean(ffn_ms)) / 1e3) / 1e9, 1)
+            roofline["hbm_gbs"] = round((float(np.mean(ffn_bytes)) - hb) / (ffn_ms_call / 1e3) / 1e9, 1)
+            roofline["host_link_gbs"] = round(hb / (ffn_ms_call / 1e3) / 1e9, 1)
+            roofline["frac_hbm"] = round(roofline["hbm_gbs"] / peak, 4)
         per_layer = float(np.mean(ffn_bytes)) + cfg.n_experts * H * 4
         roofline["step_hbm_gbs"] = round(per_layer * wl.layers_per_step / (ms / K / 1e3) / 1e9, 1)
-    elif ffn_ms:
-        achieved = ffn_flops / (float(np.mean(ffn_ms)) / 1e3) / 1e12
-        peak = float(peaks.get("bf16_tflops_sustained", peaks["bf16_tflops"]))
+        roofline["step_frac"] = round(roofline["step_hbm_gbs"] / peak, 4)
+    else:
+        achieved = ffn_flops / (ffn_ms_call / 1e3) / 1e12
+        peak = float(peaks["bf16_tflops"])
         roofline = {"bound": "tensor", "kernel": "qre_expert_ffn (gather + two tcgen05 grouped GEMMs)",
                     "achieved": round(achieved, 1), "peak": peak, "unit": "TFLOP/s",
-                    "frac": round(achieved / peak, 4), "traffic": args.traffic,
-                    "peak_source": ("of measured (MEASURED_PEAKS.json bf16_tflops_sustained; fp16 has the "
-                                    "same nominal dense rate)") if peak_src == "measured" else
-                                   "of fallback 1.7 PFLOP/s sustained",
-                    "ffn_ms_mean": round(float(np.mean(ffn_ms)), 4), "ffn_tflop": round(ffn_flops / 1e12, 4),
+                    "frac": round(achieved / peak, 4),
+                    "traffic": args.traffic if (args.traffic is not None and name == args.workload) else None,
+                    "peak_source": ("of measured (MEASURED_PEAKS.json bf16_tflops, burst: the FFN graph is timed "
+                                    "alone; fp16 has the same nominal dense rate as bf16)")
+                                   if peak_src == "measured" else "of fallback 1.9 PFLOP/s burst",
+                    "frac_of_sustained": round(achieved / float(peaks.get("bf16_tflops_sustained", peak)), 4),
+                    "ffn_ms_mean": round(ffn_ms_call, 4), "ffn_tflop": round(ffn_flops / 1e12, 4),
                     "unique_experts_mean": round(float(np.mean(n_act)) + 1, 2),
-                    "timed_region": "CUDA events around replays of a graph of expert-FFN calls over the layer sets (mean per call)"}
+                    "timed_region": "CUDA events around replays of a graph of expert-FFN calls (mean per call, "
+                                    "slowest rank)"}
+        roofline["step_tflops"] = round((ffn_flops + 2.0 * T * cfg.n_experts * H) / (ms / K / 1e3) / 1e12, 1)
 
-    # ---------------- end to end: pinned host input -> graph -> pinned host output, synced per step
-    e2e = None
-    if not args.no_e2e:
-        e2e = run_e2e(args, wl, xs, stream, device, tokens_per_step, world)
-
-    out = {
+    rec = {
         "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world, "steps": K, "warmup": W,
         "ms_per_step": round(ms / K, 6), "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-        "dtype": "u4 weights x bf16 activations, fp32 accumulate", "data": "synthetic (seeded generators; "
-        "random-init weights quantized to the library's 4-bit group format)",
-        "config": {"workload": args.workload, "note": cfg.note, "tokens_per_step": T,
-                   "layers_per_step": wl.layers_per_step, "hidden": H, "inter": cfg.inter,
-                   "experts": cfg.n_experts, "top_k": k, "group": cfg.group,
-                   "l2": f"inputs larger than L2: {wl.n_sets} distinct layer weight sets rotated "
-                         f"({wl.n_sets * (cfg.n_experts + 1) * wl.expert_payload / 1e9:.1f} GB)",
-                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
-                   "launch": "CUDA graph of captured steps"},
-        "gpu_launches": None, "roofline": roofline, "clocks": clocks, "e2e": e2e,
+        "dtype": DTYPE_PREFILL if prefill else (DTYPE_DECODE if fp8 else DTYPE_DECODE_FP16),
+        "data": "synthetic (seeded generators; random-init weights quantized to the library's 4-bit group format)",
+        "config": workload_config(name, wl.n_sets, world),
+        "gpu_launches": None, "roofline": roofline, "clocks": clocks, "e2e": None,
     }
     launches_per_layer = 2 + (1 if T * k <= 1024 else 3) + (3 if prefill else 2) + 1
-    out["gpu_launches"] = launches_per_layer * wl.layers_per_step * K
-    if rank == 0 and not args.no_cpu_baseline:
-        out["cpu_baseline"] = cpu_baseline(args, wl, device)
+    rec["gpu_launches"] = launches_per_layer * wl.layers_per_step * K
+    if not args.no_e2e:
+        rec["e2e"] = run_e2e(wl, xs, stream, device, tokens_per_step, world, max(3, min(K, args.e2e_steps)))
+    if rank == 0 and cpu_leg and not args.no_cpu_baseline:
+        rec["cpu_baseline"] = cpu_baseline(name, wl, device)
+    rec["build_s"] = round(wl.build_s, 1)
+    del g_full, g_rem
+    wl.sets.clear()
+    return rec
+
+
+def run_ours(args, rank, local_rank, world):
+    import torch
+    device = torch.device(f"cuda:{local_rank}")
+    torch.cuda.set_device(device)
+    from quantized_routed_expert_03_gb300 import build as qbuild
+    qbuild.build()
+    import quantized_routed_expert_03_gb300 as qre
+    qre.load_library()
+    log = (lambda *a: print(*a, file=sys.stderr, flush=True)) if rank == 0 else (lambda *a: None)
+
+    out = measure_workload(args.workload, args, args.steps, args.warmup, rank, local_rank, world, device, log)
+    torch.cuda.empty_cache()
+    also = [w for w in (args.also.split(",") if args.also else []) if w and w != args.workload]
+    if also:
+        out["workloads"] = {}
+    for name in also:
+        cfg = synthetic.CONFIGS[name]
+        # each extra workload: a few steps of its own, sized to seconds of timed work
+        K = max(3, min(args.steps, 10 if cfg.tokens > 8 else (20 if cfg.layers > 1 else args.steps)))
+        rec = measure_workload(name, args, K, max(3, min(args.warmup, 5)), rank, local_rank, world, device, log)
+        for key in ("metric", "unit", "n_gpus", "higher_is_better", "scaling", "vs_baseline", "data"):
+            rec.pop(key, None)
+        out["workloads"][name] = rec
+        torch.cuda.empty_cache()
     return out
 
 
-def run_e2e(args, wl, xs, stream, device, tokens_per_step, world):
+def run_e2e(wl, xs, stream, device, tokens_per_step, world, K):
     import torch
     T, H = wl.T, wl.cfg.hidden
     stack = wl.layers_per_step > 1
     sets = wl.sets
     xin_dev = [torch.empty((T, H), dtype=torch.bfloat16, device=device) for _ in sets]
     graphs = []
+
     # one graph per layer set (single-layer workloads) or one for the whole stack
     def body(idx):
         s = sets[idx]
@@ -436,7 +503,6 @@ def run_e2e(args, wl, xs, stream, device, tokens_per_step, world):
     n_x = xs[0].shape[0]
     host_x = [xs[r].cpu().pin_memory() for r in range(len(sets))]
     host_y = [torch.empty((T, H), dtype=torch.bfloat16).pin_memory() for _ in sets]
-    K = min(args.steps, args.e2e_steps)
     h2d = (len(sets) if stack else 1) * T * H * 2
     d2h = h2d
 
@@ -494,7 +560,11 @@ def _oracle_expert_source(cfg, layer, device):
     return get
 
 
-def cpu_baseline(args, wl, device):
+def _blas_note() -> str:
+    return f"numpy BLAS threads {os.environ.get('OPENBLAS_NUM_THREADS')} (OPENBLAS/OMP/MKL_NUM_THREADS)"
+
+
+def cpu_baseline(name, wl, device):
     """The oracle timed on this host's cores for one full layer-token of the workload."""
     from oracle import moe as omoe
     cfg = wl.cfg
@@ -518,9 +588,9 @@ def cpu_baseline(args, wl, device):
                        cfg.top_k, cfg.group)
         dt += time.perf_counter() - t0
         reps += 1
-    return {"value": round(reps / dt, 5), "unit": UNIT, "cores": len(os.sched_getaffinity(0)), "kind": "oracle",
-            "sample": f"1 token through 1 layer of {args.workload} (route + {len(need)} experts dequantized "
-                      f"and applied in fp64 numpy), evaluated {reps} times; {dt:.1f} s"}
+    return {"value": round(reps / dt, 5), "unit": UNIT, "cores": _NCPU, "kind": "oracle",
+            "sample": f"1 token through 1 layer of {name} (route + {len(need)} experts dequantized "
+                      f"and applied in fp64 numpy), evaluated {reps} times; {dt:.1f} s; {_blas_note()}"}
 
 
 def run_reference(args):
@@ -578,13 +648,14 @@ def run_reference(args):
     tokens = args.steps * m / blocks_per_token * (cfg.tokens if cfg.layers == 1 else 1)
     value = tokens / dt
     sample = (f"per step: route 1 token + {m} of the {blocks_per_token} 16-feature FFN blocks of a "
-              f"{args.workload} layer-token (fp64 numpy oracle); scaled to layer-tokens")
+              f"{args.workload} layer-token (fp64 numpy oracle); scaled to layer-tokens; {_blas_note()}")
+    n_sets = args.sets if args.sets is not None else default_sets(cfg)
     return {"metric": METRIC, "value": round(value, 6), "unit": UNIT, "n_gpus": 1, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": round(dt / args.steps * 1e3, 3), "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": {"workload": args.workload, "note": cfg.note}, "impl": "reference",
-            "cpu_baseline": {"value": round(value, 6), "unit": UNIT, "cores": len(os.sched_getaffinity(0)),
-                             "kind": "oracle", "sample": sample},
+            "config": workload_config(args.workload, n_sets, 1), "impl": "reference",
+            "cpu_baseline": {"value": round(value, 6), "unit": UNIT, "cores": _NCPU, "kind": "oracle",
+                             "sample": sample},
             "e2e": {"value": round(value, 6), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
 
 
@@ -595,6 +666,9 @@ def main():
     ap.add_argument("--warmup", type=int, default=64)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="decode1", choices=sorted(synthetic.CONFIGS))
+    ap.add_argument("--also", default="prefill8192",
+                    help="comma-separated workloads measured after the main one, reported under 'workloads' "
+                         "('' for none)")
     ap.add_argument("--e2e-steps", type=int, default=5000)
     ap.add_argument("--sets", type=int, default=None,
                     help="distinct layer weight sets to rotate over (default: enough to exceed L2)")
@@ -606,6 +680,8 @@ def main():
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
+    if args.steps < 1:
+        ap.error("--steps must be >= 1")
     rank, local_rank, world = dist_env()
     if args.impl == "reference":
         if rank == 0:

@@ -194,7 +194,11 @@ QRE_API qre_status qre_route(const qre_layer_shape* shape, int32_t T, const uint
  *   by every GPU that loads it until the process exits; T * n_experts must be at
  *   most 65,536 (QRE_ERR_UNSUPPORTED otherwise, nothing launched).
  *   The first call on each device looks up the array's device address with that
- *   device current; make that first call before any stream capture.
+ *   device current; make that first call before any stream capture.  The
+ *   address is kept for the life of the process: after cudaDeviceReset (or
+ *   anything else that destroys the device's primary context) it no longer
+ *   names the array, so do not call qre_route_noalloc on that device again in
+ *   the same process.
  *   Every call shares the array: calls whose kernels may overlap on the GPU race
  *   and give wrong results; keep them on one stream or otherwise ordered.
  *   Nothing in the array has to start at zero.  No cudaMalloc, cudaFree or
@@ -288,6 +292,10 @@ QRE_API qre_status qre_combine(const qre_layer_shape* shape, int32_t T, const fl
  * Misses are handled in ascending expert id; the victim is the candidate slot
  * with the lowest score of its current expert (empty slots first), ties to the
  * lowest slot index; a miss with no candidate stays host-resident this call.
+ * A call admits at most max_copies experts: once the copy list is full, the
+ * remaining misses of the call also stay host-resident (their table entries
+ * unchanged), so every slot the table points at holds its expert's weights
+ * after qre_cache_copy.
  */
 QRE_API qre_status qre_cache_update(const qre_layer_shape* shape, int32_t n_slots, float decay,
                                     const int32_t* active, const int32_t* n_active, float* scores,

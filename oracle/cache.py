@@ -22,7 +22,11 @@ Readings (the recipe states the rule in one sentence):
     the miss is served from host memory and nothing is admitted ("bypass");
   * LRU and Belady use the same candidate rule with their own victim key
     (oldest last use; farthest next use, never-again = +inf), ties to the
-    lowest slot index.
+    lowest slot index;
+  * the recipe's copy kernel moves the admitted experts of a call into their
+    slots; a call admits at most ``max_admit`` experts (the capacity of its copy
+    list), and a miss beyond that is served from host memory like a bypass, with
+    the cache left as it was for that expert.
 """
 
 from __future__ import annotations
@@ -35,11 +39,12 @@ def _calls(trace):
 
 
 def lfu_replay(trace, n_experts: int, static, n_slots: int, decay: float = 0.995, init_slots=None,
-               init_scores=None) -> dict:
+               init_scores=None, max_admit=None) -> dict:
     """LFU with multiplicative decay (fp32), the recipe's dynamic cache.
 
     Returns per-call lists of (expert, slot, evicted_expert) admissions, the
-    bypassed misses, the final slot contents and scores.
+    bypassed misses, the final slot contents and scores.  ``max_admit`` (None =
+    unlimited) caps the admissions of one call.
     """
     static = set(int(e) for e in static)
     slot_expert = [-1] * n_slots if init_slots is None else [int(e) for e in init_slots]
@@ -60,6 +65,9 @@ def lfu_replay(trace, n_experts: int, static, n_slots: int, decay: float = 0.995
             if e in static or e in where:
                 continue
             misses += 1
+            if max_admit is not None and len(adm) >= max_admit:
+                byp.append(e)
+                continue
             best = None
             for s, cur in enumerate(slot_expert):
                 if cur in used:
@@ -84,16 +92,20 @@ def lfu_replay(trace, n_experts: int, static, n_slots: int, decay: float = 0.995
 
 
 def lru_replay(trace, static, n_slots: int, init_slots=None) -> dict:
+    """Least recently used: a miss evicts the candidate expert whose last use is
+    oldest (an expert preloaded by ``init_slots`` and never used counts as used
+    before the first call).  Returns per-call (expert, slot, evicted_expert)
+    admissions, the misses and the final slot contents."""
     static = set(int(e) for e in static)
     slot_expert = [-1] * n_slots if init_slots is None else [int(e) for e in init_slots]
     last = {}
     misses = 0
+    admitted = []
     for i, call in enumerate(_calls(trace)):
         used = set(call)
+        adm = []
         for e in call:
-            if e in static:
-                continue
-            if e in slot_expert:
+            if e in static or e in slot_expert:
                 continue
             misses += 1
             best = None
@@ -104,14 +116,18 @@ def lru_replay(trace, static, n_slots: int, init_slots=None) -> dict:
                 if best is None or key < best[0]:
                     best = (key, s)
             if best is not None:
+                adm.append((e, best[1], slot_expert[best[1]]))
                 slot_expert[best[1]] = e
         for e in call:
             last[e] = i
-    return {"misses": misses, "slot_expert": slot_expert}
+        admitted.append(adm)
+    return {"misses": misses, "slot_expert": slot_expert, "admitted": admitted}
 
 
 def belady_replay(trace, static, n_slots: int, init_slots=None) -> dict:
-    """Offline optimum (evict the expert whose next use is farthest away)."""
+    """Offline optimum: a miss evicts the candidate expert whose next use lies
+    farthest ahead (never again = +inf; an empty slot also counts as +inf).
+    Returns per-call admissions, the misses and the final slot contents."""
     static = set(int(e) for e in static)
     calls = _calls(trace)
     slot_expert = [-1] * n_slots if init_slots is None else [int(e) for e in init_slots]
@@ -121,8 +137,10 @@ def belady_replay(trace, static, n_slots: int, init_slots=None) -> dict:
             uses.setdefault(e, []).append(i)
     ptr = {e: 0 for e in uses}
     misses = 0
+    admitted = []
     for i, call in enumerate(calls):
         used = set(call)
+        adm = []
         for e in call:
             ptr[e] += 1          # the use at call i is consumed
         for e in call:
@@ -142,8 +160,10 @@ def belady_replay(trace, static, n_slots: int, init_slots=None) -> dict:
                 if best is None or key > best[0]:
                     best = (key, s)
             if best is not None:
+                adm.append((e, best[1], slot_expert[best[1]]))
                 slot_expert[best[1]] = e
-    return {"misses": misses, "slot_expert": slot_expert}
+        admitted.append(adm)
+    return {"misses": misses, "slot_expert": slot_expert, "admitted": admitted}
 
 
 def static_replay(trace, resident) -> dict:

@@ -20,7 +20,9 @@
 //     miss stays host-resident for this call;
 //   * the admitted expert's table entry points at its slot (tier 0), the evicted
 //     expert's entry at its home copy (tier 1), and (expert, slot) is appended
-//     to the copy list.
+//     to the copy list;
+//   * a call admits at most max_copies experts (the copy list's capacity): a
+//     later miss of the same call stays host-resident, its table entry unchanged.
 #include "common.cuh"
 #include "internal.h"
 
@@ -64,8 +66,9 @@ __global__ void __launch_bounds__(kCacheThreads) cache_update_kernel(
     scores[e] = s;
   }
   __syncthreads();
-  // misses in ascending expert id (active is ascending)
+  // misses in ascending expert id (active is ascending), until the copy list is full
   for (int i = 0; i < na; ++i) {
+    if (n_adm >= max_copies) break;   // shared, written by thread 0 before the last barrier
     const int e = active[i];
     if (e < 0 || e >= E || expert_slot[e] != -1) continue;  // hit, static or bad id
     KeySlot best{INFINITY, 0x7fffffff};
@@ -95,16 +98,14 @@ __global__ void __launch_bounds__(kCacheThreads) cache_update_kernel(
         slot_expert[s] = e;
         expert_slot[e] = s;
         table[e] = slot_mem[s];
-        if (n_adm < max_copies) {
-          copy_list[2 * n_adm] = e;
-          copy_list[2 * n_adm + 1] = s;
-        }
+        copy_list[2 * n_adm] = e;
+        copy_list[2 * n_adm + 1] = s;
         ++n_adm;
       }
     }
     __syncthreads();
   }
-  if (tid == 0) *n_copies = n_adm < max_copies ? n_adm : max_copies;
+  if (tid == 0) *n_copies = n_adm;
 }
 
 // Copies the admitted experts' four arrays from their home copies (pinned host

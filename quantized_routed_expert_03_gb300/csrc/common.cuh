@@ -1,7 +1,8 @@
 // common.cuh -- device helpers shared by the library's kernels (sm_103a).
 //
-// Inline PTX for mbarriers, bulk (TMA) copies, the warp-level f16 tensor-core
-// MMA, the global timer used to bound every wait, and the device status word.
+// Inline PTX for mbarriers, cp.async copies, programmatic launch control, the
+// 4-bit decodes, the global timer used to bound every wait, and the device
+// status word.
 #pragma once
 
 #include <cuda_runtime.h>

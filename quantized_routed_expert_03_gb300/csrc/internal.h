@@ -10,7 +10,8 @@
 namespace qre {
 
 // Largest token count the bandwidth-bound decode FFN handles in one pass: the
-// tokens are the N = 8 side of the m16n8k16 tensor-core tile.
+// tokens (as E4M3 terms or fp16 parts) are the N side of its tcgen05 MMAs, at
+// most 32 B-operand rows.
 constexpr int kDecodeMaxTokens = 8;
 
 // Bytes of each workspace region for a call with T tokens (each call uses its

@@ -12,7 +12,9 @@
 // GPU (for example on two streams without an ordering between them) race on it;
 // calls on one stream, or otherwise ordered, are safe.  Nothing in it has to
 // start at zero: every logit the selection reads is written first by the same
-// call.
+// call.  The array's device address is looked up once per device and kept; a
+// device reset that destroys the primary context leaves it stale, so the entry
+// point must not be called on that device again in the same process.
 #include <cstdio>
 #include <mutex>
 

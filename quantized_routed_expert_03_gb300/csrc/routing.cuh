@@ -1,6 +1,6 @@
-// routing.cuh -- device building blocks of the router and the dispatch, shared
-// by their separate kernels and by the fused decode kernel that runs both in
-// one launch (route.cu).
+// routing.cuh -- device building blocks of the router (route.cu) and the
+// dispatch (dispatch.cu): the logits GEMV, the per-token warp selection and the
+// one-block dispatch.
 #pragma once
 #include "common.cuh"
 

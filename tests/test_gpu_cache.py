@@ -45,7 +45,11 @@ def _zipf_trace(n_calls, T, E, k, ranks, seed):
     return trace
 
 
-def test_cache_manager_matches_policy_replay():
+@pytest.mark.parametrize("max_copies", [64, 2])
+def test_cache_manager_matches_policy_replay(max_copies):
+    """Admissions, copy list, slots, scores and the slot table equal the LFU
+    replay call by call; with a copy list of 2 entries the calls with more
+    misses admit two and leave the rest on the host tier."""
     E, k, S, n_static = 288, 8, 148, 40
     shape = qre.make_shape(4096, 2048, E, k, 128)
     ranks = synthetic.popularity_ranks(E, seed=0, layer=5)
@@ -68,13 +72,15 @@ def test_cache_manager_matches_policy_replay():
     d_es = torch.from_numpy(expert_slot).to(DEV)
     d_se = torch.tensor(init_slots, dtype=torch.int32, device=DEV)
     d_scores = torch.zeros(E, dtype=torch.float32, device=DEV)
-    max_copies = 64
     d_list = torch.full((2 * max_copies,), -1, dtype=torch.int32, device=DEV)
     d_n = torch.zeros(4, dtype=torch.int32, device=DEV)
     d_active = torch.zeros(E, dtype=torch.int32, device=DEV)
     d_nact = torch.zeros(4, dtype=torch.int32, device=DEV)
 
-    ref = ocache.lfu_replay(trace, E, static, S, decay=0.995, init_slots=init_slots)
+    ref = ocache.lfu_replay(trace, E, static, S, decay=0.995, init_slots=init_slots, max_admit=max_copies)
+    capped = sum(1 for adm, byp in zip(ref["admitted"], ref["bypassed"]) if len(adm) == max_copies and byp)
+    if max_copies == 2:
+        assert capped > 0, "the trace must exercise the admission cap"
     for call, adm in zip(trace, ref["admitted"]):
         d_active[:len(call)] = torch.tensor(call, dtype=torch.int32)
         d_nact[0] = len(call)
@@ -157,8 +163,11 @@ def test_cache_copy_moves_the_admitted_experts():
             assert torch.equal(slots.view(int(s), name).cpu(), home.view(int(e), name).cpu())
 
 
-@pytest.mark.parametrize("T", [1, 4])
-def test_decode_with_live_cache_is_bit_identical_to_hbm(T):
+@pytest.mark.parametrize("T,max_copies", [(1, 64), (4, 64), (4, 1)])
+def test_decode_with_live_cache_is_bit_identical_to_hbm(T, max_copies):
+    """A decode loop whose slot table the cache manager rewrites every step gives
+    the same bits as all experts in device memory, also when a step has more
+    misses than its copy list holds (max_copies = 1)."""
     cfg = synthetic.LayerConfig("mid", 512, 256, 32, 4, 128, T)
     S = 6
     live, ref, st, _ = _build_cached_layer(cfg, n_static=4, S=S, T=T)
@@ -170,13 +179,15 @@ def test_decode_with_live_cache_is_bit_identical_to_hbm(T):
         live.dispatch(T)
         qre.qre_cache_update(live.shape, S, 0.995, live.active, live.n_active, st["scores"], st["expert_slot"],
                              st["slot_expert"], st["home"], st["slot_mem"], live.slots, st["copy_list"],
-                             st["n_copies"], 64)
-        qre.qre_cache_copy(live.shape, st["home"], st["slot_mem"], st["copy_list"], st["n_copies"], 64)
+                             st["n_copies"], max_copies)
+        qre.qre_cache_copy(live.shape, st["home"], st["slot_mem"], st["copy_list"], st["n_copies"], max_copies)
         live.expert_ffn(x, T)
         live.combine(T)
         ref.forward(x, wr, None, T)
         torch.cuda.synchronize()
-        admitted += int(st["n_copies"][0].item())
+        n = int(st["n_copies"][0].item())
+        assert n <= max_copies
+        admitted += n
         assert torch.equal(live.y[:T], ref.y[:T]), f"step {step}"
     assert admitted > 0
     assert qre.qre_read_device_status() == 0

@@ -2,10 +2,12 @@
 
 Tolerances (derived from the arithmetic; the layer-level bar of the pages is
 1e-3 relative RMS, the error class of their own expert kernels):
-  * decode path (T <= 8): products of exact 4-bit codes and fp16 activations are
-    exact, accumulation is fp32, h enters the down projection as an fp16 pair
-    (high + remainder, ~2^-22 relative).  Expected error is a few 1e-7; the test
-    bound is 1e-5 relative RMS per output row and per layer output.
+  * decode path (T <= 8), group 128: the 4-bit codes are exact E4M3 values, x
+    enters as two E4M3 terms (exact for bf16 above 2^-13 of its group's
+    largest), h as four (~16 significant bits); products are exact and the
+    accumulation is fp32.  Groups 32 and 64: exact fp16 codes times x and h as
+    fp16 high part + remainder.  Expected error is below 1e-6; the test bound is
+    1e-5 relative RMS per output row and per layer output.
   * the bf16 output must equal round-to-nearest-even of the fp32 output exactly.
 """
 
@@ -218,8 +220,9 @@ def test_full_size_decode_one_token():
 def test_full_size_decode_eight_tokens_zipf():
     """One layer of the 42-layer skewed-routing stack: T = 8, Zipf(1.1) bias.
 
-    Routing and dispatch are checked for all 8 tokens; the FFN outputs for two
-    tokens (the oracle dequantizes every expert it touches, ~3 s each)."""
+    Routing, dispatch, every expert_out row and the layer output are checked for
+    all 8 tokens: the active set of about 50 experts is the largest grid the
+    decode kernels see (the oracle dequantizes each expert once)."""
     cfg = synthetic.CONFIGS["decode8_zipf_x42"]
     layer = 17
     host_src, dev_src = torch_sources(cfg, layer, DEV)
@@ -228,8 +231,8 @@ def test_full_size_decode_eight_tokens_zipf():
     bias = synthetic.zipf_bias(cfg.n_experts, cfg.seed, layer)
     x_bits, wr, _ = _inputs(cfg, 8, layer=layer)
     got = _run(built, x_bits, wr, bias)
-    toks = [0, 5]
-    _check_layer(built, got, built.oracle_layer(x_bits, wr, bias, tokens=toks), tokens=toks)
+    assert got["n_active"] >= 40
+    _check_layer(built, got, built.oracle_layer(x_bits, wr, bias))
 
 
 @pytest.mark.slow

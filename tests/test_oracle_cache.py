@@ -82,3 +82,80 @@ def test_infinite_cache_misses_once_per_expert():
     assert ocache.lfu_replay(trace, 64, [], 64)["misses"] == first
     assert ocache.lru_replay(trace, [], 64)["misses"] == first
     assert ocache.belady_replay(trace, [], 64)["misses"] == first
+
+
+def test_lfu_admission_cap_hand_derived():
+    """At most max_admit admissions per call; later misses of the call stay on the host tier."""
+    fx = _fx()
+    c = fx["capped"]
+    r = ocache.lfu_replay(fx["trace"], 6, fx["static"], fx["n_slots"], decay=fx["decay"], max_admit=c["max_admit"])
+    assert [[list(a) for a in call] for call in r["admitted"]] == c["admitted"]
+    assert r["bypassed"] == c["bypassed"]
+    assert r["slot_expert"] == c["final_slots"]
+    np.testing.assert_array_equal(r["scores"], np.array(c["final_scores"], np.float32))
+    assert r["misses"] == c["misses"]
+
+
+def _pol():
+    with open(os.path.join(GOLDEN, "cache_policies_tiny.json")) as f:
+        return json.load(f)
+
+
+def test_lru_hand_derived_trace():
+    fx = _pol()["lru"]
+    r = ocache.lru_replay(fx["trace"], [], fx["n_slots"])
+    assert [[list(a) for a in call] for call in r["admitted"]] == fx["admitted"]
+    assert r["slot_expert"] == fx["final_slots"]
+    assert r["misses"] == fx["misses"]
+
+
+def test_belady_hand_derived_trace():
+    fx = _pol()["belady"]
+    r = ocache.belady_replay(fx["trace"], [], fx["n_slots"])
+    assert [[list(a) for a in call] for call in r["admitted"]] == fx["admitted"]
+    assert r["slot_expert"] == fx["final_slots"]
+    assert r["misses"] == fx["misses"]
+    assert ocache.lru_replay(fx["trace"], [], fx["n_slots"])["misses"] == fx["lru_misses"]
+
+
+def test_belady_brute_force_optimum_on_tiny_traces():
+    """Belady's miss count is the minimum over every eviction choice (exhaustive
+    search on short random traces with one expert per call)."""
+    rng = np.random.default_rng(11)
+
+    def best(trace, slots, i=0):
+        if i == len(trace):
+            return 0
+        e = trace[i]
+        if e in slots:
+            return best(trace, slots, i + 1)
+        if len(slots) < 2:
+            return 1 + best(trace, slots | {e}, i + 1)
+        return 1 + min(best(trace, (slots - {v}) | {e}, i + 1) for v in slots)
+
+    for _ in range(30):
+        trace = [int(v) for v in rng.integers(0, 5, size=9)]
+        got = ocache.belady_replay([[e] for e in trace], [], 2)["misses"]
+        assert got == best(trace, frozenset())
+
+
+def test_policy_report_is_reproducible_and_consistent():
+    """tests/golden/policy_misses.json: a recomputed slice equals the stored one,
+    Belady is the lowest of the four everywhere, and the per-token figures follow
+    from the counts."""
+    import importlib.util
+    spec = importlib.util.spec_from_file_location("make_policy_misses", os.path.join(GOLDEN, "make_policy_misses.py"))
+    mod = importlib.util.module_from_spec(spec)
+    spec.loader.exec_module(mod)
+    with open(os.path.join(GOLDEN, "policy_misses.json")) as f:
+        rep = json.load(f)
+    for name in mod.WORKLOADS:
+        assert mod.policy_misses(name, range(2), 16)["per_layer"] == rep["check"][name]
+        w = rep["workloads"][name]
+        assert w["layers"] == 42 and len(w["per_layer"]) == 42
+        for layer in w["per_layer"]:
+            for pol in ("static", "lru", "lfu_0.995"):
+                assert layer["belady"] <= layer[pol]
+        for pol, v in w["policies"].items():
+            assert v["misses"] == sum(layer[pol] for layer in w["per_layer"])
+            assert v["misses_per_token"] == pytest.approx(v["misses"] / (w["steps"] * w["tokens_per_step"]), abs=1e-3)

@@ -322,6 +322,25 @@ QRE_API qre_status qre_cache_copy(const qre_layer_shape* shape, const qre_slot* 
 QRE_API qre_status qre_validate_slots(const qre_layer_shape* shape, const qre_slot* host_slots);
 
 /*
+ * Test hook for the bounded waits' give-up path (failure handling without a
+ * GPU fault).  Every kernel of this library bounds its pipeline waits; one that
+ * runs out of time sets QRE_DEV_TIMEOUT, makes the CTA's other waits give up,
+ * lets the tensor core finish what was issued, frees its tensor memory and
+ * returns, so the context stays usable and the next call is unaffected.
+ *   wait_limit_ns  limit of the pipeline waits of later launches (process-wide),
+ *                  0 restores the default of one second; at most one second.
+ *   stall_ns       when non-zero, later expert-FFN launches delay one warp of
+ *                  one CTA (the decode kernels: the CTA that owns the first
+ *                  unit of work; the grouped GEMM: CTA 0's token loads) by this
+ *                  long before it signals its first pipeline stage (at most
+ *                  100 ms), so that a wait with a shorter limit runs out; 0
+ *                  turns it off.
+ * Results of calls made while a wait runs out are invalid.  Not for production
+ * use; a CUDA graph keeps the values in force when it was captured.
+ */
+QRE_API qre_status qre_debug_wait_test(uint64_t wait_limit_ns, uint64_t stall_ns);
+
+/*
  * Synchronizes the stream, then writes the current device's status word
  * (QRE_DEV_* bits, 0 = clean) to *status (host).  qre_clear_device_status
  * resets it to 0 (also synchronizing the stream).

@@ -40,7 +40,7 @@ EXPORTS = (
     "qre_quantize_gate_up",
     "qre_route", "qre_dispatch", "qre_expert_ffn", "qre_combine", "qre_validate_slots",
     "qre_cache_update", "qre_cache_copy",
-    "qre_read_device_status", "qre_clear_device_status", "qre_route_noalloc",
+    "qre_read_device_status", "qre_clear_device_status", "qre_route_noalloc", "qre_debug_wait_test",
 )
 
 
@@ -85,6 +85,7 @@ _SIGS = {
     "qre_read_device_status": ([_VP, ctypes.POINTER(ctypes.c_int32)], ctypes.c_int),
     "qre_clear_device_status": ([_VP], ctypes.c_int),
     "qre_route_noalloc": ([_SHAPE, _I32, _VP, _VP, _VP, _VP, _VP, _VP], ctypes.c_int),
+    "qre_debug_wait_test": ([ctypes.c_uint64, ctypes.c_uint64], ctypes.c_int),
 }
 
 
@@ -218,6 +219,12 @@ def qre_cache_copy(shape, home, slot_mem, copy_list, n_copies, max_copies, strea
 def qre_validate_slots(shape, host_slots) -> None:
     """host_slots: a ctypes array of qre_slot (n_experts + 1 entries) in host memory."""
     _check(load_library().qre_validate_slots(ctypes.byref(shape), host_slots), "qre_validate_slots")
+
+
+def qre_debug_wait_test(wait_limit_ns: int, stall_ns: int) -> None:
+    """Test hook: lower the kernels' wait limit and delay one warp of the expert
+    FFN's first CTA, so that the give-up path runs (0, 0 restores the defaults)."""
+    _check(load_library().qre_debug_wait_test(wait_limit_ns, stall_ns), "qre_debug_wait_test")
 
 
 def qre_read_device_status(stream=None) -> int:

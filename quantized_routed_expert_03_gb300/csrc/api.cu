@@ -1,5 +1,6 @@
 // api.cu -- the C ABI: argument validation, workspace sizing, error reporting,
 // the device status word, and dispatch to the kernel launchers.
+#include <atomic>
 #include <cstdarg>
 #include <cstdio>
 #include <cstring>
@@ -29,6 +30,7 @@ qre_status cuda_fail(cudaError_t e, const char* what) {
 bool misaligned(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) != 0; }
 
 constexpr int kMaxDevices = 64;
+constexpr uint64_t kMaxTestStallNs = 100000000ull;   // 100 ms
 
 }  // namespace
 
@@ -36,6 +38,14 @@ constexpr int kMaxDevices = 64;
 __device__ int g_qre_device_status;
 
 namespace qre {
+
+namespace {
+std::atomic<uint64_t> g_wait_limit_ns{kWaitLimitNs};
+std::atomic<uint64_t> g_test_stall_ns{0};
+}  // namespace
+
+uint64_t wait_limit_ns() { return g_wait_limit_ns.load(std::memory_order_relaxed); }
+uint64_t test_stall_ns() { return g_test_stall_ns.load(std::memory_order_relaxed); }
 
 void set_error_message(const char* fmt, ...) {
   va_list ap;
@@ -362,6 +372,19 @@ qre_status qre_validate_slots(const qre_layer_shape* shape, const qre_slot* host
         return fail(QRE_ERR_INVALID_ARG, "slot %d: %s has tier 1 but is not device-mapped host memory", e, names[i]);
     }
   }
+  g_err[0] = '\0';
+  return QRE_OK;
+}
+
+qre_status qre_debug_wait_test(uint64_t wait_limit_ns, uint64_t stall_ns) {
+  if (wait_limit_ns > qre::kWaitLimitNs)
+    return fail(QRE_ERR_INVALID_ARG, "wait_limit_ns %llu is above the default of %llu",
+                (unsigned long long)wait_limit_ns, (unsigned long long)qre::kWaitLimitNs);
+  if (stall_ns > kMaxTestStallNs)
+    return fail(QRE_ERR_INVALID_ARG, "stall_ns %llu is above %llu", (unsigned long long)stall_ns,
+                (unsigned long long)kMaxTestStallNs);
+  qre::g_wait_limit_ns.store(wait_limit_ns ? wait_limit_ns : qre::kWaitLimitNs, std::memory_order_relaxed);
+  qre::g_test_stall_ns.store(stall_ns, std::memory_order_relaxed);
   g_err[0] = '\0';
   return QRE_OK;
 }

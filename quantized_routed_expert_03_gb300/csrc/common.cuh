@@ -14,8 +14,11 @@
 
 namespace qre {
 
-// Every spin-wait in this library gives up after this many nanoseconds, records
-// QRE_DEV_TIMEOUT in the status word and lets the kernel finish.
+// Every spin-wait in this library gives up after a limit, records
+// QRE_DEV_TIMEOUT in the status word and lets the kernel finish.  The pipeline
+// waits take the limit as a kernel parameter (this value unless a test lowers
+// it, qre_debug_wait_test); the waits that must end before tensor memory is
+// freed always use this value.
 constexpr uint64_t kWaitLimitNs = 1000000000ull;
 
 __device__ __forceinline__ uint64_t global_timer_ns() {
@@ -64,19 +67,33 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   return done != 0;
 }
 
-// Waits for the phase of `bar` with the given parity, for at most kWaitLimitNs
+// Waits for the phase of `bar` with the given parity, for at most limit_ns
 // from the first failed poll.  Gives up early when *abort is set by another
 // warp; on expiry sets *abort and QRE_DEV_TIMEOUT.  Returns true when the phase
 // completed.
 // The polling loop is out of line: the hot loops that wait on barriers keep
 // only the first poll and a call, which keeps their code small enough for the
 // instruction cache.
-static __device__ __noinline__ bool mbar_wait_slow(uint64_t* bar, uint32_t parity, volatile int* abort, int* status) {
-  const uint64_t deadline = global_timer_ns() + kWaitLimitNs;
-  uint32_t spins = 0;
-  while (!mbar_try_wait(bar, parity)) {
+// Each poll may suspend the thread until the phase completes or for at most
+// about 1 us (the suspend-time hint), so the deadline is checked at that
+// granularity whatever the hardware's own suspend limit is.
+__device__ __forceinline__ bool mbar_try_wait_1us(uint64_t* bar, uint32_t parity) {
+  uint32_t done;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(done)
+      : "r"(smem_addr(bar)), "r"(parity), "r"(1000u)
+      : "memory");
+  return done != 0;
+}
+static __device__ __noinline__ bool mbar_wait_slow(uint64_t* bar, uint32_t parity, volatile int* abort, int* status,
+                                                   uint64_t limit_ns) {
+  const uint64_t deadline = global_timer_ns() + limit_ns;
+  while (!mbar_try_wait_1us(bar, parity)) {
     if (abort && *abort) return false;
-    if ((++spins & 63u) == 0 && global_timer_ns() > deadline) {
+    if (global_timer_ns() > deadline) {
       if (abort) *abort = 1;
       set_status(status, QRE_DEV_TIMEOUT);
       return false;
@@ -84,9 +101,25 @@ static __device__ __noinline__ bool mbar_wait_slow(uint64_t* bar, uint32_t parit
   }
   return true;
 }
-__device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity, volatile int* abort, int* status) {
+__device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity, volatile int* abort, int* status,
+                                                  uint64_t limit_ns) {
   if (mbar_try_wait(bar, parity)) return true;
-  return mbar_wait_slow(bar, parity, abort, status);
+  return mbar_wait_slow(bar, parity, abort, status, limit_ns);
+}
+// The wait before tensor memory is freed or a kernel exits with copies in
+// flight: not cut short by the abort flag, and always the full kWaitLimitNs
+// (what it waits for, issued tensor-core work or bulk copies, completes on its
+// own).
+__device__ __forceinline__ bool mbar_wait_drain(uint64_t* bar, uint32_t parity, int* status) {
+  if (mbar_try_wait(bar, parity)) return true;
+  return mbar_wait_slow(bar, parity, nullptr, status, kWaitLimitNs);
+}
+
+// Test hook (qre_debug_wait_test): spins for ns nanoseconds of the global timer.
+static __device__ __noinline__ void debug_stall(uint64_t ns) {
+  const uint64_t end = global_timer_ns() + ns;
+  while (global_timer_ns() < end) {
+  }
 }
 
 // ---------------------------------------------------------------- async copies

@@ -92,6 +92,8 @@ struct FfnParams {
   __half* hbuf;       // [(amax+1)][2*kTok][I]: row 2n = h high part of token n, 2n+1 its remainder
   float* expert_out;  // [T*k + T][H]
   int* status;
+  uint64_t wait_ns;   // limit of the pipeline waits
+  uint64_t stall_ns;  // test hook: warp 1 of the CTA that owns unit 0 delays its first stage's signal
 };
 
 struct Layout {
@@ -103,8 +105,9 @@ __host__ __device__ inline Layout make_layout(int K, int nB, int TT) {
   Layout L;
   L.b_off = 0;                                          // nB x (BN x K fp16, swizzled; 1024-aligned)
   L.red_off = L.b_off + nB * K * BN * 2;                // 2 x kWG x BM x TT fp32
-  L.bar_off = L.red_off + 2 * kWG * BM * TT * 4;        // a_full[kWG][3], done[kWG][3], red_full[2], red_empty[2]
-  L.grp_off = L.bar_off + (kWG * 6 + 4) * 8;
+  L.bar_off = L.red_off + 2 * kWG * BM * TT * 4;        // a_full[kWG][3], done[kWG][3], red_full[2], red_empty[2],
+                                                        // drain[kThreads / 32]
+  L.grp_off = L.bar_off + (kWG * 6 + 4 + kThreads / 32) * 8;
   L.misc_off = L.grp_off + kMaxGroups * (int)sizeof(Group);
   L.bytes = (size_t)L.misc_off + 16 + 1024;             // + alignment slack
   return L;
@@ -146,11 +149,12 @@ __device__ __forceinline__ void load_h(uint8_t* dst, const __half* hbuf, int a, 
 template <int MODE, int TT, bool H32 = false>
 __device__ __noinline__ void finish_unit(int v, int ub, int upe, const Group* groups, const float* red,
                                          uint64_t* red_full, uint64_t* red_empty, int kq, int T, int I, int H,
-                                         __half* hbuf, float* expert_out, volatile int* abort_flag, int* status) {
+                                         __half* hbuf, float* expert_out, volatile int* abort_flag, int* status,
+                                         uint64_t wait_ns) {
   const int tid = threadIdx.x, lane = tid & 31, wg = tid >> 7, r = tid & 127;
   const int u = ub + v, a = u / upe, m0 = (u - a * upe) * BM;
   const Group& gr = groups[a];
-  mbar_wait_bounded(&red_full[v & 1], (v >> 1) & 1, abort_flag, status);
+  mbar_wait_bounded(&red_full[v & 1], (v >> 1) & 1, abort_flag, status, wait_ns);
   constexpr int NT = TT == 1 ? 1 : 2;   // tokens per thread
   const int n0 = TT == 1 ? 0 : 2 * wg;
   if ((TT > 1 || wg == 0) && (gr.flags & 1)) {
@@ -232,6 +236,7 @@ __global__ void __launch_bounds__(kThreads, 1) ffn_decode_kernel(const FfnParams
   uint64_t* done = a_full + kWG * 3;                                  // [kWG][3]: the stage's MMAs completed
   uint64_t* red_full = done + kWG * 3;                                // [2]: every partial of a unit written
   uint64_t* red_empty = red_full + 2;                                 // [2]: every epilogue of a unit read
+  uint64_t* drain = red_empty + 2;                                    // [warps]: a warp's MMAs completed
   Group* groups = reinterpret_cast<Group*>(smem + L.grp_off);
   uint32_t* tmem_base_p = reinterpret_cast<uint32_t*>(smem + L.misc_off);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L.misc_off + 4);
@@ -288,6 +293,7 @@ __global__ void __launch_bounds__(kThreads, 1) ffn_decode_kernel(const FfnParams
       mbar_init(&red_full[i], 128 * p.kq);
       mbar_init(&red_empty[i], kThreads);
     }
+    for (int i = 0; i < kThreads / 32; ++i) mbar_init(&drain[i], 1);
     *abort_flag = 0;
     fence_barrier_init();
   }
@@ -342,7 +348,7 @@ __global__ void __launch_bounds__(kThreads, 1) ffn_decode_kernel(const FfnParams
 
   auto epilogue = [&](int v) {
     finish_unit<MODE, TT>(v, ub, upe, groups, red, red_full, red_empty, p.kq, p.T, p.I, p.H, p.hbuf, p.expert_out,
-                          abort_flag, p.status);
+                          abort_flag, p.status, p.wait_ns);
   };
   int epi = -1;   // a unit whose epilogue is due (it runs after the current block of stages)
 
@@ -428,7 +434,7 @@ __global__ void __launch_bounds__(kThreads, 1) ffn_decode_kernel(const FfnParams
         }
       }
       if (est == nst - 1) {
-        if (eul >= 2) mbar_wait_bounded(&red_empty[eul & 1], ((eul >> 1) - 1) & 1, abort_flag, p.status);
+        if (eul >= 2) mbar_wait_bounded(&red_empty[eul & 1], ((eul >> 1) - 1) & 1, abort_flag, p.status, p.wait_ns);
         float* rw = red + ((size_t)((eul & 1) * kWG + wg) * BM + r) * TT;
 #pragma unroll
         for (int n = 0; n < TT; ++n) {
@@ -445,7 +451,7 @@ __global__ void __launch_bounds__(kThreads, 1) ffn_decode_kernel(const FfnParams
     // lane 0 of the issuing warp: the four MMAs of global stage i (odd: i is odd;
     // stage ist of local unit iul; A buffer ib, whose phases have parity iph)
     auto issue = [&](int i, bool odd, int ist, int iul, int ib, int iph) {
-      mbar_wait_bounded(&a_full[wg * 3 + ib], iph, abort_flag, p.status);
+      mbar_wait_bounded(&a_full[wg * 3 + ib], iph, abort_flag, p.status, p.wait_ns);
       tc_fence_after();
       const uint32_t bstage = bbase_of(iul) + (uint32_t)((k0 / SK + ist) * (BN * 128));
 #pragma unroll
@@ -474,7 +480,7 @@ __global__ void __launch_bounds__(kThreads, 1) ffn_decode_kernel(const FfnParams
           const uint32_t sp = (SEG == 128 && (j & 1)) ? h1 : sring[j];
           // (1) stage gs - NA completed: A buffer ab is free, its segments are readable
           if (gs >= NA) {
-            mbar_wait_bounded(&done[wg * 3 + ab], aph ^ 1, abort_flag, p.status);
+            mbar_wait_bounded(&done[wg * 3 + ab], aph ^ 1, abort_flag, p.status, p.wait_ns);
             __syncwarp();
             tc_fence_after();
           }
@@ -518,6 +524,7 @@ __global__ void __launch_bounds__(kThreads, 1) ffn_decode_kernel(const FfnParams
           tmem_st_wait();
           tc_fence_before();
           __syncwarp();
+          if (p.stall_ns && gs == 0 && ub == 0 && wg == 0 && wq == 1 && lane == 0) debug_stall(p.stall_ns);
           if (lane == 0) mbar_arrive(&a_full[wg * 3 + ab]);
           // (5) issue the previous stage if it is this warp's turn
           if (gs >= 1 && issuer(gs - 1) && lane == 0) {
@@ -553,7 +560,7 @@ __global__ void __launch_bounds__(kThreads, 1) ffn_decode_kernel(const FfnParams
         eb += NA;
         eph ^= 1;
       }
-      mbar_wait_bounded(&done[wg * 3 + eb], eph, abort_flag, p.status);
+      mbar_wait_bounded(&done[wg * 3 + eb], eph, abort_flag, p.status, p.wait_ns);
       __syncwarp();
       tc_fence_after();
       int est = st - back, eul = ul;
@@ -576,7 +583,17 @@ __global__ void __launch_bounds__(kThreads, 1) ffn_decode_kernel(const FfnParams
     for (int v = 0; v < NU; ++v) epilogue(v);
   }
 
+  // Every MMA must have completed before tensor memory is freed.  Without a
+  // give-up the waits above saw every stage complete; after one, each warp's
+  // issuing lane commits once more (tracking all its earlier MMAs) and waits.
   __syncthreads();
+  if (*abort_flag) {
+    if (lane == 0) {
+      umma_commit(&drain[warp]);
+      mbar_wait_drain(&drain[warp], 0, p.status);
+    }
+    __syncthreads();
+  }
   if (warp == 0) {
     tc_fence_after();
     tmem_dealloc(*tmem_base_p, kWG * kColsPerWG);
@@ -649,7 +666,7 @@ __host__ __device__ inline Layout8 make_layout8(int MODE, int K, int nB, int TT)
   L.ring_off = (L.ec_off + nB * 2 * TT * (K / SK8) * 4 + 127) & ~127;   // [stage][kWG] x 8 KB
   L.red_off = L.ring_off + ring8_stages(MODE, TT) * kWG * kStageBytes8;   // 2 x kWG x BM x TT fp32
   L.bar_off = L.red_off + 2 * kWG * BM * TT * 4;
-  L.grp_off = L.bar_off + (kWG * 6 + 4) * 8;
+  L.grp_off = L.bar_off + (kWG * 6 + 4 + kThreads / 32) * 8;
   L.misc_off = L.grp_off + kMaxGroups * (int)sizeof(Group);
   L.bytes = (size_t)L.misc_off + 16 + 1024;
   return L;
@@ -746,6 +763,7 @@ __global__ void __launch_bounds__(kThreads, 1) ffn_e4m3_kernel(const FfnParams p
   uint64_t* done = a_full + kWG * 3;
   uint64_t* red_full = done + kWG * 3;
   uint64_t* red_empty = red_full + 2;
+  uint64_t* drain = red_empty + 2;
   Group* groups = reinterpret_cast<Group*>(smem + L.grp_off);
   uint32_t* tmem_base_p = reinterpret_cast<uint32_t*>(smem + L.misc_off);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L.misc_off + 4);
@@ -854,6 +872,7 @@ __global__ void __launch_bounds__(kThreads, 1) ffn_e4m3_kernel(const FfnParams p
       mbar_init(&red_full[i], 128 * p.kq);
       mbar_init(&red_empty[i], kThreads);
     }
+    for (int i = 0; i < kThreads / 32; ++i) mbar_init(&drain[i], 1);
     *abort_flag = 0;
     fence_barrier_init();
   }
@@ -982,7 +1001,7 @@ __global__ void __launch_bounds__(kThreads, 1) ffn_e4m3_kernel(const FfnParams p
 
   auto epilogue = [&](int v) {
     finish_unit<MODE, TT, true>(v, ub, upe, groups, red, red_full, red_empty, p.kq, p.T, p.I, p.H, p.hbuf,
-                                p.expert_out, abort_flag, p.status);
+                                p.expert_out, abort_flag, p.status, p.wait_ns);
   };
   int epi = -1;
 
@@ -1026,7 +1045,7 @@ __global__ void __launch_bounds__(kThreads, 1) ffn_e4m3_kernel(const FfnParams p
           epilogue(epi);
           epi = -1;
         }
-        if (eul >= 2) mbar_wait_bounded(&red_empty[eul & 1], ((eul >> 1) - 1) & 1, abort_flag, p.status);
+        if (eul >= 2) mbar_wait_bounded(&red_empty[eul & 1], ((eul >> 1) - 1) & 1, abort_flag, p.status, p.wait_ns);
         float* rw = red + ((size_t)((eul & 1) * kWG + wg) * BM + r) * TT;
 #pragma unroll
         for (int n = 0; n < TT; ++n) {
@@ -1041,7 +1060,7 @@ __global__ void __launch_bounds__(kThreads, 1) ffn_e4m3_kernel(const FfnParams p
     // local unit iul), A/D buffer i & 1
     auto issue = [&](int i, int ist, int iul) {
       const int ib = i & 1;
-      mbar_wait_bounded(&a_full[wg * 3 + ib], (i >> 1) & 1, abort_flag, p.status);
+      mbar_wait_bounded(&a_full[wg * 3 + ib], (i >> 1) & 1, abort_flag, p.status, p.wait_ns);
       tc_fence_after();
       const uint32_t bbuf = MODE == 0 ? 0u : (uint32_t)((ub + iul) / upe - a_first) * b_bytes;
       const uint32_t bstage = bbase + bbuf + (uint32_t)((g0 + ist) * (BN8 * 128));
@@ -1061,7 +1080,7 @@ __global__ void __launch_bounds__(kThreads, 1) ffn_e4m3_kernel(const FfnParams p
         if (gs < NS) {
           // (1) stage gs - 2 completed: A buffer ab is free, its D readable
           if (gs >= 2) {
-            mbar_wait_bounded(&done[wg * 3 + ab], ((gs - 2) >> 1) & 1, abort_flag, p.status);
+            mbar_wait_bounded(&done[wg * 3 + ab], ((gs - 2) >> 1) & 1, abort_flag, p.status, p.wait_ns);
             __syncwarp();
             tc_fence_after();
           }
@@ -1107,6 +1126,7 @@ __global__ void __launch_bounds__(kThreads, 1) ffn_e4m3_kernel(const FfnParams p
           tmem_st_wait();
           tc_fence_before();
           __syncwarp();
+          if (p.stall_ns && gs == 0 && ub == 0 && wg == 0 && wq == 1 && lane == 0) debug_stall(p.stall_ns);
           if (lane == 0) mbar_arrive(&a_full[wg * 3 + ab]);
           // (5) issue stage gs - 1 if it is this warp's turn
           if (gs >= 1 && ((gs - 1) & 3) == wq && lane == 0) issue(gs - 1, st > 0 ? st - 1 : nst - 1, st > 0 ? ul : ul - 1);
@@ -1126,7 +1146,7 @@ __global__ void __launch_bounds__(kThreads, 1) ffn_e4m3_kernel(const FfnParams p
     __syncwarp();
     for (int back = NS < 2 ? NS : 2; back >= 1; --back) {
       const int e = NS - back;
-      mbar_wait_bounded(&done[wg * 3 + (e & 1)], (e >> 1) & 1, abort_flag, p.status);
+      mbar_wait_bounded(&done[wg * 3 + (e & 1)], (e >> 1) & 1, abort_flag, p.status, p.wait_ns);
       __syncwarp();
       tc_fence_after();
       int est = st - back, eul = ul;
@@ -1143,7 +1163,17 @@ __global__ void __launch_bounds__(kThreads, 1) ffn_e4m3_kernel(const FfnParams p
     for (int v = 0; v < NU; ++v) epilogue(v);
   }
 
+  // Every MMA must have completed before tensor memory is freed.  Without a
+  // give-up the waits above saw every stage complete; after one, each warp's
+  // issuing lane commits once more (tracking all its earlier MMAs) and waits.
   __syncthreads();
+  if (*abort_flag) {
+    if (lane == 0) {
+      umma_commit(&drain[warp]);
+      mbar_wait_drain(&drain[warp], 0, p.status);
+    }
+    __syncthreads();
+  }
   if (warp == 0) {
     tc_fence_after();
     tmem_dealloc(*tmem_base_p, kWG * kColsPerWG);
@@ -1283,6 +1313,8 @@ cudaError_t launch_ffn_decode(const qre_layer_shape& s, int T, const uint16_t* x
   p.hbuf = static_cast<__half*>(ws);
   p.expert_out = expert_out;
   p.status = status;
+  p.wait_ns = wait_limit_ns();
+  p.stall_ns = test_stall_ns();
   const long long pk = (long long)T * s.top_k;
   p.amax = (int)(pk < s.n_experts ? pk : s.n_experts);
   p.K = s.hidden;

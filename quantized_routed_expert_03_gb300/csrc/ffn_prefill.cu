@@ -63,6 +63,8 @@ struct PrefillParams {
   __half* h16;         // [T*k + T][I]
   float* expert_out;   // [T*k + T][H]
   int* status;
+  uint64_t wait_ns;    // limit of the pipeline waits
+  uint64_t stall_ns;   // test hook: the TMA warp of CTA 0 delays its first load (0 = off)
 };
 
 struct SmemLayout {
@@ -245,12 +247,13 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_gemm_kernel(const Prefill
   if (warp == 0) {
     // ---------------- token operand: TMA
     if (lane == 0) {
+      if (p.stall_ns && blockIdx.x == 0) debug_stall(p.stall_ns);
       int it = 0;
       for (int t = blockIdx.x; t < ntiles; t += gridDim.x) {
         const Tile tl = decode_tile(t, ngroups, tstart, grow0, gM, mt_per, n_act, p.active, p.E);
         for (int kb = 0; kb < KB; ++kb, ++it) {
           const int s = it % NSTAGE;
-          if (!mbar_wait_bounded(&empty[s], ((it / NSTAGE) & 1) ^ 1, abort_flag, p.status)) goto b_done;
+          if (!mbar_wait_bounded(&empty[s], ((it / NSTAGE) & 1) ^ 1, abort_flag, p.status, p.wait_ns)) goto b_done;
           mbar_arrive_expect_tx(&full_b[s], B_STAGE);
           tma_load_2d(Bs + (size_t)s * B_STAGE, &tmap_b, kb * BK, tl.row0 + tl.n0, &full_b[s]);
         }
@@ -258,7 +261,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_gemm_kernel(const Prefill
     b_done:
       const int first = it > NSTAGE ? it - NSTAGE : 0;
       for (int j = first; j < it; ++j)
-        mbar_wait_bounded(&full_b[j % NSTAGE], (j / NSTAGE) & 1, nullptr, p.status);
+        mbar_wait_drain(&full_b[j % NSTAGE], (j / NSTAGE) & 1, p.status);
     }
   } else if (warp == 1) {
     // ---------------- MMA issue (one thread)
@@ -267,7 +270,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_gemm_kernel(const Prefill
       for (int t = blockIdx.x; t < ntiles; t += gridDim.x, ++lt) {
         const Tile tl = decode_tile(t, ngroups, tstart, grow0, gM, mt_per, n_act, p.active, p.E);
         const int buf = lt & 1;
-        if (!mbar_wait_bounded(&acc_empty[buf], ((lt >> 1) & 1) ^ 1, abort_flag, p.status)) break;
+        if (!mbar_wait_bounded(&acc_empty[buf], ((lt >> 1) & 1) ^ 1, abort_flag, p.status, p.wait_ns)) break;
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + buf * kAccCols;
         const int n_mma = (tl.n + 15) & ~15;
@@ -276,8 +279,8 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_gemm_kernel(const Prefill
         for (int kb = 0; kb < KB; ++kb, ++it) {
           const int s = it % NSTAGE;
           const uint32_t ph = (it / NSTAGE) & 1;
-          if (!mbar_wait_bounded(&full_a[s], ph, abort_flag, p.status) ||
-              !mbar_wait_bounded(&full_b[s], ph, abort_flag, p.status)) {
+          if (!mbar_wait_bounded(&full_a[s], ph, abort_flag, p.status, p.wait_ns) ||
+              !mbar_wait_bounded(&full_b[s], ph, abort_flag, p.status, p.wait_ns)) {
             ok = false;
             break;
           }
@@ -294,7 +297,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_gemm_kernel(const Prefill
         if (!ok) break;
       }
       // TMEM is freed below: every MMA issued here must have completed first
-      if (last >= 0) mbar_wait_bounded(&acc_full[last & 1], (last >> 1) & 1, nullptr, p.status);
+      if (last >= 0) mbar_wait_drain(&acc_full[last & 1], (last >> 1) & 1, p.status);
     }
   } else if (warp < 10) {
     // ---------------- weight operand: dequantize into the swizzled stage
@@ -338,7 +341,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_gemm_kernel(const Prefill
           const int kb = kb0 + j;
           if (kb < KB) {
             const int s = it % NSTAGE;
-            const bool go = mbar_wait_bounded(&empty[s], ((it / NSTAGE) & 1) ^ 1, abort_flag, p.status);
+            const bool go = mbar_wait_bounded(&empty[s], ((it / NSTAGE) & 1) ^ 1, abort_flag, p.status, p.wait_ns);
             if (go) {
               const __half2 s2 = __half2half2(__ushort_as_half(sring[j]));
               const uint32_t words[4] = {ring[j].x, ring[j].y, ring[j].z, ring[j].w};
@@ -367,7 +370,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_gemm_kernel(const Prefill
     for (int t = blockIdx.x; t < ntiles; t += gridDim.x, ++lt) {
       const Tile tl = decode_tile(t, ngroups, tstart, grow0, gM, mt_per, n_act, p.active, p.E);
       const int buf = lt & 1;
-      const bool have = mbar_wait_bounded(&acc_full[buf], (lt >> 1) & 1, abort_flag, p.status);
+      const bool have = mbar_wait_bounded(&acc_full[buf], (lt >> 1) & 1, abort_flag, p.status, p.wait_ns);
       tc_fence_after();
       if (have) {
         const uint32_t tbase = tmem_base + ((uint32_t)(32 * q) << 16) + buf * kAccCols;
@@ -495,6 +498,8 @@ cudaError_t launch_ffn_prefill(const qre_layer_shape& s, int T, const uint16_t* 
   p.h16 = h16;
   p.expert_out = expert_out;
   p.status = status;
+  p.wait_ns = wait_limit_ns();
+  p.stall_ns = test_stall_ns();
   const size_t smem = SmemLayout::bytes(s.n_experts);
   const int grid = device_sm_count();
 

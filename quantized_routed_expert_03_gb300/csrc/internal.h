@@ -20,6 +20,11 @@ size_t route_ws_bytes(const qre_layer_shape& s, int T);
 size_t dispatch_ws_bytes(const qre_layer_shape& s, int T);
 size_t ffn_ws_bytes(const qre_layer_shape& s, int T);
 
+// Limit of the kernels' pipeline waits in ns (one second unless a test lowered
+// it with qre_debug_wait_test), and the test hook's stall (0 = off).
+uint64_t wait_limit_ns();
+uint64_t test_stall_ns();
+
 // Sets the calling thread's qre_last_error() message (printf format).
 void set_error_message(const char* fmt, ...);
 

@@ -153,3 +153,11 @@ def test_cache_argument_errors(lib):
     assert st == qre.QRE_ERR_MISALIGNED and "slot_expert" in msg
     st, msg = _status(lambda: qre.qre_cache_copy(s, A, None, A, A, 8, stream=0))
     assert st == qre.QRE_ERR_INVALID_ARG and "slot_mem" in msg
+
+
+def test_wait_test_hook_checks_its_arguments(lib):
+    st, msg = _status(lambda: qre.qre_debug_wait_test(2_000_000_000, 0))
+    assert st == qre.QRE_ERR_INVALID_ARG and "wait_limit_ns" in msg
+    st, msg = _status(lambda: qre.qre_debug_wait_test(0, 500_000_000))
+    assert st == qre.QRE_ERR_INVALID_ARG and "stall_ns" in msg
+    qre.qre_debug_wait_test(0, 0)      # the defaults

@@ -467,6 +467,9 @@ __global__ void __launch_bounds__(kThreads, 1) ffn_decode_kernel(const FfnParams
 
     uint32_t h1 = 0, h2 = 0, h3 = 0;   // scale words of global stages gs-1, gs-2, gs-3
     int st = 0, ul = 0;                // stage and local unit of gs
+    // test hook (outside the stage loop, whose code size matters): warp 1 of
+    // warpgroup 0 of the CTA owning unit 0 publishes its first stage late
+    if (p.stall_ns && ub == 0 && wg == 0 && wq == 1 && lane == 0) debug_stall(p.stall_ns);
     int ab = 0, aph = 0;               // A buffer of gs and the parity of its phase there
     for (int gs0 = 0; gs0 < NS; gs0 += R) {
 #pragma unroll
@@ -524,7 +527,6 @@ __global__ void __launch_bounds__(kThreads, 1) ffn_decode_kernel(const FfnParams
           tmem_st_wait();
           tc_fence_before();
           __syncwarp();
-          if (p.stall_ns && gs == 0 && ub == 0 && wg == 0 && wq == 1 && lane == 0) debug_stall(p.stall_ns);
           if (lane == 0) mbar_arrive(&a_full[wg * 3 + ab]);
           // (5) issue the previous stage if it is this warp's turn
           if (gs >= 1 && issuer(gs - 1) && lane == 0) {
@@ -1073,6 +1075,9 @@ __global__ void __launch_bounds__(kThreads, 1) ffn_e4m3_kernel(const FfnParams p
 
     uint32_t h1 = 0, h2 = 0;   // weight scales of stages gs-1, gs-2
     int st = 0, ul = 0;
+    // test hook (outside the stage loop, whose code size matters): warp 1 of
+    // warpgroup 0 of the CTA owning unit 0 publishes its first stage late
+    if (p.stall_ns && ub == 0 && wg == 0 && wq == 1 && lane == 0) debug_stall(p.stall_ns);
     for (int gs0 = 0; gs0 < NS; gs0 += R) {
 #pragma unroll
       for (int j = 0; j < R; ++j) {
@@ -1126,7 +1131,6 @@ __global__ void __launch_bounds__(kThreads, 1) ffn_e4m3_kernel(const FfnParams p
           tmem_st_wait();
           tc_fence_before();
           __syncwarp();
-          if (p.stall_ns && gs == 0 && ub == 0 && wg == 0 && wq == 1 && lane == 0) debug_stall(p.stall_ns);
           if (lane == 0) mbar_arrive(&a_full[wg * 3 + ab]);
           // (5) issue stage gs - 1 if it is this warp's turn
           if (gs >= 1 && ((gs - 1) & 3) == wq && lane == 0) issue(gs - 1, st > 0 ? st - 1 : nst - 1, st > 0 ? ul : ul - 1);

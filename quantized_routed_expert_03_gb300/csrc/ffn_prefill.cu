@@ -24,12 +24,18 @@
 //   warp 0      TMA loads of the token operand (128-byte swizzle) into a 4-stage ring
 //   warp 1      allocates 512 TMEM columns (two 128x256 fp32 accumulators) and
 //               issues tcgen05.mma (M=128, N<=256, K=16) from one thread
-//   warps 2-9   dequantize the weight operand: two threads per row each decode
-//               32 nibbles per stage (words and scales prefetched four stages
-//               ahead), multiply by the group scale in fp16 and store the
-//               128-byte swizzled rows the MMA expects
-//   warps 10-13 epilogue: tcgen05.ld of the finished accumulator while the MMA
-//               warp fills the other one
+//   warp 18     bulk-copies each stage's packed weights (one 4 KB chunk of the
+//               tiled format) and its group scales into a ring of its own in
+//               shared memory (host-mapped experts: plain loads by the warp)
+//   warps 2-9   dequantize the weight operand from that ring: two threads per
+//               row each decode 32 nibbles per stage, multiply by the group
+//               scale in fp16 and store the 128-byte swizzled rows the MMA
+//               expects
+//   warps 10-17 epilogue: tcgen05.ld of the finished accumulator while the MMA
+//               warp fills the other one; two warps per TMEM lane quarter take
+//               the tile's 32-token column chunks in turn.  GEMM 1 stages each
+//               chunk's h through a small shared-memory transpose so that every
+//               lane stores one token's 16 features as two 16-byte writes.
 // Operands are fp16 (x bf16 -> fp16 is exact in fp16's normal range; dequantized
 // weights and h are rounded to fp16), accumulation fp32.
 #include "common.cuh"
@@ -45,7 +51,13 @@ constexpr int BK = 64;                  // reduction elements per stage: one 128
 constexpr int NSTAGE = 4;
 constexpr int A_STAGE = BM * BK * 2;    // 16 KB
 constexpr int B_STAGE = BN * BK * 2;    // 32 KB
-constexpr int kWarps = 14;          // 0 TMA, 1 MMA, 2-9 dequant, 10-13 epilogue
+constexpr int kWarps = 19;          // 0 TMA, 1 MMA, 2-9 dequant, 10-17 epilogue, 18 weight copies
+constexpr int kEpiWarps = 8;
+constexpr int kEpiScratch = 32 * 32;   // bytes per epilogue warp: 32 tokens x 16 fp16 features
+constexpr int kDqWarps = 8;
+constexpr int kWChunk = BM * BK / 2;   // packed bytes of one stage: the 4 KB chunk (m0 / 128, kb)
+constexpr int kWSlot = kWChunk + 512;  // + the stage's group scales (two groups of 128 rows at most)
+constexpr int kMaxWStages = 8;
 constexpr int kDqThreads = 256;
 constexpr int kThreads = kWarps * 32;
 constexpr int kTmemCols = 512;
@@ -65,17 +77,21 @@ struct PrefillParams {
   int* status;
   uint64_t wait_ns;    // limit of the pipeline waits
   uint64_t stall_ns;   // test hook: the TMA warp of CTA 0 delays its first load (0 = off)
+  int wst;             // stages of the weight ring (2 .. kMaxWStages, what shared memory holds)
 };
 
 struct SmemLayout {
   static constexpr int a_off = 0;
   static constexpr int b_off = NSTAGE * A_STAGE;
   static constexpr int bar_off = b_off + NSTAGE * B_STAGE;
-  // full_a[NS], full_b[NS], empty[NS], acc_full[2], acc_empty[2]
-  static constexpr int nbars = 3 * NSTAGE + 4;
+  // full_a[NS], full_b[NS], empty[NS], acc_full[2], acc_empty[2], wfull[8], wempty[8]
+  static constexpr int nbars = 3 * NSTAGE + 4 + 2 * kMaxWStages;
   static constexpr int misc_off = bar_off + nbars * 8;   // tmem base, abort flag, group count, tile count
-  static constexpr int tab_off = misc_off + 16;
-  static size_t bytes(int E) { return (size_t)tab_off + 3 * (size_t)(E + 2) * 4 + 1024; }
+  static constexpr int epi_off = misc_off + 16;                 // kEpiWarps x kEpiScratch (16-byte aligned)
+  static constexpr int tab_off = epi_off + kEpiWarps * kEpiScratch;
+  // the weight ring follows the group table, 128-byte aligned
+  __host__ __device__ static int ring_off(int E) { return (tab_off + 3 * (E + 2) * 4 + 127) & ~127; }
+  static size_t bytes(int E, int wst) { return (size_t)ring_off(E) + (size_t)wst * kWSlot + 1024; }
 };
 
 // ---------------------------------------------------------------- gather
@@ -169,6 +185,9 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_gemm_kernel(const Prefill
   uint64_t* empty = bars + 2 * NSTAGE;
   uint64_t* acc_full = bars + 3 * NSTAGE;
   uint64_t* acc_empty = acc_full + 2;
+  uint64_t* wfull = acc_empty + 2;           // [wst]: a stage's weights and scales landed
+  uint64_t* wempty = wfull + kMaxWStages;    // [wst]: the dequantizing warps read them
+  uint8_t* wring = smem + SmemLayout::ring_off(p.E);
   uint32_t* tmem_base_p = reinterpret_cast<uint32_t*>(smem + SmemLayout::misc_off);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + SmemLayout::misc_off + 4);
   int* counts_p = reinterpret_cast<int*>(smem + SmemLayout::misc_off + 8);  // ngroups, ntiles
@@ -228,7 +247,11 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_gemm_kernel(const Prefill
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&acc_full[b], 1);
-      mbar_init(&acc_empty[b], 128);
+      mbar_init(&acc_empty[b], kEpiWarps * 32);
+    }
+    for (int w = 0; w < p.wst; ++w) {
+      mbar_init(&wfull[w], 1);
+      mbar_init(&wempty[w], kDqWarps);
     }
     *abort_flag = 0;
     fence_barrier_init();
@@ -306,8 +329,11 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_gemm_kernel(const Prefill
     const int hf = dq >> 7;                 // which 32 of the stage's 64 reduction elements
     const int sw = r & 7;
     const uint32_t row_off = (uint32_t)(r >> 3) * 1024 + (uint32_t)sw * 128;
-    int it = 0;
-    const int KG = p.K / p.G;
+    // in a ring slot: this thread's 16 bytes of the chunk (2048 * hf + 16 * r)
+    // and its row's scale in the stage's first or second group
+    const int wofs = 2048 * hf + 16 * r;
+    const int sofs = kWChunk + ((32 * hf) / p.G) * (BM * 2) + 2 * r;
+    int it = 0, w = 0, wph = 0;
     for (int t = blockIdx.x; t < ntiles; t += gridDim.x) {
       const Tile tl = decode_tile(t, ngroups, tstart, grow0, gM, mt_per, n_act, p.active, p.E);
       const qre_slot* sl = p.slots + tl.e;
@@ -315,86 +341,136 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_gemm_kernel(const Prefill
       const uint16_t* sb = MODE == 0 ? sl->s_gate_up : sl->s_down;
       const bool valid = wb && sb && ((reinterpret_cast<uintptr_t>(wb) | reinterpret_cast<uintptr_t>(sb)) & 15) == 0;
       if (!valid && dq == 0) set_status(p.status, QRE_DEV_NULL_SLOT);
-      // 16 bytes (32 nibbles) of row m0 + r per stage, and the scale of its group:
-      // stage kb of the tile is the 4 KB chunk (m0 / 128, kb); this thread's
-      // 16 bytes sit at 2048 * hf + 16 * r in it, and the scale of group g of
-      // the tile's rows at (m0 / 128 * KG + g) * 128 + r
-      const uint4* wrow = valid ? reinterpret_cast<const uint4*>(wb + (size_t)(tl.m0 / BM) * (p.K / BK) * 4096) +
-                                      128 * hf + r
-                                : nullptr;
-      const uint16_t* srow = valid ? sb + (size_t)(tl.m0 / BM) * KG * BM + r : nullptr;
-      uint4 ring[4];
-      unsigned short sring[4];
-#pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        if (valid && j < KB) {
-          ring[j] = __ldg(wrow + 256 * j);
-          sring[j] = __ldg(reinterpret_cast<const unsigned short*>(srow) + (j * BK + 32 * hf) / p.G * BM);
-        } else {
-          ring[j] = make_uint4(0x88888888u, 0x88888888u, 0x88888888u, 0x88888888u);
-          sring[j] = 0;
-        }
-      }
-      for (int kb0 = 0; kb0 < KB; kb0 += 4) {
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          const int kb = kb0 + j;
-          if (kb < KB) {
-            const int s = it % NSTAGE;
-            const bool go = mbar_wait_bounded(&empty[s], ((it / NSTAGE) & 1) ^ 1, abort_flag, p.status, p.wait_ns);
-            if (go) {
-              const __half2 s2 = __half2half2(__ushort_as_half(sring[j]));
-              const uint32_t words[4] = {ring[j].x, ring[j].y, ring[j].z, ring[j].w};
-              uint8_t* stage = As + (size_t)s * A_STAGE + row_off;
-#pragma unroll
-              for (int c = 0; c < 4; ++c) {
-                const uint4 v = dequant8(words[c], s2);
-                *reinterpret_cast<uint4*>(stage + (((4 * hf + c) ^ sw) << 4)) = v;
-              }
-              fence_proxy_async_smem();
-            }
-            mbar_arrive(&full_a[s]);
-            ++it;
-            if (valid && kb + 4 < KB) {
-              ring[j] = __ldg(wrow + 256 * (kb + 4));
-              sring[j] = __ldg(reinterpret_cast<const unsigned short*>(srow) + ((kb + 4) * BK + 32 * hf) / p.G * BM);
-            }
+      for (int kb = 0; kb < KB; ++kb, ++it) {
+        const int s = it % NSTAGE;
+        const bool go = mbar_wait_bounded(&empty[s], ((it / NSTAGE) & 1) ^ 1, abort_flag, p.status, p.wait_ns);
+        const bool wok = mbar_wait_bounded(&wfull[w], wph, abort_flag, p.status, p.wait_ns);
+        if (go && wok) {
+          const uint8_t* slot = wring + w * kWSlot;
+          uint4 wv = make_uint4(0x88888888u, 0x88888888u, 0x88888888u, 0x88888888u);
+          unsigned short sv = 0;
+          if (valid) {
+            wv = *reinterpret_cast<const uint4*>(slot + wofs);
+            sv = *reinterpret_cast<const unsigned short*>(slot + sofs);
           }
+          const __half2 s2 = __half2half2(__ushort_as_half(sv));
+          const uint32_t words[4] = {wv.x, wv.y, wv.z, wv.w};
+          uint8_t* stage = As + (size_t)s * A_STAGE + row_off;
+#pragma unroll
+          for (int c = 0; c < 4; ++c) {
+            const uint4 v = dequant8(words[c], s2);
+            *reinterpret_cast<uint4*>(stage + (((4 * hf + c) ^ sw) << 4)) = v;
+          }
+          fence_proxy_async_smem();
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&wempty[w]);   // this warp is done with the ring slot
+        mbar_arrive(&full_a[s]);
+        if (++w == p.wst) {
+          w = 0;
+          wph ^= 1;
         }
       }
     }
+  } else if (warp == 18) {
+    // ---------------- weight copies: the packed chunk and group scales of each stage
+    int it = 0, w = 0, wph = 0;
+    const int KG = p.K / p.G;
+    const uint32_t sbytes = 256u * (p.G < BK ? (uint32_t)(BK / p.G) : 1u);   // scales of the stage's groups
+    for (int t = blockIdx.x; t < ntiles; t += gridDim.x) {
+      const Tile tl = decode_tile(t, ngroups, tstart, grow0, gM, mt_per, n_act, p.active, p.E);
+      const qre_slot* sl = p.slots + tl.e;
+      const uint8_t* wb = MODE == 0 ? sl->w_gate_up : sl->w_down;
+      const uint16_t* sb = MODE == 0 ? sl->s_gate_up : sl->s_down;
+      const bool valid = wb && sb && ((reinterpret_cast<uintptr_t>(wb) | reinterpret_cast<uintptr_t>(sb)) & 15) == 0;
+      const bool host = sl->tier != 0;
+      const uint8_t* wsrc = valid ? wb + (size_t)(tl.m0 / BM) * (p.K / BK) * kWChunk : nullptr;
+      const uint16_t* ssrc = valid ? sb + (size_t)(tl.m0 / BM) * KG * BM : nullptr;
+      for (int kb = 0; kb < KB; ++kb, ++it) {
+        // warp-uniform exit (the host-mapped path below synchronizes the warp)
+        if (!__all_sync(0xffffffffu, mbar_wait_bounded(&wempty[w], wph ^ 1, abort_flag, p.status, p.wait_ns)))
+          goto w_done;
+        uint8_t* dst = wring + w * kWSlot;
+        const size_t g0 = (size_t)(kb * BK) / p.G;   // first group of the stage
+        if (valid && !host) {
+          if (lane == 0) {
+            mbar_arrive_expect_tx(&wfull[w], kWChunk + sbytes);
+            bulk_copy_g2s(dst, wsrc + (size_t)kb * kWChunk, kWChunk, &wfull[w]);
+            bulk_copy_g2s(dst + kWChunk, ssrc + g0 * BM, sbytes, &wfull[w]);
+          }
+        } else {
+          if (valid) {   // host-mapped expert: the warp copies with plain 16-byte loads
+            const uint4* src = reinterpret_cast<const uint4*>(wsrc + (size_t)kb * kWChunk);
+            for (int i = lane; i < kWChunk / 16; i += 32) reinterpret_cast<uint4*>(dst)[i] = __ldg(src + i);
+            const uint4* ss = reinterpret_cast<const uint4*>(ssrc + g0 * BM);
+            for (int i = lane; i < (int)sbytes / 16; i += 32) reinterpret_cast<uint4*>(dst + kWChunk)[i] = __ldg(ss + i);
+          }
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&wfull[w]);
+        }
+        if (++w == p.wst) {
+          w = 0;
+          wph ^= 1;
+        }
+      }
+    }
+  w_done:
+    // copies still in flight land before the CTA exits
+    if (lane == 0) {
+      const int first = it > p.wst ? it - p.wst : 0;
+      for (int j = first; j < it; ++j) mbar_wait_drain(&wfull[j % p.wst], (j / p.wst) & 1, p.status);
+    }
   } else {
     // ---------------- epilogue
-    const int q = warp & 3;  // TMEM lane quarter this warp may access
+    const int q = warp & 3;               // TMEM lane quarter this warp may access
+    const int half = (warp - 10) >> 2;    // which 32-token chunks: even (0) or odd (1)
+    // GEMM 1: this warp's transpose scratch, 32 rows (tokens) of 32 bytes (16
+    // features); the two 16-byte halves of row j are swapped when (j >> 2) & 1,
+    // which keeps both the 2-byte writes and the 16-byte reads conflict-free.
+    uint8_t* scratch = smem + SmemLayout::epi_off + (warp - 10) * kEpiScratch;
     int lt = 0;
     for (int t = blockIdx.x; t < ntiles; t += gridDim.x, ++lt) {
       const Tile tl = decode_tile(t, ngroups, tstart, grow0, gM, mt_per, n_act, p.active, p.E);
       const int buf = lt & 1;
-      const bool have = mbar_wait_bounded(&acc_full[buf], (lt >> 1) & 1, abort_flag, p.status, p.wait_ns);
+      // warp-uniform: the chunk loop below uses whole-warp shuffles
+      const bool have =
+          __all_sync(0xffffffffu, mbar_wait_bounded(&acc_full[buf], (lt >> 1) & 1, abort_flag, p.status, p.wait_ns));
       tc_fence_after();
       if (have) {
         const uint32_t tbase = tmem_base + ((uint32_t)(32 * q) << 16) + buf * kAccCols;
-        for (int c0 = 0; c0 < tl.n; c0 += 32) {
+        bool overflow = false;
+        for (int c0 = 32 * half; c0 < tl.n; c0 += 64) {
           uint32_t v[32];
           tmem_ld_32x32b_x32(tbase + c0, v);
           tmem_ld_wait();
           if constexpr (MODE == 0) {
-            // lanes 0-15 hold gate rows, lanes 16-31 the matching up rows
-            const int feat = tl.m0 / 2 + 16 * q + (lane & 15);
+            // lanes 0-15 hold gate rows, lanes 16-31 the matching up rows;
+            // feature f = lane of the warp's 16 (group-of-8 order: i at 2(i%4) + i/4)
+            const int f = lane & 15;
+            const int pos = (f & 8) | ((f & 3) << 1) | ((f >> 2) & 1);
 #pragma unroll
             for (int j = 0; j < 32; ++j) {
               const float up = __shfl_down_sync(0xffffffffu, __uint_as_float(v[j]), 16);
-              const int n = c0 + j;
-              if (lane < 16 && n < tl.n) {
+              if (lane < 16) {
                 const float g = __uint_as_float(v[j]);
-                const float h = g / (1.0f + expf(-g)) * up;
-                const __half hh = __float2half_rn(h);
-                if (__hisinf(hh)) set_status(p.status, QRE_DEV_FP16_RANGE);
-                // within each group of 8 features, feature i sits at 2*(i%4) + i/4
-                const int pos = (feat & ~7) | (((feat & 3) << 1) | ((feat >> 2) & 1));
-                p.h16[(size_t)(tl.row0 + tl.n0 + n) * p.I + pos] = hh;
+                const __half hh = __float2half_rn(__fdividef(g, 1.0f + __expf(-g)) * up);
+                overflow |= __hisinf(hh) && c0 + j < tl.n;
+                const int sw = (pos >> 3) ^ ((j >> 2) & 1);
+                *reinterpret_cast<__half*>(scratch + j * 32 + sw * 16 + (pos & 7) * 2) = hh;
               }
             }
+            __syncwarp();
+            // lane L: token c0 + L, the warp's 16 features (32 bytes) in h16 order
+            const int n = c0 + lane;
+            if (n < tl.n) {
+              const int s0 = (lane >> 2) & 1;
+              const uint4 lo = *reinterpret_cast<const uint4*>(scratch + lane * 32 + s0 * 16);
+              const uint4 hi = *reinterpret_cast<const uint4*>(scratch + lane * 32 + (s0 ^ 1) * 16);
+              uint4* dst = reinterpret_cast<uint4*>(p.h16 + (size_t)(tl.row0 + tl.n0 + n) * p.I + tl.m0 / 2 + 16 * q);
+              dst[0] = lo;
+              dst[1] = hi;
+            }
+            __syncwarp();
           } else {
             const int col = tl.m0 + 32 * q + lane;
 #pragma unroll
@@ -404,6 +480,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_gemm_kernel(const Prefill
             }
           }
         }
+        if (MODE == 0 && __any_sync(0xffffffffu, overflow) && lane == 0) set_status(p.status, QRE_DEV_FP16_RANGE);
       }
       tc_fence_before();
       mbar_arrive(&acc_empty[buf]);
@@ -460,9 +537,16 @@ size_t ffn_prefill_ws_bytes(const qre_layer_shape& s, int T) {
   return align256(rows * s.hidden * 2) + align256(rows * s.inter * 2);
 }
 
+// Weight-ring stages that fit next to everything else in shared memory.
+int weight_stages(int E) {
+  const long long spare = (long long)device_max_smem_optin() - (long long)SmemLayout::bytes(E, 0);
+  const long long n = spare / kWSlot;
+  return (int)(n > kMaxWStages ? kMaxWStages : n);
+}
+
 bool ffn_prefill_supported(const qre_layer_shape& s) {
   return s.hidden % BK == 0 && s.inter % BK == 0 && (2 * s.inter) % BM == 0 && s.hidden % BM == 0 &&
-         SmemLayout::bytes(s.n_experts) <= (size_t)device_max_smem_optin();
+         weight_stages(s.n_experts) >= 2;
 }
 
 cudaError_t launch_ffn_prefill(const qre_layer_shape& s, int T, const uint16_t* x, const qre_slot* slots,
@@ -500,7 +584,8 @@ cudaError_t launch_ffn_prefill(const qre_layer_shape& s, int T, const uint16_t* 
   p.status = status;
   p.wait_ns = wait_limit_ns();
   p.stall_ns = test_stall_ns();
-  const size_t smem = SmemLayout::bytes(s.n_experts);
+  p.wst = weight_stages(s.n_experts);
+  const size_t smem = SmemLayout::bytes(s.n_experts, p.wst);
   const int grid = device_sm_count();
 
   p.K = s.hidden;

@@ -278,6 +278,26 @@ def test_prefill_layers_match_oracle(cfg, T):
     assert err > 1e-6      # fp16 operands: the error is visible, not zero
 
 
+@pytest.mark.parametrize("T", [40, 300])
+def test_prefill_host_resident_experts_bit_identical_to_hbm(T):
+    """Slot placement invariance for the grouped GEMM: experts read from pinned
+    host memory (copied into shared memory with plain loads) give the same bits
+    as the same experts in device memory (bulk-copied)."""
+    cfg = MID
+    src = numpy_source(cfg)
+    a = BuiltLayer(cfg.hidden, cfg.inter, cfg.n_experts, cfg.top_k, cfg.group, T, DEV, src)
+    rng = np.random.default_rng(8)
+    host = rng.random(cfg.n_experts + 1) < 0.5
+    b = BuiltLayer(cfg.hidden, cfg.inter, cfg.n_experts, cfg.top_k, cfg.group, T, DEV, src, host_mask=host,
+                   arena_order=rng.permutation(cfg.n_experts + 1))
+    x_bits, wr, _ = _inputs(cfg, T, step=77)
+    ga = _run(a, x_bits, wr, None)
+    gb = _run(b, x_bits, wr, None)
+    np.testing.assert_array_equal(ga["expert_out"], gb["expert_out"])
+    np.testing.assert_array_equal(ga["y"], gb["y"])
+    _check_layer(b, gb, b.oracle_layer(x_bits, wr, None), tol=PREFILL_TOL)
+
+
 def test_prefill_token_order_invariance_bit_exact():
     cfg, T = MID, 200
     built = BuiltLayer(cfg.hidden, cfg.inter, cfg.n_experts, cfg.top_k, cfg.group, T, DEV, numpy_source(cfg))

@@ -154,6 +154,11 @@ def workload_config(name: str, n_sets: int, world: int) -> dict:
             "launch": "CUDA graph of captured steps"}
 
 
+def side_note(args) -> dict:
+    return {"shared_expert": "side stream (qre_expert_ffn_shared forked beside route/dispatch)"} if getattr(
+        args, "side_stream", False) else {}
+
+
 class ClockSampler:
     """nvidia-smi clocks/throttle reasons sampled every 200 ms in the background."""
 
@@ -277,8 +282,13 @@ def measure_workload(name, args, K, W, rank, local_rank, world, device, log, cpu
     n_x = 4 if stack else (2 if prefill else per_graph // wl.n_sets)
     xs = wl.x_pool(n_x, device)
 
+    side = torch.cuda.Stream(device) if args.side_stream else None
+
     def one_layer(s, x):
         L = s["layer"]
+        if side is not None:   # the shared expert on a second stream (fork/join inside the graph)
+            L.forward(x, s["wr"], s["bias"], T, stream=stream, shared_stream=side)
+            return
         L.route(x, s["wr"], s["bias"], T)
         L.dispatch(T)
         L.expert_ffn(x, T)
@@ -429,7 +439,7 @@ def measure_workload(name, args, K, W, rank, local_rank, world, device, log, cpu
         "ms_per_step": round(ms / K, 6), "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": DTYPE_PREFILL if prefill else (DTYPE_DECODE if fp8 else DTYPE_DECODE_FP16),
         "data": "synthetic (seeded generators; random-init weights quantized to the library's 4-bit group format)",
-        "config": workload_config(name, wl.n_sets, world),
+        "config": {**workload_config(name, wl.n_sets, world), **side_note(args)},
         "gpu_launches": None, "roofline": roofline, "clocks": clocks, "e2e": None,
     }
     launches_per_layer = 2 + (1 if T * k <= 1024 else 3) + (3 if prefill else 2) + 1
@@ -672,6 +682,8 @@ def main():
     ap.add_argument("--e2e-steps", type=int, default=5000)
     ap.add_argument("--sets", type=int, default=None,
                     help="distinct layer weight sets to rotate over (default: enough to exceed L2)")
+    ap.add_argument("--side-stream", action="store_true",
+                    help="run the shared expert on a second stream beside the router and dispatch")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-clocks", action="store_true")

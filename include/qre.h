@@ -256,6 +256,32 @@ QRE_API qre_status qre_expert_ffn(const qre_layer_shape* shape, int32_t T, const
                           void* workspace, size_t workspace_bytes, qre_stream_t stream);
 
 /*
+ * The expert FFN in two parts that may run concurrently on two streams: the
+ * routed experts (qre_expert_ffn_routed, which needs the dispatch results) and
+ * the shared expert (qre_expert_ffn_shared, which needs only x, so it can start
+ * while the router and the dispatch run -- the glm53-flash-offload README's
+ * "Decode kernels" bullet moves the shared expert to a side stream).  Together
+ * they write exactly what one qre_expert_ffn call writes, with the same bits
+ * (every expert row is computed by the same arithmetic whichever launch or CTA
+ * computes it), so the combine order and the layer output do not change.
+ *   qre_expert_ffn_routed: arguments as qre_expert_ffn; writes expert_out rows
+ *     0 .. T*k-1; workspace >= qre_workspace_size bytes.
+ *   qre_expert_ffn_shared: writes expert_out rows T*k .. T*k+T-1 (the shared
+ *     expert's output per token) from x and slots[n_experts]; workspace: its own
+ *     buffer of at least qre_shared_workspace_size bytes (not the one the router,
+ *     the dispatch or the routed part use while it runs).
+ */
+QRE_API qre_status qre_expert_ffn_routed(const qre_layer_shape* shape, int32_t T, const uint16_t* x_bf16,
+                                         const qre_slot* slots, const int32_t* offsets, const int32_t* perm,
+                                         const int32_t* active, const int32_t* n_active, float* expert_out,
+                                         void* workspace, size_t workspace_bytes, qre_stream_t stream);
+QRE_API qre_status qre_expert_ffn_shared(const qre_layer_shape* shape, int32_t T, const uint16_t* x_bf16,
+                                         const qre_slot* slots, float* expert_out, void* workspace,
+                                         size_t workspace_bytes, qre_stream_t stream);
+/* Bytes of workspace qre_expert_ffn_shared needs for T tokens (bytes: host). */
+QRE_API qre_status qre_shared_workspace_size(const qre_layer_shape* shape, int32_t T, size_t* bytes);
+
+/*
  * Combine: y[t] = sum_j topk_w[t][j] * expert_out[inv_perm[t*k + j]] +
  * expert_out[T*k + t], accumulated in fp32 in ascending j (ascending expert
  * id), the shared term last.  The fp32 partial sums are added after the

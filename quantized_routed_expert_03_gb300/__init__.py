@@ -41,6 +41,7 @@ EXPORTS = (
     "qre_route", "qre_dispatch", "qre_expert_ffn", "qre_combine", "qre_validate_slots",
     "qre_cache_update", "qre_cache_copy",
     "qre_read_device_status", "qre_clear_device_status", "qre_route_noalloc", "qre_debug_wait_test",
+    "qre_expert_ffn_routed", "qre_expert_ffn_shared", "qre_shared_workspace_size",
 )
 
 
@@ -86,6 +87,9 @@ _SIGS = {
     "qre_clear_device_status": ([_VP], ctypes.c_int),
     "qre_route_noalloc": ([_SHAPE, _I32, _VP, _VP, _VP, _VP, _VP, _VP], ctypes.c_int),
     "qre_debug_wait_test": ([ctypes.c_uint64, ctypes.c_uint64], ctypes.c_int),
+    "qre_expert_ffn_routed": ([_SHAPE, _I32, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _SZ, _VP], ctypes.c_int),
+    "qre_expert_ffn_shared": ([_SHAPE, _I32, _VP, _VP, _VP, _VP, _SZ, _VP], ctypes.c_int),
+    "qre_shared_workspace_size": ([_SHAPE, _I32, ctypes.POINTER(ctypes.c_size_t)], ctypes.c_int),
 }
 
 
@@ -196,6 +200,29 @@ def qre_expert_ffn(shape, T, x_bf16, slots, offsets, perm, active, n_active, exp
                                          _ptr(perm), _ptr(active), _ptr(n_active), _ptr(expert_out),
                                          _ptr(workspace), _nbytes(workspace, workspace_bytes), _stream(stream)),
            "qre_expert_ffn")
+
+
+def qre_expert_ffn_routed(shape, T, x_bf16, slots, offsets, perm, active, n_active, expert_out, workspace,
+                          workspace_bytes=None, stream=None) -> None:
+    _check(load_library().qre_expert_ffn_routed(ctypes.byref(shape), T, _ptr(x_bf16), _ptr(slots), _ptr(offsets),
+                                                _ptr(perm), _ptr(active), _ptr(n_active), _ptr(expert_out),
+                                                _ptr(workspace), _nbytes(workspace, workspace_bytes),
+                                                _stream(stream)), "qre_expert_ffn_routed")
+
+
+def qre_expert_ffn_shared(shape, T, x_bf16, slots, expert_out, workspace, workspace_bytes=None,
+                          stream=None) -> None:
+    _check(load_library().qre_expert_ffn_shared(ctypes.byref(shape), T, _ptr(x_bf16), _ptr(slots),
+                                                _ptr(expert_out), _ptr(workspace),
+                                                _nbytes(workspace, workspace_bytes), _stream(stream)),
+           "qre_expert_ffn_shared")
+
+
+def qre_shared_workspace_size(shape: qre_layer_shape, T: int) -> int:
+    out = ctypes.c_size_t(0)
+    _check(load_library().qre_shared_workspace_size(ctypes.byref(shape), T, ctypes.byref(out)),
+           "qre_shared_workspace_size")
+    return out.value
 
 
 def qre_combine(shape, T, expert_out, topk_w, inv_perm, y_f32, y_bf16, stream=None) -> None:

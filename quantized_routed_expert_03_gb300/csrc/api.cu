@@ -250,39 +250,84 @@ qre_status qre_dispatch(const qre_layer_shape* shape, int32_t T, const int32_t* 
                   "qre_dispatch launch");
 }
 
-qre_status qre_expert_ffn(const qre_layer_shape* shape, int32_t T, const uint16_t* x_bf16, const qre_slot* slots,
-                          const int32_t* offsets, const int32_t* perm, const int32_t* active,
-                          const int32_t* n_active, float* expert_out, void* workspace, size_t workspace_bytes,
-                          qre_stream_t stream) {
+namespace {
+
+// The expert FFN over the groups of `part` (qre::FfnPart); the routing
+// arguments are only needed when routed groups are computed.
+qre_status expert_ffn_part(const qre_layer_shape* shape, int32_t T, const uint16_t* x_bf16, const qre_slot* slots,
+                           const int32_t* offsets, const int32_t* perm, const int32_t* active,
+                           const int32_t* n_active, float* expert_out, void* workspace, size_t workspace_bytes,
+                           qre_stream_t stream, int part, const char* name) {
   qre_status st = check_shape(shape, T);
   if (st != QRE_OK) return st;
   if (T == 0) return QRE_OK;
   QRE_REQUIRE_PTR(x_bf16);
   QRE_REQUIRE_PTR(slots);
-  QRE_REQUIRE_PTR(offsets);
-  QRE_REQUIRE_PTR(perm);
-  QRE_REQUIRE_PTR(active);
-  QRE_REQUIRE_PTR(n_active);
+  if (part != qre::kFfnShared) {
+    QRE_REQUIRE_PTR(offsets);
+    QRE_REQUIRE_PTR(perm);
+    QRE_REQUIRE_PTR(active);
+    QRE_REQUIRE_PTR(n_active);
+  }
   QRE_REQUIRE_PTR(expert_out);
   cudaStream_t st_ = reinterpret_cast<cudaStream_t>(stream);
+  const bool shared_only = part == qre::kFfnShared;
   if (T > qre::kDecodeMaxTokens) {
     if (!qre::ffn_prefill_supported(*shape))
       return fail(QRE_ERR_UNSUPPORTED, "no grouped-GEMM plan for hidden %d, inter %d, %d experts", shape->hidden,
                   shape->inter, shape->n_experts);
-    st = check_workspace(workspace, workspace_bytes, qre::ffn_prefill_ws_bytes(*shape, T));
+    st = check_workspace(workspace, workspace_bytes,
+                         shared_only ? qre::ffn_prefill_shared_ws_bytes(*shape, T) : qre::ffn_prefill_ws_bytes(*shape, T));
     if (st != QRE_OK) return st;
     return launched(qre::launch_ffn_prefill(*shape, T, x_bf16, slots, offsets, perm, active, n_active, expert_out,
-                                            workspace, qre::device_status_word(), st_),
-                    "qre_expert_ffn (grouped GEMM) launch");
+                                            workspace, qre::device_status_word(), st_, part),
+                    name);
   }
   if (!qre::ffn_decode_supported(*shape))
     return fail(QRE_ERR_UNSUPPORTED, "no decode kernel plan for hidden %d, inter %d, group %d", shape->hidden,
                 shape->inter, shape->group);
-  st = check_workspace(workspace, workspace_bytes, qre::ffn_ws_bytes(*shape, T));
+  st = check_workspace(workspace, workspace_bytes,
+                       shared_only ? qre::ffn_shared_ws_bytes(*shape, T) : qre::ffn_ws_bytes(*shape, T));
   if (st != QRE_OK) return st;
   return launched(qre::launch_ffn_decode(*shape, T, x_bf16, slots, offsets, perm, active, n_active, expert_out,
-                                         workspace, qre::device_status_word(), st_),
-                  "qre_expert_ffn launch");
+                                         workspace, qre::device_status_word(), st_, part),
+                  name);
+}
+
+}  // namespace
+
+qre_status qre_expert_ffn(const qre_layer_shape* shape, int32_t T, const uint16_t* x_bf16, const qre_slot* slots,
+                          const int32_t* offsets, const int32_t* perm, const int32_t* active,
+                          const int32_t* n_active, float* expert_out, void* workspace, size_t workspace_bytes,
+                          qre_stream_t stream) {
+  return expert_ffn_part(shape, T, x_bf16, slots, offsets, perm, active, n_active, expert_out, workspace,
+                         workspace_bytes, stream, qre::kFfnAll, "qre_expert_ffn launch");
+}
+
+qre_status qre_expert_ffn_routed(const qre_layer_shape* shape, int32_t T, const uint16_t* x_bf16,
+                                 const qre_slot* slots, const int32_t* offsets, const int32_t* perm,
+                                 const int32_t* active, const int32_t* n_active, float* expert_out, void* workspace,
+                                 size_t workspace_bytes, qre_stream_t stream) {
+  return expert_ffn_part(shape, T, x_bf16, slots, offsets, perm, active, n_active, expert_out, workspace,
+                         workspace_bytes, stream, qre::kFfnRouted, "qre_expert_ffn_routed launch");
+}
+
+qre_status qre_expert_ffn_shared(const qre_layer_shape* shape, int32_t T, const uint16_t* x_bf16,
+                                 const qre_slot* slots, float* expert_out, void* workspace, size_t workspace_bytes,
+                                 qre_stream_t stream) {
+  return expert_ffn_part(shape, T, x_bf16, slots, nullptr, nullptr, nullptr, nullptr, expert_out, workspace,
+                         workspace_bytes, stream, qre::kFfnShared, "qre_expert_ffn_shared launch");
+}
+
+qre_status qre_shared_workspace_size(const qre_layer_shape* shape, int32_t T, size_t* bytes) {
+  qre_status st = check_shape(shape, T);
+  if (st != QRE_OK) return st;
+  if (!bytes) return fail(QRE_ERR_INVALID_ARG, "bytes is NULL");
+  const size_t b = T <= qre::kDecodeMaxTokens ? qre::ffn_shared_ws_bytes(*shape, T)
+                                              : qre::ffn_prefill_shared_ws_bytes(*shape, T);
+  *bytes = align256(b > 0 ? b : 1);
+  g_err[0] = '\0';
+  return QRE_OK;
 }
 
 qre_status qre_combine(const qre_layer_shape* shape, int32_t T, const float* expert_out, const float* topk_w,

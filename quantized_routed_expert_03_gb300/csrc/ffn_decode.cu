@@ -83,6 +83,7 @@ struct FfnParams {
   int lgG;          // log2 G
   int nB;           // B buffers in shared memory (down kernel: experts resident at once)
   int amax;         // largest possible number of active experts, min(E, T*k)
+  int part;         // groups of this launch: 0 routed + shared, 1 routed only, 2 shared only
   const uint16_t* x;
   const qre_slot* slots;
   const int32_t* offsets;
@@ -243,10 +244,12 @@ __global__ void __launch_bounds__(kThreads, 1) ffn_decode_kernel(const FfnParams
 
   // the possible active ids are read together with their count (one dependent
   // load less before the slot table)
-  const int a_spec = threadIdx.x < p.amax ? __ldg(p.active + threadIdx.x) : p.E;
-  int n_act = *p.n_active;
+  // groups: the active experts (parts 0, 1), then the shared one (parts 0, 2);
+  // the shared-only launch reads no routing at all
+  const int a_spec = (p.part != 2 && threadIdx.x < p.amax) ? __ldg(p.active + threadIdx.x) : p.E;
+  int n_act = p.part == 2 ? 0 : *p.n_active;
   n_act = n_act < 0 ? 0 : (n_act > p.amax ? p.amax : n_act);
-  const int ngroups = n_act + 1;
+  const int ngroups = n_act + (p.part == 1 ? 0 : 1);
   const int upe = p.n_out / BM;
   const int U = ngroups * upe;
   const int ub = (int)((long long)blockIdx.x * U / gridDim.x);
@@ -810,10 +813,12 @@ __global__ void __launch_bounds__(kThreads, 1) ffn_e4m3_kernel(const FfnParams p
       if (wk >= 0 && wk + kNW * b < p.T * KG) pre[b] = job_load(wk + kNW * b, 0);
   }
 
-  const int a_spec = threadIdx.x < p.amax ? __ldg(p.active + threadIdx.x) : p.E;
-  int n_act = *p.n_active;
+  // groups: the active experts (parts 0, 1), then the shared one (parts 0, 2);
+  // the shared-only launch reads no routing at all
+  const int a_spec = (p.part != 2 && threadIdx.x < p.amax) ? __ldg(p.active + threadIdx.x) : p.E;
+  int n_act = p.part == 2 ? 0 : *p.n_active;
   n_act = n_act < 0 ? 0 : (n_act > p.amax ? p.amax : n_act);
-  const int ngroups = n_act + 1;
+  const int ngroups = n_act + (p.part == 1 ? 0 : 1);
   const int upe = p.n_out / BM;
   const int U = ngroups * upe;
   const int ub = (int)((long long)blockIdx.x * U / gridDim.x);
@@ -1266,7 +1271,7 @@ cudaError_t launch_mode(const FfnParams& base, long long units, bool fp8, cudaSt
     int smem = 0;
     if (e4m3_plan(MODE, p.K, p.G, TT, &p.nB, &smem)) {
       p.kq = pick_kq(p.K, p.G);
-      const int grid = (int)decode_grid(MODE, p.nB, units, p.amax, sms);
+      const int grid = (int)decode_grid(MODE, p.nB, units, (int)(units / (p.n_out / BM)) - 1, sms);
       if (TT == 1) return launch_e4m3<MODE, 1>(p, grid, smem, stream);
       return launch_e4m3<MODE, kTok>(p, grid, smem, stream);
     }
@@ -1276,7 +1281,7 @@ cudaError_t launch_mode(const FfnParams& base, long long units, bool fp8, cudaSt
   const int seg = Kq < p.G ? Kq : p.G;
   p.nB = (MODE == 1 && smem_needed(p.K, 2, TT) <= budget) ? 2 : 1;
   const int smem = smem_needed(p.K, p.nB, TT);
-  const long long grid = decode_grid(MODE, p.nB, units, p.amax, sms);
+  const long long grid = decode_grid(MODE, p.nB, units, (int)(units / (p.n_out / BM)) - 1, sms);
   if (TT == 1) return launch_tt<MODE, 1>(p, seg, (int)grid, smem, stream);
   return launch_tt<MODE, kTok>(p, seg, (int)grid, smem, stream);
 }
@@ -1296,10 +1301,12 @@ size_t ffn_ws_bytes(const qre_layer_shape& s, int T) {
   return (size_t)(amax + 1) * 2 * kTok * s.inter * sizeof(__half);
 }
 
+size_t ffn_shared_ws_bytes(const qre_layer_shape& s, int) { return (size_t)2 * kTok * s.inter * sizeof(__half); }
+
 cudaError_t launch_ffn_decode(const qre_layer_shape& s, int T, const uint16_t* x, const qre_slot* slots,
                               const int32_t* offsets, const int32_t* perm, const int32_t* active,
                               const int32_t* n_active, float* expert_out, void* ws, int* status,
-                              cudaStream_t stream) {
+                              cudaStream_t stream, int part) {
   if (!ffn_decode_supported(s)) return cudaErrorInvalidValue;
   FfnParams p{};
   p.H = s.hidden;
@@ -1317,6 +1324,7 @@ cudaError_t launch_ffn_decode(const qre_layer_shape& s, int T, const uint16_t* x
   p.hbuf = static_cast<__half*>(ws);
   p.expert_out = expert_out;
   p.status = status;
+  p.part = part;
   p.wait_ns = wait_limit_ns();
   p.stall_ns = test_stall_ns();
   const long long pk = (long long)T * s.top_k;
@@ -1326,12 +1334,14 @@ cudaError_t launch_ffn_decode(const qre_layer_shape& s, int T, const uint16_t* x
   const int TT = T == 1 ? 1 : kTok;
   int nb = 0, sm = 0;
   const bool fp8 = e4m3_plan(0, s.hidden, s.group, TT, &nb, &sm) && e4m3_plan(1, s.inter, s.group, TT, &nb, &sm);
-  cudaError_t err = launch_mode<0>(p, (long long)(p.amax + 1) * (p.n_out / BM), fp8, stream);
+  // most groups a launch of this part can have (the grid is sized for them)
+  const long long gmax = part == 2 ? 1 : (part == 1 ? p.amax : p.amax + 1);
+  cudaError_t err = launch_mode<0>(p, gmax * (p.n_out / BM), fp8, stream);
   if (err != cudaSuccess) return err;
 
   p.K = s.inter;
   p.n_out = s.hidden;
-  return launch_mode<1>(p, (long long)(p.amax + 1) * (p.n_out / BM), fp8, stream);
+  return launch_mode<1>(p, gmax * (p.n_out / BM), fp8, stream);
 }
 
 }  // namespace qre

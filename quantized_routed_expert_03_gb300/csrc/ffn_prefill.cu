@@ -68,6 +68,8 @@ struct PrefillParams {
   int K;        // reduction length: H (gate/up) or I (down)
   int n_out;    // weight rows: 2I or H
   int amax;     // largest possible number of active experts
+  int part;     // groups: 0 routed + shared, 1 routed only, 2 shared only
+  int xrow0;    // expert_out row of Xg / h16 row 0 (P for the shared-only part, which keeps its own)
   const qre_slot* slots;
   const int32_t* offsets;
   const int32_t* active;
@@ -96,15 +98,19 @@ struct SmemLayout {
 
 // ---------------------------------------------------------------- gather
 
-__global__ void __launch_bounds__(256) gather_x_kernel(int T, int H, int k, const uint16_t* __restrict__ x,
+// Rows q in [q0, q1) of the pick order (q >= T*k: the shared expert's token q - T*k),
+// written at Xg row q - q0.
+__global__ void __launch_bounds__(256) gather_x_kernel(int T, int H, int k, long long q0, long long q1,
+                                                       const uint16_t* __restrict__ x,
                                                        const int32_t* __restrict__ perm, __half* __restrict__ xg,
                                                        int* status) {
   const long long P = (long long)T * k;
   const int per_row = H / 8;
   const long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x;
-  if (i >= (P + T) * per_row) return;
-  const long long q = i / per_row;
-  const int c = (int)(i - q * per_row) * 8;
+  if (i >= (q1 - q0) * per_row) return;
+  const long long qi = i / per_row;           // row within this launch's range
+  const int c = (int)(i - qi * per_row) * 8;  // first of the thread's 8 columns
+  const long long q = q0 + qi;
   const int t = q < P ? __ldg(perm + q) / k : (int)(q - P);
   const uint4 v = __ldg(reinterpret_cast<const uint4*>(x + (size_t)t * H + c));
   float f[8];
@@ -121,7 +127,7 @@ __global__ void __launch_bounds__(256) gather_x_kernel(int T, int H, int k, cons
     o[j] = h2_as_u32(h);
   }
   if (bad) set_status(status, QRE_DEV_FP16_RANGE);
-  *reinterpret_cast<uint4*>(xg + (size_t)q * H + c) = make_uint4(o[0], o[1], o[2], o[3]);
+  *reinterpret_cast<uint4*>(xg + (size_t)(q - q0) * H + c) = make_uint4(o[0], o[1], o[2], o[3]);
 }
 
 // ---------------------------------------------------------------- GEMM
@@ -200,9 +206,10 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_gemm_kernel(const Prefill
   const int mt_per = p.n_out / BM;
   const int KB = p.K / BK;
 
-  int n_act = *p.n_active;
+  // groups: the active experts (parts 0, 1), then the shared one (parts 0, 2)
+  int n_act = p.part == 2 ? 0 : *p.n_active;
   n_act = n_act < 0 ? 0 : (n_act > p.amax ? p.amax : n_act);
-  const int ngroups = n_act + 1;
+  const int ngroups = n_act + (p.part == 1 ? 0 : 1);
 
   // group table: rows, tokens and first tile of every group (one warp)
   if (warp == 0) {
@@ -278,7 +285,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_gemm_kernel(const Prefill
           const int s = it % NSTAGE;
           if (!mbar_wait_bounded(&empty[s], ((it / NSTAGE) & 1) ^ 1, abort_flag, p.status, p.wait_ns)) goto b_done;
           mbar_arrive_expect_tx(&full_b[s], B_STAGE);
-          tma_load_2d(Bs + (size_t)s * B_STAGE, &tmap_b, kb * BK, tl.row0 + tl.n0, &full_b[s]);
+          tma_load_2d(Bs + (size_t)s * B_STAGE, &tmap_b, kb * BK, tl.row0 + tl.n0 - p.xrow0, &full_b[s]);
         }
       }
     b_done:
@@ -466,7 +473,8 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_gemm_kernel(const Prefill
               const int s0 = (lane >> 2) & 1;
               const uint4 lo = *reinterpret_cast<const uint4*>(scratch + lane * 32 + s0 * 16);
               const uint4 hi = *reinterpret_cast<const uint4*>(scratch + lane * 32 + (s0 ^ 1) * 16);
-              uint4* dst = reinterpret_cast<uint4*>(p.h16 + (size_t)(tl.row0 + tl.n0 + n) * p.I + tl.m0 / 2 + 16 * q);
+              uint4* dst = reinterpret_cast<uint4*>(p.h16 + (size_t)(tl.row0 + tl.n0 + n - p.xrow0) * p.I +
+                                                    tl.m0 / 2 + 16 * q);
               dst[0] = lo;
               dst[1] = hi;
             }
@@ -537,6 +545,10 @@ size_t ffn_prefill_ws_bytes(const qre_layer_shape& s, int T) {
   return align256(rows * s.hidden * 2) + align256(rows * s.inter * 2);
 }
 
+size_t ffn_prefill_shared_ws_bytes(const qre_layer_shape& s, int T) {
+  return align256((size_t)T * s.hidden * 2) + align256((size_t)T * s.inter * 2);
+}
+
 // Weight-ring stages that fit next to everything else in shared memory.
 int weight_stages(int E) {
   const long long spare = (long long)device_max_smem_optin() - (long long)SmemLayout::bytes(E, 0);
@@ -552,15 +564,20 @@ bool ffn_prefill_supported(const qre_layer_shape& s) {
 cudaError_t launch_ffn_prefill(const qre_layer_shape& s, int T, const uint16_t* x, const qre_slot* slots,
                                const int32_t* offsets, const int32_t* perm, const int32_t* active,
                                const int32_t* n_active, float* expert_out, void* ws, int* status,
-                               cudaStream_t stream) {
+                               cudaStream_t stream, int part) {
   const long long P = (long long)T * s.top_k;
-  const long long rows = P + T;
+  // Xg / h16 rows: the pick rows and/or the shared rows of this part; the
+  // shared-only part keeps its T rows in a workspace of its own
+  const long long q0 = part == kFfnShared ? P : 0, q1 = part == kFfnRouted ? P : P + T;
+  const long long rows = part == kFfnShared ? T : P + T;
   __half* xg = static_cast<__half*>(ws);
   __half* h16 = reinterpret_cast<__half*>(static_cast<uint8_t*>(ws) + align256((size_t)rows * s.hidden * 2));
 
   {
-    const long long n = rows * (s.hidden / 8);
-    gather_x_kernel<<<(unsigned)((n + 255) / 256), 256, 0, stream>>>(T, s.hidden, s.top_k, x, perm, xg, status);
+    const long long n = (q1 - q0) * (s.hidden / 8);
+    if (n > 0)
+      gather_x_kernel<<<(unsigned)((n + 255) / 256), 256, 0, stream>>>(T, s.hidden, s.top_k, q0, q1, x, perm, xg,
+                                                                       status);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
   }
@@ -582,6 +599,8 @@ cudaError_t launch_ffn_prefill(const qre_layer_shape& s, int T, const uint16_t* 
   p.h16 = h16;
   p.expert_out = expert_out;
   p.status = status;
+  p.part = part;
+  p.xrow0 = (int)q0;
   p.wait_ns = wait_limit_ns();
   p.stall_ns = test_stall_ns();
   p.wst = weight_stages(s.n_experts);

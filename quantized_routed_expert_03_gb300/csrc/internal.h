@@ -19,6 +19,12 @@ constexpr int kDecodeMaxTokens = 8;
 size_t route_ws_bytes(const qre_layer_shape& s, int T);
 size_t dispatch_ws_bytes(const qre_layer_shape& s, int T);
 size_t ffn_ws_bytes(const qre_layer_shape& s, int T);
+// The shared-expert-only FFN call keeps its own, smaller workspace.
+size_t ffn_shared_ws_bytes(const qre_layer_shape& s, int T);
+size_t ffn_prefill_shared_ws_bytes(const qre_layer_shape& s, int T);
+
+// Which groups an expert-FFN launch computes.
+enum FfnPart { kFfnAll = 0, kFfnRouted = 1, kFfnShared = 2 };
 
 // Limit of the kernels' pipeline waits in ns (one second unless a test lowered
 // it with qre_debug_wait_test), and the test hook's stall (0 = off).
@@ -78,7 +84,7 @@ cudaError_t launch_dispatch(const qre_layer_shape& s, int T, const int32_t* topk
 cudaError_t launch_ffn_decode(const qre_layer_shape& s, int T, const uint16_t* x, const qre_slot* slots,
                               const int32_t* offsets, const int32_t* perm, const int32_t* active,
                               const int32_t* n_active, float* expert_out, void* ws, int* status,
-                              cudaStream_t stream);
+                              cudaStream_t stream, int part = kFfnAll);
 bool ffn_decode_supported(const qre_layer_shape& s);
 
 // Grouped-GEMM expert FFN for T > kDecodeMaxTokens (tcgen05, TMEM, TMA).
@@ -87,7 +93,7 @@ bool ffn_prefill_supported(const qre_layer_shape& s);
 cudaError_t launch_ffn_prefill(const qre_layer_shape& s, int T, const uint16_t* x, const qre_slot* slots,
                                const int32_t* offsets, const int32_t* perm, const int32_t* active,
                                const int32_t* n_active, float* expert_out, void* ws, int* status,
-                               cudaStream_t stream);
+                               cudaStream_t stream, int part = kFfnAll);
 
 cudaError_t launch_cache_update(int E, int S, float decay, const int32_t* active, const int32_t* n_active,
                                 float* scores, int32_t* slot_expert, int32_t* expert_slot, const qre_slot* home,

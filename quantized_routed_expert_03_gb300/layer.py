@@ -8,7 +8,10 @@ call into libqre.so through the binding in ``__init__``.
   reads zero-copy (the glm53-flash-offload README, "Zero-copy home": one
   exact-size pinned arena per layer).
 * :class:`MoELayer` owns the per-call buffers and the device slot table, and
-  runs route -> dispatch -> expert FFN -> combine on one stream.
+  runs route -> dispatch -> expert FFN -> combine on one stream, or with the
+  shared expert on a second stream beside the router and the dispatch (the
+  glm53-flash-offload README, "Decode kernels": the shared expert on a side
+  stream); both give the same bits.
 """
 
 from __future__ import annotations
@@ -17,8 +20,9 @@ import ctypes
 
 import torch
 
-from . import (make_shape, qre_combine, qre_dispatch, qre_expert_ffn, qre_quantize, qre_quantize_gate_up,
-               qre_route, qre_slot, qre_validate_slots, qre_workspace_size, slot_array)
+from . import (make_shape, qre_combine, qre_dispatch, qre_expert_ffn, qre_expert_ffn_routed, qre_expert_ffn_shared,
+               qre_quantize, qre_quantize_gate_up, qre_route, qre_shared_workspace_size, qre_slot,
+               qre_validate_slots, qre_workspace_size, slot_array)
 
 _ALIGN = 256
 
@@ -134,6 +138,8 @@ class MoELayer:
         self.workspace = torch.empty(max(self.ws_bytes, 256), dtype=torch.uint8, device=dev)
         self.slots = torch.zeros((E + 1) * ctypes.sizeof(qre_slot), dtype=torch.uint8, device=dev)
         self.host_slots = None
+        self.shared_ws = None          # workspace of the side-stream shared expert, allocated on first use
+        self._fork = self._join = None
 
     def set_slots(self, entries, validate: bool = True) -> None:
         """entries: E + 1 tuples (w_gate_up, s_gate_up, w_down, s_down, tier); entry E is the shared expert."""
@@ -156,15 +162,45 @@ class MoELayer:
         qre_expert_ffn(self.shape, T, x, self.slots, self.offsets, self.perm, self.active, self.n_active,
                        self.expert_out, self.workspace, self.ws_bytes, stream)
 
+    def expert_ffn_routed(self, x, T, stream=None):
+        qre_expert_ffn_routed(self.shape, T, x, self.slots, self.offsets, self.perm, self.active, self.n_active,
+                              self.expert_out, self.workspace, self.ws_bytes, stream)
+
+    def expert_ffn_shared(self, x, T, stream=None):
+        if self.shared_ws is None:
+            n = qre_shared_workspace_size(self.shape, self.t_max)
+            self.shared_ws = torch.empty(max(n, 256), dtype=torch.uint8, device=self.device)
+        qre_expert_ffn_shared(self.shape, T, x, self.slots, self.expert_out, self.shared_ws, None, stream)
+
     def combine(self, T, stream=None, bf16: bool = True):
         qre_combine(self.shape, T, self.expert_out, self.topk_w, self.inv_perm, self.y,
                     self.y_bf16 if bf16 else None, stream)
 
-    def forward(self, x, w_router, bias, T=None, stream=None):
-        """Runs the whole layer on ``x`` ([T, H] bf16, device); results stay in the buffers."""
+    def forward(self, x, w_router, bias, T=None, stream=None, shared_stream=None):
+        """Runs the whole layer on ``x`` ([T, H] bf16, device); results stay in the buffers.
+
+        With ``shared_stream`` (a torch.cuda.Stream) the shared expert runs there,
+        forked after ``x`` is ready and joined before the combine; the routed
+        experts, router and dispatch stay on ``stream`` (default: the current one).
+        The output bits are the same either way.  Works inside CUDA graph capture.
+        """
         T = x.shape[0] if T is None else T
-        self.route(x, w_router, bias, T, stream)
-        self.dispatch(T, stream)
-        self.expert_ffn(x, T, stream)
-        self.combine(T, stream)
+        if shared_stream is None:
+            self.route(x, w_router, bias, T, stream)
+            self.dispatch(T, stream)
+            self.expert_ffn(x, T, stream)
+            self.combine(T, stream)
+            return self.y[:T]
+        main = stream if stream is not None else torch.cuda.current_stream(self.device)
+        if self._fork is None:
+            self._fork, self._join = torch.cuda.Event(), torch.cuda.Event()
+        self._fork.record(main)
+        shared_stream.wait_event(self._fork)
+        self.expert_ffn_shared(x, T, shared_stream)
+        self._join.record(shared_stream)
+        self.route(x, w_router, bias, T, main)
+        self.dispatch(T, main)
+        self.expert_ffn_routed(x, T, main)
+        main.wait_event(self._join)
+        self.combine(T, main)
         return self.y[:T]

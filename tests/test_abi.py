@@ -161,3 +161,15 @@ def test_wait_test_hook_checks_its_arguments(lib):
     st, msg = _status(lambda: qre.qre_debug_wait_test(0, 500_000_000))
     assert st == qre.QRE_ERR_INVALID_ARG and "stall_ns" in msg
     qre.qre_debug_wait_test(0, 0)      # the defaults
+
+
+def test_split_expert_ffn_checks_its_arguments(lib):
+    shape = _shape()
+    n = qre.qre_shared_workspace_size(shape, 1)
+    assert n >= 2 * 8 * 2048 * 2
+    assert qre.qre_shared_workspace_size(shape, 4096) >= 4096 * (4096 + 2048) * 2
+    st, msg = _status(lambda: qre.qre_expert_ffn_shared(shape, 1, None, 16, 16, 16, n, stream=0))
+    assert st == qre.QRE_ERR_INVALID_ARG and "x_bf16" in msg
+    st, msg = _status(lambda: qre.qre_expert_ffn_routed(shape, 1, 16, 16, None, 16, 16, 16, 16, 16, 1 << 30,
+                                                        stream=0))
+    assert st == qre.QRE_ERR_INVALID_ARG and "offsets" in msg

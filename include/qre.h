@@ -340,6 +340,31 @@ QRE_API qre_status qre_cache_copy(const qre_layer_shape* shape, const qre_slot* 
                                   qre_stream_t stream);
 
 /*
+ * Prefill staging: a prefill chunk touches nearly every expert of a layer, so
+ * the experts that live in host memory are copied into HBM one layer ahead on
+ * a copy stream, and the FFN reads the staged copies (the RTX PRO 6000
+ * recipe's config.expert_cache.mechanism, prefill staging; the
+ * glm53-flash-offload README, "Prefill staging").  For each entry e of the
+ * layer's slot table with tier 1, in ascending e while staging slots remain,
+ * the expert's four arrays are copied with cudaMemcpyAsync (the copy engines,
+ * leaving the SMs to the computation) into the next staging slot, and the staged
+ * table's entry e points there (tier 0); every other entry is copied as it is.
+ *   host_table    [E+1] qre_slot, HOST: the layer's table
+ *   host_staging  [n_staging] qre_slot, HOST: the staging slots (device memory, tier 0)
+ *   host_out      [E+1] qre_slot, HOST, written by this call and uploaded on the
+ *                 stream: keep it unchanged until the stream has passed the call
+ *                 (pinned memory keeps the upload asynchronous)
+ *   table_out     [E+1] qre_slot, DEVICE: the staged table (written on the stream)
+ *   n_staged      host int32: experts staged (the rest of tier 1 stays host-mapped)
+ * The staging slots must not be in use by a kernel that runs concurrently (use
+ * two staging areas to stage layer l+1 while layer l computes).  Works inside
+ * CUDA graph capture (the copies and the upload become graph nodes).
+ */
+QRE_API qre_status qre_stage_experts(const qre_layer_shape* shape, const qre_slot* host_table,
+                                     const qre_slot* host_staging, int32_t n_staging, qre_slot* host_out,
+                                     qre_slot* table_out, int32_t* n_staged, qre_stream_t stream);
+
+/*
  * Checks a HOST copy of a slot table before it is uploaded: every pointer
  * non-null and 16-byte aligned, reserved == 0, tier in {0, 1}, tier-0
  * pointers in device memory and tier-1 pointers in host memory that the

@@ -41,7 +41,7 @@ EXPORTS = (
     "qre_route", "qre_dispatch", "qre_expert_ffn", "qre_combine", "qre_validate_slots",
     "qre_cache_update", "qre_cache_copy",
     "qre_read_device_status", "qre_clear_device_status", "qre_route_noalloc", "qre_debug_wait_test",
-    "qre_expert_ffn_routed", "qre_expert_ffn_shared", "qre_shared_workspace_size",
+    "qre_expert_ffn_routed", "qre_expert_ffn_shared", "qre_shared_workspace_size", "qre_stage_experts",
 )
 
 
@@ -90,6 +90,8 @@ _SIGS = {
     "qre_expert_ffn_routed": ([_SHAPE, _I32, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _SZ, _VP], ctypes.c_int),
     "qre_expert_ffn_shared": ([_SHAPE, _I32, _VP, _VP, _VP, _VP, _SZ, _VP], ctypes.c_int),
     "qre_shared_workspace_size": ([_SHAPE, _I32, ctypes.POINTER(ctypes.c_size_t)], ctypes.c_int),
+    "qre_stage_experts": ([_SHAPE, ctypes.POINTER(qre_slot), ctypes.POINTER(qre_slot), _I32, _VP, _VP,
+                           ctypes.POINTER(ctypes.c_int32), _VP], ctypes.c_int),
 }
 
 
@@ -241,6 +243,18 @@ def qre_cache_update(shape, n_slots, decay, active, n_active, scores, expert_slo
 def qre_cache_copy(shape, home, slot_mem, copy_list, n_copies, max_copies, stream=None) -> None:
     _check(load_library().qre_cache_copy(ctypes.byref(shape), _ptr(home), _ptr(slot_mem), _ptr(copy_list),
                                          _ptr(n_copies), max_copies, _stream(stream)), "qre_cache_copy")
+
+
+def qre_stage_experts(shape, host_table, host_staging, host_out, table_out, stream=None) -> int:
+    """Stages the host-resident experts of ``host_table`` (ctypes qre_slot array) into
+    ``host_staging`` slots; ``host_out``: a host buffer of (E + 1) qre_slot (an int
+    address or a tensor, kept alive until the stream passes the call); returns the
+    number of experts staged."""
+    n = ctypes.c_int32(0)
+    _check(load_library().qre_stage_experts(ctypes.byref(shape), host_table, host_staging, len(host_staging),
+                                            _ptr(host_out), _ptr(table_out), ctypes.byref(n), _stream(stream)),
+           "qre_stage_experts")
+    return n.value
 
 
 def qre_validate_slots(shape, host_slots) -> None:

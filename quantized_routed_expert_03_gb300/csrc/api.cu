@@ -384,6 +384,61 @@ qre_status qre_cache_copy(const qre_layer_shape* shape, const qre_slot* home, co
                   "qre_cache_copy launch");
 }
 
+qre_status qre_stage_experts(const qre_layer_shape* shape, const qre_slot* host_table, const qre_slot* host_staging,
+                             int32_t n_staging, qre_slot* host_out, qre_slot* table_out, int32_t* n_staged,
+                             qre_stream_t stream) {
+  qre_status st = check_shape(shape, 0);
+  if (st != QRE_OK) return st;
+  if (!host_table || !host_out || !n_staged) return fail(QRE_ERR_INVALID_ARG, "host_table, host_out and n_staged must be non-NULL");
+  if (n_staging < 0 || (n_staging > 0 && !host_staging))
+    return fail(QRE_ERR_INVALID_ARG, "n_staging %d with host_staging %p", n_staging, (const void*)host_staging);
+  QRE_REQUIRE_PTR(table_out);
+  const char* names[4] = {"w_gate_up", "s_gate_up", "w_down", "s_down"};
+  const size_t H = shape->hidden, I = shape->inter, G = shape->group;
+  const size_t bytes[4] = {I * H, 2 * I * (H / G) * 2, H * I / 2, H * (I / G) * 2};
+  for (int j = 0; j < n_staging; ++j) {
+    const qre_slot& s = host_staging[j];
+    const void* ptrs[4] = {s.w_gate_up, s.s_gate_up, s.w_down, s.s_down};
+    if (s.tier != 0 || s.reserved != 0) return fail(QRE_ERR_INVALID_ARG, "staging slot %d: tier must be 0", j);
+    for (int i = 0; i < 4; ++i) {
+      if (!ptrs[i]) return fail(QRE_ERR_INVALID_ARG, "staging slot %d: %s is NULL", j, names[i]);
+      if (misaligned(ptrs[i])) return fail(QRE_ERR_MISALIGNED, "staging slot %d: %s is not 16-byte aligned", j, names[i]);
+    }
+  }
+  for (int e = 0; e <= shape->n_experts; ++e) {
+    const qre_slot& s = host_table[e];
+    if (s.tier > 1 || s.reserved != 0) return fail(QRE_ERR_INVALID_ARG, "slot %d: tier %u / reserved %u", e, s.tier, s.reserved);
+    if (s.tier == 1) {
+      const void* ptrs[4] = {s.w_gate_up, s.s_gate_up, s.w_down, s.s_down};
+      for (int i = 0; i < 4; ++i)
+        if (!ptrs[i] || misaligned(ptrs[i]))
+          return fail(QRE_ERR_INVALID_ARG, "slot %d: %s is NULL or not 16-byte aligned", e, names[i]);
+    }
+  }
+  cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
+  int j = 0;
+  for (int e = 0; e <= shape->n_experts; ++e) {
+    const qre_slot& s = host_table[e];
+    host_out[e] = s;
+    if (s.tier != 1 || j >= n_staging) continue;
+    const qre_slot& d = host_staging[j];
+    const void* src[4] = {s.w_gate_up, s.s_gate_up, s.w_down, s.s_down};
+    const void* dst[4] = {d.w_gate_up, d.s_gate_up, d.w_down, d.s_down};
+    for (int i = 0; i < 4; ++i) {
+      const cudaError_t err = cudaMemcpyAsync(const_cast<void*>(dst[i]), src[i], bytes[i], cudaMemcpyDefault, cs);
+      if (err != cudaSuccess) return cuda_fail(err, "qre_stage_experts: copy");
+    }
+    host_out[e] = d;
+    ++j;
+  }
+  const cudaError_t err =
+      cudaMemcpyAsync(table_out, host_out, (size_t)(shape->n_experts + 1) * sizeof(qre_slot), cudaMemcpyHostToDevice, cs);
+  if (err != cudaSuccess) return cuda_fail(err, "qre_stage_experts: table upload");
+  *n_staged = j;
+  g_err[0] = '\0';
+  return QRE_OK;
+}
+
 qre_status qre_validate_slots(const qre_layer_shape* shape, const qre_slot* host_slots) {
   qre_status st = check_shape(shape, 0);
   if (st != QRE_OK) return st;

@@ -22,7 +22,7 @@ import torch
 
 from . import (make_shape, qre_combine, qre_dispatch, qre_expert_ffn, qre_expert_ffn_routed, qre_expert_ffn_shared,
                qre_quantize, qre_quantize_gate_up, qre_route, qre_shared_workspace_size, qre_slot,
-               qre_validate_slots, qre_workspace_size, slot_array)
+               qre_stage_experts, qre_validate_slots, qre_workspace_size, slot_array)
 
 _ALIGN = 256
 
@@ -158,9 +158,10 @@ class MoELayer:
         qre_dispatch(self.shape, T, self.topk_idx, self.counts, self.offsets, self.perm, self.inv_perm, self.active,
                      self.n_active, self.workspace, self.ws_bytes, stream)
 
-    def expert_ffn(self, x, T, stream=None):
-        qre_expert_ffn(self.shape, T, x, self.slots, self.offsets, self.perm, self.active, self.n_active,
-                       self.expert_out, self.workspace, self.ws_bytes, stream)
+    def expert_ffn(self, x, T, stream=None, slots=None):
+        """slots: another device slot table for this call (a staged one), default the layer's."""
+        qre_expert_ffn(self.shape, T, x, self.slots if slots is None else slots, self.offsets, self.perm,
+                       self.active, self.n_active, self.expert_out, self.workspace, self.ws_bytes, stream)
 
     def expert_ffn_routed(self, x, T, stream=None):
         qre_expert_ffn_routed(self.shape, T, x, self.slots, self.offsets, self.perm, self.active, self.n_active,
@@ -176,7 +177,7 @@ class MoELayer:
         qre_combine(self.shape, T, self.expert_out, self.topk_w, self.inv_perm, self.y,
                     self.y_bf16 if bf16 else None, stream)
 
-    def forward(self, x, w_router, bias, T=None, stream=None, shared_stream=None):
+    def forward(self, x, w_router, bias, T=None, stream=None, shared_stream=None, slots=None):
         """Runs the whole layer on ``x`` ([T, H] bf16, device); results stay in the buffers.
 
         With ``shared_stream`` (a torch.cuda.Stream) the shared expert runs there,
@@ -188,9 +189,10 @@ class MoELayer:
         if shared_stream is None:
             self.route(x, w_router, bias, T, stream)
             self.dispatch(T, stream)
-            self.expert_ffn(x, T, stream)
+            self.expert_ffn(x, T, stream, slots)
             self.combine(T, stream)
             return self.y[:T]
+        assert slots is None, "a staged table is not combined with the side-stream shared expert here"
         main = stream if stream is not None else torch.cuda.current_stream(self.device)
         if self._fork is None:
             self._fork, self._join = torch.cuda.Event(), torch.cuda.Event()
@@ -204,3 +206,59 @@ class MoELayer:
         main.wait_event(self._join)
         self.combine(T, main)
         return self.y[:T]
+
+
+class StagingArea:
+    """HBM slots that hold one layer's host-resident experts during a prefill chunk.
+
+    ``stage(layer, stream)`` copies the layer's tier-1 experts into the slots on
+    ``stream`` (copy engines) and leaves a staged slot table in ``self.table``
+    (device) that points at them.  Use two areas to stage layer l + 1 while layer
+    l computes (:func:`staged_prefill`).
+    """
+
+    def __init__(self, H: int, I: int, G: int, E: int, n_slots: int, device="cuda"):
+        self.E = E
+        self.arena = ExpertArena(H, I, G, n_slots, device=device)
+        self.host_staging = slot_array([self.arena.addresses(j) + (0,) for j in range(n_slots)])
+        self.table = torch.zeros((E + 1) * ctypes.sizeof(qre_slot), dtype=torch.uint8, device=device)
+        self.n_staged = 0
+
+    def stage(self, layer: "MoELayer", stream=None) -> int:
+        if getattr(layer, "stage_host_out", None) is None:   # per layer: stays valid while its upload is queued
+            layer.stage_host_out = torch.empty((layer.E + 1) * ctypes.sizeof(qre_slot), dtype=torch.uint8,
+                                               pin_memory=True)
+        self.n_staged = qre_stage_experts(layer.shape, layer.host_slots, self.host_staging, layer.stage_host_out,
+                                          self.table, stream)
+        return self.n_staged
+
+
+def staged_prefill(layers, inputs, areas, copy_stream, T, stream=None):
+    """A prefill chunk through a stack of layers with each layer's host-resident
+    experts staged into HBM one layer ahead on ``copy_stream``.
+
+    layers: MoELayer objects; inputs: (x, w_router, bias) per layer (the layers are
+    independent here: between MoE layers a model has attention, which is not this
+    library's); areas: two StagingArea objects used alternately.  Ordering: layer l
+    waits for its area's copies; the copies into an area wait until the layer that
+    last read it has finished its expert FFN.  Works inside CUDA graph capture.
+    """
+    main = stream if stream is not None else torch.cuda.current_stream()
+    staged = [torch.cuda.Event() for _ in areas]
+    freed = [torch.cuda.Event() for _ in areas]
+    copy_stream.wait_stream(main)
+    areas[0].stage(layers[0], copy_stream)
+    staged[0].record(copy_stream)
+    for l, L in enumerate(layers):
+        a = l % 2
+        if l + 1 < len(layers):
+            b = (l + 1) % 2
+            if l >= 1:
+                copy_stream.wait_event(freed[b])
+            areas[b].stage(layers[l + 1], copy_stream)
+            staged[b].record(copy_stream)
+        main.wait_event(staged[a])
+        x, wr, bias = inputs[l]
+        L.forward(x, wr, bias, T, stream=main, slots=areas[a].table)
+        freed[a].record(main)
+    main.wait_stream(copy_stream)

@@ -173,3 +173,15 @@ def test_split_expert_ffn_checks_its_arguments(lib):
     st, msg = _status(lambda: qre.qre_expert_ffn_routed(shape, 1, 16, 16, None, 16, 16, 16, 16, 16, 1 << 30,
                                                         stream=0))
     assert st == qre.QRE_ERR_INVALID_ARG and "offsets" in msg
+
+
+def test_stage_experts_checks_its_arguments(lib):
+    shape = _shape(n_experts=4, top_k=2)
+    table = qre.slot_array([(16, 16, 16, 16, 0)] * 5)
+    bad_staging = qre.slot_array([(16, 16, 16, 16, 1)])
+    st, msg = _status(lambda: qre.qre_stage_experts(shape, table, bad_staging, 16, 16, stream=0))
+    assert st == qre.QRE_ERR_INVALID_ARG and "staging slot 0" in msg
+    bad_table = qre.slot_array([(16, 16, 16, 16, 0)] * 4 + [(0, 16, 16, 16, 1)])
+    st, msg = _status(lambda: qre.qre_stage_experts(shape, bad_table, qre.slot_array([(16, 16, 16, 16, 0)]), 16, 16,
+                                                    stream=0))
+    assert st == qre.QRE_ERR_INVALID_ARG and "slot 4" in msg

@@ -13,6 +13,7 @@ Workloads (``--workload``):
   decode1           H4096 I2048 E288 top-8 + shared, T = 1, all 289 experts in HBM
   decode8_zipf_x42  T = 8, Zipf(1.1) routing bias, 42 distinct layers
   cache4_x42        T = 4, Zipf(1.1), 42 layers, 100 experts/layer in pinned host memory
+  cache4_live_x16   the same layout with the 148 HBM slots as a live LFU cache, 16 layers
   prefill8192       T = 8192 tokens through one layer (tcgen05 grouped GEMM)
   tiny              H256 I128 E16 top-4 + shared, T = 4
 The line's top level is the ``--workload`` (decode1 by default); the workloads
@@ -125,6 +126,39 @@ def load_peaks():
     return dict(FALLBACK_PEAKS), "fallback"
 
 
+def read_probe_gbs(buf, reps=5) -> float:
+    """Best read rate in GB/s of qre_read_probe over ``buf`` (a device tensor or a
+    pinned host tensor, read zero-copy), CUDA events around each call."""
+    import torch
+    import quantized_routed_expert_03_gb300 as qre
+    sink = torch.zeros(4, dtype=torch.int32, device="cuda")
+    nbytes = buf.numel() * buf.element_size() // 16 * 16
+    qre.qre_read_probe(buf.data_ptr(), nbytes, sink)
+    best = float("inf")
+    for _ in range(reps):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        qre.qre_read_probe(buf.data_ptr(), nbytes, sink)
+        e1.record()
+        torch.cuda.synchronize()
+        best = min(best, e0.elapsed_time(e1))
+    return nbytes / (best / 1e3) / 1e9
+
+
+def link_peaks(device) -> dict:
+    """Host-link (1 GiB pinned host buffer read zero-copy) and device-memory (4 GiB)
+    read rates of the library's streaming-read kernel."""
+    import torch
+    host = torch.empty(1 << 30, dtype=torch.uint8, pin_memory=True)
+    host.fill_(1)
+    dev = torch.ones(4 << 30, dtype=torch.uint8, device=device)
+    out = {"host_link_read_gbs": round(read_probe_gbs(host), 1), "hbm_read_gbs": round(read_probe_gbs(dev), 1),
+           "probe": "qre_read_probe: 16-byte streaming loads, 8 in flight per thread, 4 CTAs of 512 threads per SM; "
+                    "1 GiB pinned host buffer read zero-copy / 4 GiB device buffer; best of 5"}
+    del host, dev
+    return out
+
+
 def default_sets(cfg) -> int:
     """Distinct layer weight sets the steps rotate over: a stack has its own
     layers; one decode layer is repeated in 8 copies (30 GB, far more than L2); a
@@ -225,6 +259,11 @@ class Workload:
         self.sets = []
         staging = None
         for r in range(n_sets):
+            if cfg.live_cache:
+                self.sets.append(self._live_set(cfg, r, device))
+                if (r + 1) % 8 == 0:
+                    log(f"[bench] {name}: built {r + 1}/{n_sets} layers ({time.time() - t0:.0f} s)")
+                continue
             host = np.append(synthetic.host_resident(cfg, r), False)
             n_host = int(host.sum())
             dev = ExpertArena(H, I, G, E + 1 - n_host, device=device)
@@ -256,6 +295,65 @@ class Workload:
         self.build_s = time.time() - t0
         log(f"[bench] {name}: weights ready, {n_sets} layer set(s), {self.build_s:.1f} s")
 
+    def _live_set(self, cfg, r, device):
+        """One layer with a live expert cache: ranks 1-40 (and the shared expert) in
+        static HBM, cfg.hbm_slots - 40 HBM slots run by qre_cache_update /
+        qre_cache_copy (first holding ranks 41..hbm_slots), and every non-static
+        expert's home copy in pinned host memory."""
+        import torch
+        import quantized_routed_expert_03_gb300 as qre
+        from quantized_routed_expert_03_gb300.layer import ExpertArena, MoELayer
+        H, I, E, k, G, T = cfg.hidden, cfg.inter, cfg.n_experts, cfg.top_k, cfg.group, cfg.tokens
+        S = cfg.hbm_slots - cfg.static_slots
+        ranks = synthetic.popularity_ranks(E, cfg.seed, r)
+        static = ranks <= cfg.static_slots
+        n_home = int((~static).sum())
+        st_arena = ExpertArena(H, I, G, int(static.sum()) + 1, device=device)
+        slots = ExpertArena(H, I, G, S, device=device)
+        home = ExpertArena(H, I, G, n_home, host=True)
+        staging = torch.empty(home.layout["stride"], dtype=torch.uint8, device=device)
+        table, home_entries = [None] * (E + 1), [None] * (E + 1)
+        expert_slot = np.full(E, -1, np.int32)
+        slot_expert = np.full(S, -1, np.int32)
+        si = hi = 0
+        for e in range(E + 1):
+            wg, wu, wd = synthetic.expert_fp32_torch(H, I, cfg.seed, r, e, device)
+            if e == E or static[e]:
+                st_arena.quantize_into(si, wg, wu, wd)
+                table[e] = home_entries[e] = st_arena.addresses(si) + (0,)
+                if e < E:
+                    expert_slot[e] = -2
+                si += 1
+            else:
+                home.quantize_into(hi, wg, wu, wd, staging=staging)
+                home_entries[e] = home.addresses(hi) + (1,)
+                table[e] = home_entries[e]
+                s = int(ranks[e]) - cfg.static_slots - 1
+                if s < S:                       # initially cached: its weights in slot s
+                    slots.quantize_into(s, wg, wu, wd)
+                    table[e] = slots.addresses(s) + (0,)
+                    expert_slot[e], slot_expert[s] = s, e
+                hi += 1
+            del wg, wu, wd
+        L = MoELayer(H, I, E, k, G, T, device=device)
+        L.set_slots(table)
+
+        def dev_slots(entries):
+            raw = bytearray(memoryview(qre.slot_array(entries)).cast("B"))
+            return torch.frombuffer(raw, dtype=torch.uint8).to(device)
+        max_copies = 16
+        cache = {"home": dev_slots(home_entries), "slot_mem": dev_slots([slots.addresses(s) + (0,) for s in range(S)]),
+                 "scores": torch.zeros(E, dtype=torch.float32, device=device),
+                 "expert_slot": torch.from_numpy(expert_slot).to(device),
+                 "slot_expert": torch.from_numpy(slot_expert).to(device),
+                 "copy_list": torch.zeros(2 * max_copies, dtype=torch.int32, device=device),
+                 "n_copies": torch.zeros(4, dtype=torch.int32, device=device), "S": S, "max_copies": max_copies}
+        wr = torch.from_numpy(synthetic.router_weights(E, H, cfg.seed, r)).to(device)
+        bias = torch.from_numpy(synthetic.zipf_bias(E, cfg.seed, r)).to(device)
+        host_mask = np.append(~static, False)
+        return {"layer": L, "dev": st_arena, "host": home, "slots_arena": slots, "wr": wr, "bias": bias,
+                "n_host": n_home, "host_mask": host_mask, "cache": cache}
+
     def x_pool(self, n, device):
         """n distinct activation batches per layer set, [n_sets][n][T,H] bf16 on device."""
         import torch
@@ -270,8 +368,12 @@ class Workload:
 def measure_workload(name, args, K, W, rank, local_rank, world, device, log, cpu_leg=True):
     """Times K steps of one workload (after W warm-up steps) and returns its record."""
     import torch
+    import quantized_routed_expert_03_gb300 as qre
     wl = Workload(name, device, n_sets=args.sets if name == args.workload else None, log=log)
     cfg, T, H, k = wl.cfg, wl.T, wl.cfg.hidden, wl.cfg.top_k
+    # host-mapped experts in the tables: cut the decode work at equal cost
+    host_cost = args.host_unit_cost if args.host_unit_cost is not None else (4 if cfg.host_tier else 0)
+    qre.qre_set_host_unit_cost(host_cost)
     stream = torch.cuda.Stream(device)
 
     # one captured unit = `per_graph` steps; each step covers one layer set
@@ -279,28 +381,38 @@ def measure_workload(name, args, K, W, rank, local_rank, world, device, log, cpu
     stack = wl.layers_per_step > 1
     prefill = T > 8
     per_graph = 1 if (stack or prefill) else wl.n_sets * 4
-    n_x = 4 if stack else (2 if prefill else per_graph // wl.n_sets)
+    # a live cache must see fresh routing every step (a short cycle of batches
+    # would let it learn the cycle): one batch per step, warm-up and miss count
+    n_x = min(K + W + 16, 256) if cfg.live_cache else (4 if stack else (2 if prefill else per_graph // wl.n_sets))
     xs = wl.x_pool(n_x, device)
 
     side = torch.cuda.Stream(device) if args.side_stream else None
 
     def one_layer(s, x):
-        L = s["layer"]
-        if side is not None:   # the shared expert on a second stream (fork/join inside the graph)
-            L.forward(x, s["wr"], s["bias"], T, stream=stream, shared_stream=side)
-            return
-        L.route(x, s["wr"], s["bias"], T)
-        L.dispatch(T)
-        L.expert_ffn(x, T)
-        L.combine(T)
+        layer_step(s, x, T, stream, side)
+
+    # live cache: the captured step reads a static input that each step refills
+    # from the pool with one device copy (inside the timed region)
+    live = cfg.live_cache
+    if live:
+        pool = torch.stack([torch.stack([xs[r][j] for r in range(wl.n_sets)]) for j in range(n_x)])
+        x_static = pool[0].clone()
 
     def step_fn(j):
-        if stack:
+        if live:
+            for r, s in enumerate(wl.sets):
+                one_layer(s, x_static[r])
+        elif stack:
             for r, s in enumerate(wl.sets):
                 one_layer(s, xs[r][j % n_x])
         else:
             r = j % wl.n_sets
             one_layer(wl.sets[r], xs[r][(j // wl.n_sets) % n_x])
+
+    def replay(g, j):
+        if live:
+            x_static.copy_(pool[j % n_x])
+        g.replay()
 
     # eager warm-up (sets kernel attributes, loads modules) then capture
     with torch.cuda.stream(stream):
@@ -321,13 +433,14 @@ def measure_workload(name, args, K, W, rank, local_rank, world, device, log, cpu
 
     # warm-up replays: at least W steps, and every graph the timed region replays has run before
     warm = 0
-    while warm < W or (g_full is not None and warm == 0):
-        if g_full is not None:
-            g_full.replay()
-            warm += per_graph
-        if g_rem is not None:
-            g_rem.replay()
-            warm += rem
+    with torch.cuda.stream(stream):
+        while warm < W or (g_full is not None and warm == 0):
+            if g_full is not None:
+                replay(g_full, warm)
+                warm += per_graph
+            if g_rem is not None:
+                replay(g_rem, warm)
+                warm += rem
     torch.cuda.synchronize()
 
     sampler = ClockSampler(local_rank)
@@ -339,12 +452,13 @@ def measure_workload(name, args, K, W, rank, local_rank, world, device, log, cpu
     torch.cuda.synchronize()
     t_wall0 = time.time()
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    start.record()
-    for _ in range(n_full):
-        g_full.replay()
-    if g_rem is not None:
-        g_rem.replay()
-    end.record()
+    with torch.cuda.stream(stream):
+        start.record(stream)
+        for i in range(n_full):
+            replay(g_full, warm + i)
+        if g_rem is not None:
+            replay(g_rem, warm + n_full)
+        end.record(stream)
     torch.cuda.synchronize()
     if world > 1:
         torch.distributed.barrier()
@@ -382,7 +496,11 @@ def measure_workload(name, args, K, W, rank, local_rank, world, device, log, cpu
         ids = L.active[:a].cpu().numpy()
         n_act.append(a)
         ffn_bytes.append((a + 1) * wl.expert_payload + T * H * 2 + (T * k + T) * H * 4)
-        n_host_act = int(sset["host_mask"][ids].sum()) if sset["n_host"] else 0
+        if "cache" in sset:     # live cache: host-resident = neither static nor in a slot now
+            es = sset["cache"]["expert_slot"].cpu().numpy()
+            n_host_act = int((es[ids[ids < cfg.n_experts]] == -1).sum())
+        else:
+            n_host_act = int(sset["host_mask"][ids].sum()) if sset["n_host"] else 0
         host_bytes.append(n_host_act * wl.expert_payload)
     del g_ffn
 
@@ -414,6 +532,9 @@ def measure_workload(name, args, K, W, rank, local_rank, world, device, log, cpu
             roofline["hbm_gbs"] = round((float(np.mean(ffn_bytes)) - hb) / (ffn_ms_call / 1e3) / 1e9, 1)
             roofline["host_link_gbs"] = round(hb / (ffn_ms_call / 1e3) / 1e9, 1)
             roofline["frac_hbm"] = round(roofline["hbm_gbs"] / peak, 4)
+            lp = link_peaks(device)
+            roofline["host_link_peak"] = lp
+            roofline["frac_host_link"] = round(roofline["host_link_gbs"] / lp["host_link_read_gbs"], 4)
         per_layer = float(np.mean(ffn_bytes)) + cfg.n_experts * H * 4
         roofline["step_hbm_gbs"] = round(per_layer * wl.layers_per_step / (ms / K / 1e3) / 1e9, 1)
         roofline["step_frac"] = round(roofline["step_hbm_gbs"] / peak, 4)
@@ -439,10 +560,17 @@ def measure_workload(name, args, K, W, rank, local_rank, world, device, log, cpu
         "ms_per_step": round(ms / K, 6), "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": DTYPE_PREFILL if prefill else (DTYPE_DECODE if fp8 else DTYPE_DECODE_FP16),
         "data": "synthetic (seeded generators; random-init weights quantized to the library's 4-bit group format)",
-        "config": {**workload_config(name, wl.n_sets, world), **side_note(args)},
+        "config": {**workload_config(name, wl.n_sets, world), **side_note(args),
+                   **({"host_unit_cost": host_cost} if host_cost > 1 else {})},
         "gpu_launches": None, "roofline": roofline, "clocks": clocks, "e2e": None,
     }
     launches_per_layer = 2 + (1 if T * k <= 1024 else 3) + (3 if prefill else 2) + 1
+    if cfg.live_cache:
+        launches_per_layer += 2
+        rec["cache"] = cache_misses(wl, xs, T, first=warm + K + 1)
+        rec["config"]["inputs"] = "a fresh token batch every step (one 512 KB device copy into the graph's input per step)"
+        rec["cache"]["copy_gbs_per_step_time"] = round(
+            rec["cache"]["copy_bytes_per_layer_step"] * wl.layers_per_step / (ms / K / 1e3) / 1e9, 1)
     rec["gpu_launches"] = launches_per_layer * wl.layers_per_step * K
     if not args.no_e2e:
         rec["e2e"] = run_e2e(wl, xs, stream, device, tokens_per_step, world, max(3, min(K, args.e2e_steps)))
@@ -452,6 +580,42 @@ def measure_workload(name, args, K, W, rank, local_rank, world, device, log, cpu
     del g_full, g_rem
     wl.sets.clear()
     return rec
+
+
+def layer_step(s, x, T, stream, side=None):
+    """One layer of a step: route -> dispatch -> [expert cache update + miss
+    copy, for a live cache] -> expert FFN -> combine, on the current stream."""
+    import quantized_routed_expert_03_gb300 as qre
+    L = s["layer"]
+    if side is not None:   # the shared expert on a second stream (fork/join inside the graph)
+        L.forward(x, s["wr"], s["bias"], T, stream=stream, shared_stream=side)
+        return
+    L.route(x, s["wr"], s["bias"], T)
+    L.dispatch(T)
+    c = s.get("cache")
+    if c is not None:
+        qre.qre_cache_update(L.shape, c["S"], 0.995, L.active, L.n_active, c["scores"], c["expert_slot"],
+                             c["slot_expert"], c["home"], c["slot_mem"], L.slots, c["copy_list"], c["n_copies"],
+                             c["max_copies"])
+        qre.qre_cache_copy(L.shape, c["home"], c["slot_mem"], c["copy_list"], c["n_copies"], c["max_copies"])
+    L.expert_ffn(x, T)
+    L.combine(T)
+
+
+def cache_misses(wl, xs, T, first, steps=8) -> dict:
+    """Admissions (miss copies) per layer-step of a live cache over `steps` more
+    steps on activation batches first, first + 1, ... (not used by the timed
+    steps), counted on the host after each layer (outside any timed region)."""
+    import torch
+    n_adm = 0
+    for j in range(first, first + steps):
+        for r, s in enumerate(wl.sets):
+            layer_step(s, xs[r][j % xs[r].shape[0]], T, None)
+            torch.cuda.synchronize()
+            n_adm += int(s["cache"]["n_copies"][0].item())
+    per = n_adm / (steps * len(wl.sets))
+    return {"misses_per_layer_step": round(per, 3), "copy_bytes_per_layer_step": int(per * wl.expert_payload),
+            "counted_over": f"{steps} steps x {len(wl.sets)} layers after the timed region"}
 
 
 def run_ours(args, rank, local_rank, world):
@@ -491,9 +655,7 @@ def run_e2e(wl, xs, stream, device, tokens_per_step, world, K):
 
     # one graph per layer set (single-layer workloads) or one for the whole stack
     def body(idx):
-        s = sets[idx]
-        L = s["layer"]
-        L.forward(xin_dev[idx], s["wr"], s["bias"], T)
+        layer_step(sets[idx], xin_dev[idx], T, stream)
     with torch.cuda.stream(stream):
         for i in range(len(sets)):
             body(i)
@@ -545,7 +707,8 @@ def run_e2e(wl, xs, stream, device, tokens_per_step, world, K):
     ms = max_over_ranks(s0.elapsed_time(s1), world)
     return {"value": round(job_throughput(world, tokens_per_step, K, ms), 2), "unit": UNIT, "steps": K,
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-            "api": "MoELayer.forward captured in a CUDA graph; per step: pinned H2D input copy, replay, "
+            "api": "the layer's C-ABI calls (route, dispatch, [cache update + miss copy], expert FFN, combine) "
+                   "through the binding, captured in a CUDA graph; per step: pinned H2D input copy, replay, "
                    "pinned D2H of the bf16 output, stream synchronize"}
 
 
@@ -684,6 +847,8 @@ def main():
                     help="distinct layer weight sets to rotate over (default: enough to exceed L2)")
     ap.add_argument("--side-stream", action="store_true",
                     help="run the shared expert on a second stream beside the router and dispatch")
+    ap.add_argument("--host-unit-cost", type=int, default=None,
+                    help="decode work cut: cost of a host-mapped unit (default 4 with host-resident experts, else 0)")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-clocks", action="store_true")

@@ -365,12 +365,36 @@ QRE_API qre_status qre_stage_experts(const qre_layer_shape* shape, const qre_slo
                                      qre_slot* table_out, int32_t* n_staged, qre_stream_t stream);
 
 /*
+ * Bandwidth probe: one streaming read of `bytes` bytes at src (device memory,
+ * or pinned host memory mapped into the device address space, read zero-copy
+ * the way host-resident experts are read), 16-byte loads with several in flight
+ * per thread over 4 CTAs per SM.  Time it with events on `stream` to get the
+ * copy-free read rate of device memory or of the host link.  src 16-byte
+ * aligned, bytes a positive multiple of 16; sink: one device uint32 the kernel
+ * may write (it keeps the loads from being removed).
+ */
+QRE_API qre_status qre_read_probe(const void* src, size_t bytes, uint32_t* sink, qre_stream_t stream);
+
+/*
  * Checks a HOST copy of a slot table before it is uploaded: every pointer
  * non-null and 16-byte aligned, reserved == 0, tier in {0, 1}, tier-0
  * pointers in device memory and tier-1 pointers in host memory that the
  * device can read.  host_slots: host array of n_experts + 1 entries.
  */
 QRE_API qre_status qre_validate_slots(const qre_layer_shape* shape, const qre_slot* host_slots);
+
+/*
+ * Decode expert FFN with host-mapped experts in the slot table (the
+ * expert-cache layout): every call after this one, process-wide, cuts the
+ * decode kernels' work ranges at equal cost with a 128-row unit of a
+ * host-mapped expert counted as `cost` units of device memory (it streams over
+ * the host link at a fraction of the rate), so host-resident experts spread
+ * over more SMs.  0 or 1 (the default) cuts at equal unit counts, the right
+ * choice when every expert is in device memory.  cost in [0, 64].  Results are
+ * the same bits either way.  A CUDA graph keeps the value in force when it was
+ * captured.
+ */
+QRE_API qre_status qre_set_host_unit_cost(int32_t cost);
 
 /*
  * Test hook for the bounded waits' give-up path (failure handling without a

@@ -42,6 +42,7 @@ EXPORTS = (
     "qre_cache_update", "qre_cache_copy",
     "qre_read_device_status", "qre_clear_device_status", "qre_route_noalloc", "qre_debug_wait_test",
     "qre_expert_ffn_routed", "qre_expert_ffn_shared", "qre_shared_workspace_size", "qre_stage_experts",
+    "qre_read_probe", "qre_set_host_unit_cost",
 )
 
 
@@ -92,6 +93,8 @@ _SIGS = {
     "qre_shared_workspace_size": ([_SHAPE, _I32, ctypes.POINTER(ctypes.c_size_t)], ctypes.c_int),
     "qre_stage_experts": ([_SHAPE, ctypes.POINTER(qre_slot), ctypes.POINTER(qre_slot), _I32, _VP, _VP,
                            ctypes.POINTER(ctypes.c_int32), _VP], ctypes.c_int),
+    "qre_read_probe": ([_VP, _SZ, _VP, _VP], ctypes.c_int),
+    "qre_set_host_unit_cost": ([_I32], ctypes.c_int),
 }
 
 
@@ -257,6 +260,11 @@ def qre_stage_experts(shape, host_table, host_staging, host_out, table_out, stre
     return n.value
 
 
+def qre_read_probe(src, nbytes, sink, stream=None) -> None:
+    """One streaming read of ``nbytes`` at ``src`` (device or host-mapped); time it with events."""
+    _check(load_library().qre_read_probe(_ptr(src), nbytes, _ptr(sink), _stream(stream)), "qre_read_probe")
+
+
 def qre_validate_slots(shape, host_slots) -> None:
     """host_slots: a ctypes array of qre_slot (n_experts + 1 entries) in host memory."""
     _check(load_library().qre_validate_slots(ctypes.byref(shape), host_slots), "qre_validate_slots")
@@ -266,6 +274,12 @@ def qre_debug_wait_test(wait_limit_ns: int, stall_ns: int) -> None:
     """Test hook: lower the kernels' wait limit and delay one warp of the expert
     FFN's first CTA, so that the give-up path runs (0, 0 restores the defaults)."""
     _check(load_library().qre_debug_wait_test(wait_limit_ns, stall_ns), "qre_debug_wait_test")
+
+
+def qre_set_host_unit_cost(cost: int) -> None:
+    """Process-wide: cut the decode kernels' work at equal cost with a host-mapped
+    unit counted as ``cost`` (0 or 1: equal counts, the default)."""
+    _check(load_library().qre_set_host_unit_cost(cost), "qre_set_host_unit_cost")
 
 
 def qre_read_device_status(stream=None) -> int:

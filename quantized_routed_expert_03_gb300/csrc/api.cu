@@ -42,7 +42,10 @@ namespace qre {
 namespace {
 std::atomic<uint64_t> g_wait_limit_ns{kWaitLimitNs};
 std::atomic<uint64_t> g_test_stall_ns{0};
+std::atomic<int> g_host_unit_cost{0};
 }  // namespace
+
+int host_unit_cost() { return g_host_unit_cost.load(std::memory_order_relaxed); }
 
 uint64_t wait_limit_ns() { return g_wait_limit_ns.load(std::memory_order_relaxed); }
 uint64_t test_stall_ns() { return g_test_stall_ns.load(std::memory_order_relaxed); }
@@ -439,6 +442,14 @@ qre_status qre_stage_experts(const qre_layer_shape* shape, const qre_slot* host_
   return QRE_OK;
 }
 
+qre_status qre_read_probe(const void* src, size_t bytes, uint32_t* sink, qre_stream_t stream) {
+  QRE_REQUIRE_PTR(src);
+  QRE_REQUIRE_PTR(sink);
+  if (bytes == 0 || bytes % 16) return fail(QRE_ERR_INVALID_ARG, "bytes %zu must be a positive multiple of 16", bytes);
+  return launched(qre::launch_read_probe(src, bytes, sink, reinterpret_cast<cudaStream_t>(stream)),
+                  "qre_read_probe launch");
+}
+
 qre_status qre_validate_slots(const qre_layer_shape* shape, const qre_slot* host_slots) {
   qre_status st = check_shape(shape, 0);
   if (st != QRE_OK) return st;
@@ -485,6 +496,13 @@ qre_status qre_debug_wait_test(uint64_t wait_limit_ns, uint64_t stall_ns) {
                 (unsigned long long)kMaxTestStallNs);
   qre::g_wait_limit_ns.store(wait_limit_ns ? wait_limit_ns : qre::kWaitLimitNs, std::memory_order_relaxed);
   qre::g_test_stall_ns.store(stall_ns, std::memory_order_relaxed);
+  g_err[0] = '\0';
+  return QRE_OK;
+}
+
+qre_status qre_set_host_unit_cost(int32_t cost) {
+  if (cost < 0 || cost > 64) return fail(QRE_ERR_INVALID_ARG, "host unit cost %d not in [0, 64]", cost);
+  qre::g_host_unit_cost.store(cost, std::memory_order_relaxed);
   g_err[0] = '\0';
   return QRE_OK;
 }

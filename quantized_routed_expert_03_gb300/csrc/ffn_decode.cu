@@ -84,6 +84,7 @@ struct FfnParams {
   int nB;           // B buffers in shared memory (down kernel: experts resident at once)
   int amax;         // largest possible number of active experts, min(E, T*k)
   int part;         // groups of this launch: 0 routed + shared, 1 routed only, 2 shared only
+  int host_cost;    // > 1: the cost-cut instance, a host-mapped unit counted as this many (qre_set_host_unit_cost)
   const uint16_t* x;
   const qre_slot* slots;
   const int32_t* offsets;
@@ -748,7 +749,46 @@ __device__ __noinline__ void e4m3_b_job(int job, const uint4 raw, int T, int KG,
   }
 }
 
-template <int MODE, int TT>
+// A unit of a host-mapped expert streams over the host link at a fraction of
+// the rate of device memory.  With qre_set_host_unit_cost the FP8 kernels run
+// an instance that cuts its contiguous unit ranges at equal cost, such a unit
+// counted as `cost` device-memory units, so the host-resident experts of a
+// call spread over more CTAs.  (A separate instance: in the default one the
+// extra code measurably slowed the all-HBM decode.)
+
+// This CTA's unit range [ub, ue) (x, y): contiguous ranges over the grid cut at
+// equal cost, `cost` for units of host-mapped groups and 1 otherwise,
+// when a host-mapped group is present and (down kernel, max_span_groups > 0)
+// no range can then span more than two groups; else at equal unit counts.
+// Out of line: it runs once per CTA and keeps its registers off the kernel.
+__device__ __noinline__ int2 unit_range(const Group* groups, int ngroups, int upe, bool limit_span, int nB,
+                                        int cost) {
+  const long long U = (long long)ngroups * upe, grid = gridDim.x, c = blockIdx.x;
+  long long C = 0;
+  bool host = false;
+  for (int a = 0; a < ngroups; ++a) {
+    const bool h = (groups[a].flags & 2) != 0;
+    host |= h;
+    C += (long long)upe * (h ? cost : 1);
+  }
+  if (!host || (limit_span && (nB < 2 || C > grid * upe))) return make_int2((int)(c * U / grid), (int)((c + 1) * U / grid));
+  // the first unit whose cost before it, times the grid, reaches `target`
+  auto first_unit = [&](long long target) -> int {
+    long long base = 0;
+    for (int a = 0; a < ngroups; ++a) {
+      const long long w = (groups[a].flags & 2) ? cost : 1;
+      if ((base + (upe - 1) * w) * grid >= target) {
+        const long long num = target - base * grid;
+        return a * upe + (num <= 0 ? 0 : (int)((num + w * grid - 1) / (w * grid)));
+      }
+      base += upe * w;
+    }
+    return (int)U;
+  };
+  return make_int2(first_unit(c * C), first_unit((c + 1) * C));
+}
+
+template <int MODE, int TT, bool HC = false>
 __global__ void __launch_bounds__(kThreads, 1) ffn_e4m3_kernel(const FfnParams p) {
   constexpr int kStages = ring8_stages(MODE, TT);   // shared-memory ring depth (0: register ring)
   constexpr int R = kStages ? kStages : 2;          // ring depth = unroll
@@ -821,15 +861,15 @@ __global__ void __launch_bounds__(kThreads, 1) ffn_e4m3_kernel(const FfnParams p
   const int ngroups = n_act + (p.part == 1 ? 0 : 1);
   const int upe = p.n_out / BM;
   const int U = ngroups * upe;
-  const int ub = (int)((long long)blockIdx.x * U / gridDim.x);
-  const int ue = (int)((long long)(blockIdx.x + 1) * U / gridDim.x);
+  int ub = (int)((long long)blockIdx.x * U / gridDim.x);
+  int ue = (int)((long long)(blockIdx.x + 1) * U / gridDim.x);
   if (ub >= ue) return;
 
   const int wg = tid >> 7, r = tid & 127, wq = warp & 3;
   const uint32_t b_bytes = (uint32_t)BN8 * p.K;
-  const int a_first = ub / upe, a_last = (ue - 1) / upe;
-  const int nbuf = MODE == 0 ? 1 : (a_last - a_first + 1 < p.nB ? a_last - a_first + 1 : p.nB);
-  const int njobs = nbuf * p.T * KG;
+  int a_first = ub / upe, a_last = (ue - 1) / upe;
+  int nbuf = MODE == 0 ? 1 : (a_last - a_first + 1 < p.nB ? a_last - a_first + 1 : p.nB);
+  int njobs = nbuf * p.T * KG;
   auto b_fill = [&](int a0) {
     for (int b0 = 0; wk >= 0 && wk + kNW * b0 < njobs; b0 += kJB) {
       if (b0 > 0) {
@@ -896,6 +936,31 @@ __global__ void __launch_bounds__(kThreads, 1) ffn_e4m3_kernel(const FfnParams p
   // table in place every warpgroup puts its first ring stages in flight (down:
   // while the gate/up grid finishes, before h is read).
   __syncthreads();
+  if constexpr (HC) {
+    // Host-mapped groups in the table: re-cut the ranges at equal cost
+    // (unit_range; every CTA had units when U >= grid, so none returned early
+    // above); a CTA left without units gives its tensor memory back.
+    if (U >= (int)gridDim.x) {
+      const int2 rc = unit_range(groups, ngroups, upe, MODE == 1, p.nB, p.host_cost);
+      if (rc.x != ub || rc.y != ue) {
+        ub = rc.x;
+        ue = rc.y;
+        if (ub >= ue) {
+          if (warp == 0) {
+            tc_fence_after();
+            tmem_dealloc(*tmem_base_p, kWG * kColsPerWG);
+          }
+          return;
+        }
+        a_first = ub / upe;
+        a_last = (ue - 1) / upe;
+        if (MODE == 1) {
+          nbuf = a_last - a_first + 1 < p.nB ? a_last - a_first + 1 : p.nB;
+          njobs = nbuf * p.T * KG;
+        }
+      }
+    }
+  }
   const int NU = ue - ub;
   const int Kq = p.K / p.kq;
   const int nst = Kq / SK8;
@@ -1232,9 +1297,10 @@ int smem_needed8(int MODE, int K, int nB, int TT) {
 
 template <int MODE, int TT>
 cudaError_t launch_e4m3(const FfnParams& p, int grid, int smem, cudaStream_t stream) {
-  const cudaError_t err = ensure_smem_limit(reinterpret_cast<const void*>(ffn_e4m3_kernel<MODE, TT>), smem);
+  auto kernel = p.host_cost > 1 ? ffn_e4m3_kernel<MODE, TT, true> : ffn_e4m3_kernel<MODE, TT, false>;
+  const cudaError_t err = ensure_smem_limit(reinterpret_cast<const void*>(kernel), smem);
   if (err != cudaSuccess) return err;
-  return launch_dependent(ffn_e4m3_kernel<MODE, TT>, dim3(grid), dim3(kThreads), smem, stream, p);
+  return launch_dependent(kernel, dim3(grid), dim3(kThreads), smem, stream, p);
 }
 
 // One CTA per SM.  The down kernels hold the B operand (h) of every expert of
@@ -1325,6 +1391,7 @@ cudaError_t launch_ffn_decode(const qre_layer_shape& s, int T, const uint16_t* x
   p.expert_out = expert_out;
   p.status = status;
   p.part = part;
+  p.host_cost = host_unit_cost();
   p.wait_ns = wait_limit_ns();
   p.stall_ns = test_stall_ns();
   const long long pk = (long long)T * s.top_k;

@@ -30,6 +30,8 @@ enum FfnPart { kFfnAll = 0, kFfnRouted = 1, kFfnShared = 2 };
 // it with qre_debug_wait_test), and the test hook's stall (0 = off).
 uint64_t wait_limit_ns();
 uint64_t test_stall_ns();
+// Cost of a host-mapped unit in the decode kernels' range cut (<= 1: off).
+int host_unit_cost();
 
 // Sets the calling thread's qre_last_error() message (printf format).
 void set_error_message(const char* fmt, ...);
@@ -102,6 +104,9 @@ cudaError_t launch_cache_update(int E, int S, float decay, const int32_t* active
 cudaError_t launch_cache_copy(const qre_layer_shape& s, const qre_slot* home, const qre_slot* slot_mem,
                               const int32_t* copy_list, const int32_t* n_copies, int max_copies,
                               cudaStream_t stream);
+
+// A streaming read of `bytes` bytes (device or host-mapped memory).
+cudaError_t launch_read_probe(const void* src, size_t bytes, uint32_t* sink, cudaStream_t stream);
 
 cudaError_t launch_combine(const qre_layer_shape& s, int T, const float* expert_out, const float* topk_w,
                            const int32_t* inv_perm, float* y_f32, uint16_t* y_bf16, cudaStream_t stream);

@@ -53,6 +53,7 @@ class LayerConfig:
     host_tier: bool = False          # popularity ranks > hbm_slots live in host memory
     hbm_slots: int = 188
     static_slots: int = 40
+    live_cache: bool = False         # the HBM slots past the static ones are a live LFU cache
     seed: int = 0
     note: str = field(default="", compare=False)
 
@@ -67,6 +68,11 @@ CONFIGS = {
     "cache4_x42": LayerConfig("cache4_x42", 4096, 2048, 288, 8, 128, 4, layers=42, zipf=True, host_tier=True,
                               note="T4, Zipf(1.1), 42 layers; 188 HBM slots (40 static + 148 cache), "
                                    "100 experts per layer in pinned host memory read zero-copy"),
+    "cache4_live_x16": LayerConfig("cache4_live_x16", 4096, 2048, 288, 8, 128, 4, layers=16, zipf=True,
+                                   host_tier=True, live_cache=True,
+                                   note="T4, Zipf(1.1), 16 layers; 40 static HBM experts + 148 HBM slots run as an "
+                                        "LFU(0.995) cache (starting with ranks 41-188), misses copied from pinned "
+                                        "host memory every step; the other experts read zero-copy until admitted"),
     "prefill8192": LayerConfig("prefill8192", 4096, 2048, 288, 8, 128, 8192,
                                note="T8192 prefill chunk, uniform routing, + shared expert"),
 }

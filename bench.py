@@ -564,7 +564,7 @@ def measure_workload(name, args, K, W, rank, local_rank, world, device, log, cpu
                    **({"host_unit_cost": host_cost} if host_cost > 1 else {})},
         "gpu_launches": None, "roofline": roofline, "clocks": clocks, "e2e": None,
     }
-    launches_per_layer = 2 + (1 if T * k <= 1024 else 3) + (3 if prefill else 2) + 1
+    launches_per_layer = (2 if T <= 8 else 2 + (1 if T * k <= 1024 else 3)) + (3 if prefill else 2) + 1
     if cfg.live_cache:
         launches_per_layer += 2
         rec["cache"] = cache_misses(wl, xs, T, first=warm + K + 1)
@@ -590,8 +590,7 @@ def layer_step(s, x, T, stream, side=None):
     if side is not None:   # the shared expert on a second stream (fork/join inside the graph)
         L.forward(x, s["wr"], s["bias"], T, stream=stream, shared_stream=side)
         return
-    L.route(x, s["wr"], s["bias"], T)
-    L.dispatch(T)
+    L.route_dispatch(x, s["wr"], s["bias"], T)
     c = s.get("cache")
     if c is not None:
         qre.qre_cache_update(L.shape, c["S"], 0.995, L.active, L.n_active, c["scores"], c["expert_slot"],

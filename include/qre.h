@@ -230,6 +230,19 @@ QRE_API qre_status qre_dispatch(const qre_layer_shape* shape, int32_t T, const i
                         size_t workspace_bytes, qre_stream_t stream);
 
 /*
+ * qre_route followed by qre_dispatch in one call, with the same outputs (bit
+ * for bit) and arguments.  For one token the top-k selection and the dispatch
+ * share one single-CTA kernel, one dependent launch less on the way to the
+ * expert FFN; other T runs the two calls' kernels.  The workspace must hold
+ * qre_workspace_size bytes.
+ */
+QRE_API qre_status qre_route_dispatch(const qre_layer_shape* shape, int32_t T, const uint16_t* x_bf16,
+                                      const float* w_router, const float* bias, int32_t* topk_idx, float* topk_w,
+                                      int32_t* counts, int32_t* offsets, int32_t* perm, int32_t* inv_perm,
+                                      int32_t* active, int32_t* n_active, void* workspace, size_t workspace_bytes,
+                                      qre_stream_t stream);
+
+/*
  * Expert FFN: for every active expert e and each of its picks, and for the
  * shared expert (slot n_experts) over all T tokens,
  *   o = W_down (silu(W_gate x) * (W_up x)),

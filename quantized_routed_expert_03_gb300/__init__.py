@@ -42,7 +42,7 @@ EXPORTS = (
     "qre_cache_update", "qre_cache_copy",
     "qre_read_device_status", "qre_clear_device_status", "qre_route_noalloc", "qre_debug_wait_test",
     "qre_expert_ffn_routed", "qre_expert_ffn_shared", "qre_shared_workspace_size", "qre_stage_experts",
-    "qre_read_probe", "qre_set_host_unit_cost",
+    "qre_read_probe", "qre_set_host_unit_cost", "qre_route_dispatch",
 )
 
 
@@ -95,6 +95,8 @@ _SIGS = {
                            ctypes.POINTER(ctypes.c_int32), _VP], ctypes.c_int),
     "qre_read_probe": ([_VP, _SZ, _VP, _VP], ctypes.c_int),
     "qre_set_host_unit_cost": ([_I32], ctypes.c_int),
+    "qre_route_dispatch": ([_SHAPE, _I32, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _SZ, _VP],
+                           ctypes.c_int),
 }
 
 
@@ -189,6 +191,15 @@ def qre_route_noalloc(shape, T, x_bf16, w_router, bias, topk_idx, topk_w, stream
     is a fixed array inside the library (T * n_experts <= 65,536)."""
     _check(load_library().qre_route_noalloc(ctypes.byref(shape), T, _ptr(x_bf16), _ptr(w_router), _ptr(bias),
                                             _ptr(topk_idx), _ptr(topk_w), _stream(stream)), "qre_route_noalloc")
+
+
+def qre_route_dispatch(shape, T, x_bf16, w_router, bias, topk_idx, topk_w, counts, offsets, perm, inv_perm, active,
+                       n_active, workspace, workspace_bytes=None, stream=None) -> None:
+    _check(load_library().qre_route_dispatch(ctypes.byref(shape), T, _ptr(x_bf16), _ptr(w_router), _ptr(bias),
+                                             _ptr(topk_idx), _ptr(topk_w), _ptr(counts), _ptr(offsets), _ptr(perm),
+                                             _ptr(inv_perm), _ptr(active), _ptr(n_active), _ptr(workspace),
+                                             _nbytes(workspace, workspace_bytes), _stream(stream)),
+           "qre_route_dispatch")
 
 
 def qre_dispatch(shape, T, topk_idx, counts, offsets, perm, inv_perm, active, n_active, workspace,

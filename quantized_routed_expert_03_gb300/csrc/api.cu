@@ -233,6 +233,38 @@ qre_status qre_route(const qre_layer_shape* shape, int32_t T, const uint16_t* x_
                   "qre_route launch");
 }
 
+qre_status qre_route_dispatch(const qre_layer_shape* shape, int32_t T, const uint16_t* x_bf16, const float* w_router,
+                              const float* bias, int32_t* topk_idx, float* topk_w, int32_t* counts, int32_t* offsets,
+                              int32_t* perm, int32_t* inv_perm, int32_t* active, int32_t* n_active, void* workspace,
+                              size_t workspace_bytes, qre_stream_t stream) {
+  qre_status st = check_shape(shape, T);
+  if (st != QRE_OK) return st;
+  if (T == 0) return QRE_OK;
+  if (!qre::route_dispatch_fused(*shape, T)) {
+    st = qre_route(shape, T, x_bf16, w_router, bias, topk_idx, topk_w, workspace, workspace_bytes, stream);
+    if (st != QRE_OK) return st;
+    return qre_dispatch(shape, T, topk_idx, counts, offsets, perm, inv_perm, active, n_active, workspace,
+                        workspace_bytes, stream);
+  }
+  QRE_REQUIRE_PTR(x_bf16);
+  QRE_REQUIRE_PTR(w_router);
+  QRE_OPTIONAL_PTR(bias);
+  QRE_REQUIRE_PTR(topk_idx);
+  QRE_REQUIRE_PTR(topk_w);
+  QRE_REQUIRE_PTR(counts);
+  QRE_REQUIRE_PTR(offsets);
+  QRE_REQUIRE_PTR(perm);
+  QRE_REQUIRE_PTR(inv_perm);
+  QRE_REQUIRE_PTR(active);
+  QRE_REQUIRE_PTR(n_active);
+  st = check_workspace(workspace, workspace_bytes, qre::route_ws_bytes(*shape, T));
+  if (st != QRE_OK) return st;
+  return launched(qre::launch_route_dispatch(*shape, T, x_bf16, w_router, bias, topk_idx, topk_w, counts, offsets,
+                                             perm, inv_perm, active, n_active, workspace,
+                                             reinterpret_cast<cudaStream_t>(stream)),
+                  "qre_route_dispatch launch");
+}
+
 qre_status qre_dispatch(const qre_layer_shape* shape, int32_t T, const int32_t* topk_idx, int32_t* counts,
                         int32_t* offsets, int32_t* perm, int32_t* inv_perm, int32_t* active, int32_t* n_active,
                         void* workspace, size_t workspace_bytes, qre_stream_t stream) {

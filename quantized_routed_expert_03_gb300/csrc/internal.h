@@ -78,6 +78,15 @@ cudaError_t launch_route(const qre_layer_shape& s, int T, const uint16_t* x, con
                          const float* bias, int32_t* topk_idx, float* topk_w, void* ws,
                          cudaStream_t stream);
 
+// Router + dispatch in two launches (GEMV, then selection and dispatch in one
+// CTA) when route_dispatch_fused(s, T) (one token); the outputs of launch_route
+// followed by launch_dispatch.
+bool route_dispatch_fused(const qre_layer_shape& s, int T);
+cudaError_t launch_route_dispatch(const qre_layer_shape& s, int T, const uint16_t* x, const float* w_router,
+                                  const float* bias, int32_t* topk_idx, float* topk_w, int32_t* counts,
+                                  int32_t* offsets, int32_t* perm, int32_t* inv_perm, int32_t* active,
+                                  int32_t* n_active, void* ws, cudaStream_t stream);
+
 cudaError_t launch_dispatch(const qre_layer_shape& s, int T, const int32_t* topk_idx, int32_t* counts,
                             int32_t* offsets, int32_t* perm, int32_t* inv_perm, int32_t* active,
                             int32_t* n_active, void* ws, int* status, cudaStream_t stream);

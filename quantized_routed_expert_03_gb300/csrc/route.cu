@@ -209,9 +209,92 @@ __global__ void __launch_bounds__(1024) route_select_rank(int T, int E, int k, c
   }
 }
 
+// One token: selection and dispatch in one CTA, one dependent launch less
+// between the router and the expert FFN.  It ranks the token's experts exactly
+// as route_select_rank does and dispatches the k picks with dispatch_block: the
+// same bits as route_select_rank followed by dispatch_single.  (For several
+// tokens, a version whose last CTA dispatched all picks measured slower than
+// the two kernels.)
+__global__ void __launch_bounds__(1024) route_select_dispatch1(int E, int k, const float* __restrict__ logits,
+                                                               const float* __restrict__ bias, int32_t* idx,
+                                                               float* __restrict__ wout, int32_t* counts,
+                                                               int32_t* offsets, int32_t* perm, int32_t* inv_perm,
+                                                               int32_t* active, int32_t* n_active) {
+  __shared__ float sel_s[1024];
+  __shared__ int wcount[32];
+  __shared__ int chosen[16];
+  __shared__ float chosen_s[16];
+  __shared__ int s_cnt[1024];
+  __shared__ int total;
+  grid_dependency_wait();
+  grid_dependents_launch();
+  const int e = threadIdx.x, lane = e & 31, warp = e >> 5;
+  float sc = 0.f, my = -INFINITY;
+  if (e < E) {
+    sc = 1.0f / (1.0f + expf(-logits[e]));
+    my = bias ? sc + bias[e] : sc;
+    sel_s[e] = my;
+  }
+  __syncthreads();
+  int rank = 0;
+  if (e < E) {
+    for (int j = 0; j < E; ++j) {
+      const float v = sel_s[j];
+      rank += (v > my || (v == my && j < e)) ? 1 : 0;
+    }
+  }
+  const bool pick = e < E && rank < k;
+  const unsigned bal = __ballot_sync(0xffffffffu, pick);
+  if (lane == 0) wcount[warp] = __popc(bal);
+  __syncthreads();
+  if (pick) {
+    int pos = __popc(bal & ((1u << lane) - 1u));
+    for (int w = 0; w < warp; ++w) pos += wcount[w];
+    if (pos < 16) {
+      chosen[pos] = e;
+      chosen_s[pos] = sc;
+    }
+  }
+  __syncthreads();
+  if (e == 0) {
+    float tot = 0.f;
+    for (int j = 0; j < k; ++j) tot += chosen_s[j];
+    for (int j = 0; j < k; ++j) {
+      idx[j] = chosen[j];
+      wout[j] = chosen_s[j] / tot;
+    }
+  }
+  __syncthreads();
+  dispatch_block(k, E, chosen, counts, offsets, perm, inv_perm, active, n_active, s_cnt, wcount, &total);
+}
+
 }  // namespace
 
 size_t route_ws_bytes(const qre_layer_shape& s, int T) { return (size_t)T * s.n_experts * sizeof(float); }
+
+bool route_dispatch_fused(const qre_layer_shape&, int T) { return T == 1; }
+
+cudaError_t launch_route_dispatch(const qre_layer_shape& s, int T, const uint16_t* x, const float* w_router,
+                                  const float* bias, int32_t* topk_idx, float* topk_w, int32_t* counts,
+                                  int32_t* offsets, int32_t* perm, int32_t* inv_perm, int32_t* active,
+                                  int32_t* n_active, void* ws, cudaStream_t stream) {
+  float* logits = static_cast<float*>(ws);
+  const int H = s.hidden, E = s.n_experts;
+  const size_t xs_bytes = (size_t)T * H * 2;
+  const int stage = xs_bytes <= 64 * 1024 ? 1 : 0;
+  const size_t dyn = stage ? xs_bytes : 0;
+  auto kernel = route_logits_gemv<8>;
+  cudaError_t err;
+  if (stage) {
+    err = ensure_smem_limit(reinterpret_cast<const void*>(kernel), (int)dyn);
+    if (err != cudaSuccess) return err;
+  }
+  err = launch_dependent(kernel, dim3((E + 1) / 2), dim3(256), dyn, stream, T, H, E, x, w_router, logits, stage);
+  if (err != cudaSuccess) return err;
+  return launch_dependent(route_select_dispatch1, dim3(1), dim3(((E + 31) / 32) * 32), 0, stream, E, s.top_k,
+                          (const float*)logits, bias, topk_idx, topk_w, counts, offsets, perm, inv_perm, active,
+                          n_active);
+}
 
 cudaError_t launch_route(const qre_layer_shape& s, int T, const uint16_t* x, const float* w_router,
                          const float* bias, int32_t* topk_idx, float* topk_w, void* ws, cudaStream_t stream) {

@@ -21,7 +21,7 @@ import ctypes
 import torch
 
 from . import (make_shape, qre_combine, qre_dispatch, qre_expert_ffn, qre_expert_ffn_routed, qre_expert_ffn_shared,
-               qre_quantize, qre_quantize_gate_up, qre_route, qre_shared_workspace_size, qre_slot,
+               qre_quantize, qre_quantize_gate_up, qre_route, qre_route_dispatch, qre_shared_workspace_size, qre_slot,
                qre_stage_experts, qre_validate_slots, qre_workspace_size, slot_array)
 
 _ALIGN = 256
@@ -154,6 +154,11 @@ class MoELayer:
     def route(self, x, w_router, bias, T, stream=None):
         qre_route(self.shape, T, x, w_router, bias, self.topk_idx, self.topk_w, self.workspace, self.ws_bytes, stream)
 
+    def route_dispatch(self, x, w_router, bias, T, stream=None):
+        """route + dispatch in one library call (fewer launches for decode batches)."""
+        qre_route_dispatch(self.shape, T, x, w_router, bias, self.topk_idx, self.topk_w, self.counts, self.offsets,
+                           self.perm, self.inv_perm, self.active, self.n_active, self.workspace, self.ws_bytes, stream)
+
     def dispatch(self, T, stream=None):
         qre_dispatch(self.shape, T, self.topk_idx, self.counts, self.offsets, self.perm, self.inv_perm, self.active,
                      self.n_active, self.workspace, self.ws_bytes, stream)
@@ -187,8 +192,7 @@ class MoELayer:
         """
         T = x.shape[0] if T is None else T
         if shared_stream is None:
-            self.route(x, w_router, bias, T, stream)
-            self.dispatch(T, stream)
+            self.route_dispatch(x, w_router, bias, T, stream)
             self.expert_ffn(x, T, stream, slots)
             self.combine(T, stream)
             return self.y[:T]
@@ -200,8 +204,7 @@ class MoELayer:
         shared_stream.wait_event(self._fork)
         self.expert_ffn_shared(x, T, shared_stream)
         self._join.record(shared_stream)
-        self.route(x, w_router, bias, T, main)
-        self.dispatch(T, main)
+        self.route_dispatch(x, w_router, bias, T, main)
         self.expert_ffn_routed(x, T, main)
         main.wait_event(self._join)
         self.combine(T, main)

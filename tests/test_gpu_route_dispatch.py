@@ -119,3 +119,35 @@ def test_empty_call_is_a_no_op():
     qre.qre_dispatch(shape, 0, None, None, None, None, None, None, None, None, 0)
     qre.qre_expert_ffn(shape, 0, None, None, None, None, None, None, None, None, 0)
     qre.qre_combine(shape, 0, None, None, None, None, None)
+
+
+@pytest.mark.parametrize("H,E,k,T,bias", [(4096, 288, 8, 1, False), (4096, 288, 8, 8, True), (256, 16, 4, 4, False),
+                                          (512, 64, 6, 7, True), (768, 1024, 16, 8, False), (512, 64, 6, 40, False)])
+def test_route_dispatch_equals_route_then_dispatch(H, E, k, T, bias):
+    """qre_route_dispatch (selection and dispatch in one CTA for T <= 8, the two
+    calls' kernels above) writes the same bits as qre_route then qre_dispatch."""
+    shape = qre.make_shape(H, 128, E, k, 32)
+    x = bits_to_bf16_tensor(synthetic.activations_bits(T, H, seed=6, layer=1), DEV)
+    wr = torch.from_numpy(synthetic.router_weights(E, H, seed=6, layer=1)).to(DEV)
+    b = torch.from_numpy(synthetic.zipf_bias(E, seed=6, layer=1, beta=0.05)).to(DEV) if bias else None
+    ws = torch.empty(max(qre.qre_workspace_size(shape, T), 256), dtype=torch.uint8, device=DEV)
+    i32 = dict(dtype=torch.int32, device=DEV)
+
+    def outs():
+        return {"idx": torch.full((T, k), -1, **i32), "w": torch.full((T, k), -1.0, device=DEV),
+                "counts": torch.full((E,), -1, **i32), "offsets": torch.full((E + 1,), -1, **i32),
+                "perm": torch.full((T * k,), -1, **i32), "inv_perm": torch.full((T * k,), -1, **i32),
+                "active": torch.full((E,), -1, **i32), "n_active": torch.full((4,), -1, **i32)}
+    a, f = outs(), outs()
+    qre.qre_route(shape, T, x, wr, b, a["idx"], a["w"], ws)
+    qre.qre_dispatch(shape, T, a["idx"], a["counts"], a["offsets"], a["perm"], a["inv_perm"], a["active"],
+                     a["n_active"], ws)
+    qre.qre_route_dispatch(shape, T, x, wr, b, f["idx"], f["w"], f["counts"], f["offsets"], f["perm"], f["inv_perm"],
+                           f["active"], f["n_active"], ws)
+    torch.cuda.synchronize()
+    n = int(a["n_active"][0].item())
+    assert int(f["n_active"][0].item()) == n
+    for name in ("idx", "w", "counts", "offsets", "perm", "inv_perm"):
+        np.testing.assert_array_equal(f[name].cpu().numpy(), a[name].cpu().numpy(), err_msg=name)
+    np.testing.assert_array_equal(f["active"][:n].cpu().numpy(), a["active"][:n].cpu().numpy())
+    assert qre.qre_read_device_status() == 0

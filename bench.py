@@ -15,6 +15,7 @@ Workloads (``--workload``):
   cache4_x42        T = 4, Zipf(1.1), 42 layers, 100 experts/layer in pinned host memory
   cache4_live_x16   the same layout with the 148 HBM slots as a live LFU cache, 16 layers
   prefill8192       T = 8192 tokens through one layer (tcgen05 grouped GEMM)
+  prefill2048_e64   the same kernels on 64 experts and 2048 tokens (a small profiling case)
   tiny              H256 I128 E16 top-4 + shared, T = 4
 The line's top level is the ``--workload`` (decode1 by default); the workloads
 named by ``--also`` (prefill8192 by default) are measured in the same run, each
@@ -67,7 +68,7 @@ def dist_env():
 # DRAM bytes per expert-FFN call (both kernels) measured with ncu on a workload,
 # for the FFN kernel code with the given hash (ffn_source_hash).  Reported only
 # while the sources still hash to that value; a changed kernel reports null.
-MEASURED_TRAFFIC = {"decode1": (117405568, "7a5a27b151322a8e")}
+MEASURED_TRAFFIC = {"decode1": (117586944, "fc875e822f0ce5ef")}
 FFN_SOURCES = ("ffn_decode.cu", "common.cuh", "tc.cuh", "internal.h")
 
 

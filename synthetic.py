@@ -73,6 +73,9 @@ CONFIGS = {
                                    note="T4, Zipf(1.1), 16 layers; 40 static HBM experts + 148 HBM slots run as an "
                                         "LFU(0.995) cache (starting with ranks 41-188), misses copied from pinned "
                                         "host memory every step; the other experts read zero-copy until admitted"),
+    "prefill2048_e64": LayerConfig("prefill2048_e64", 4096, 2048, 64, 8, 128, 2048,
+                                   note="profiling case: the prefill8192 kernels on 64 experts and 2048 tokens "
+                                        "(~256 tokens per expert, 0.84 GB of packed experts)"),
     "prefill8192": LayerConfig("prefill8192", 4096, 2048, 288, 8, 128, 8192,
                                note="T8192 prefill chunk, uniform routing, + shared expert"),
 }

@@ -821,6 +821,12 @@ __global__ void __launch_bounds__(kThreads, 1) ffn_e4m3_kernel(const FfnParams p
   // group table and fill their weight ring (dispatch outputs and weights, all
   // complete by then), and wait for the gate/up grid only before reading h.
   if constexpr (MODE == 0) {
+    // While the dispatch still runs: bring the slot table into L2 (it is read
+    // right after the wait, one dependent load before the first weights; a
+    // line written meanwhile, e.g. by the cache manager, is current in L2).
+    const int lines = ((p.E + 1) * (int)sizeof(qre_slot) + 127) / 128;
+    if ((int)threadIdx.x < lines)
+      asm volatile("prefetch.global.L2 [%0];" ::"l"(reinterpret_cast<const char*>(p.slots) + 128 * threadIdx.x));
     grid_dependency_wait();
     grid_dependents_launch();
   }

@@ -1044,9 +1044,16 @@ __global__ void __launch_bounds__(kThreads, 1) ffn_e4m3_kernel(const FfnParams p
     }
   }
 
-  // down: the expert_out rows of each routed group's tokens (read by the
-  // epilogues only, so after the first weights are on their way)
+  // down: everything above (group table, first weight stages) overlaps the end
+  // of the gate/up grid; h is read only once that grid has completed
   if constexpr (MODE == 1) {
+    grid_dependency_wait();
+    grid_dependents_launch();
+#pragma unroll
+    for (int b = 0; b < kJB; ++b)
+      if (wk + kNW * b < njobs) pre[b] = job_load(wk + kNW * b, a_first);
+    // the expert_out rows of each routed group's tokens (read by the epilogues
+    // only): their perm loads travel together with the h loads above
     for (int a = tid; a < n_act; a += blockDim.x) {
       Group& dst = groups[a];
       if (!(dst.flags & 1)) continue;
@@ -1057,15 +1064,6 @@ __global__ void __launch_bounds__(kThreads, 1) ffn_e4m3_kernel(const FfnParams p
         if (tk >= 0 && tk < kTok) dst.outq[tk] = q;
       }
     }
-  }
-  // down: everything above (group table, first weight stages) overlaps the end
-  // of the gate/up grid; h is read only once that grid has completed
-  if constexpr (MODE == 1) {
-    grid_dependency_wait();
-    grid_dependents_launch();
-#pragma unroll
-    for (int b = 0; b < kJB; ++b)
-      if (wk + kNW * b < njobs) pre[b] = job_load(wk + kNW * b, a_first);
   }
   // B: gate/up one buffer of the tokens, down one buffer of h per expert of the
   // range (at most nB, by the launch).

@@ -159,113 +159,96 @@ __global__ void __launch_bounds__(kSelWarps * 32) route_select(int T, int E, int
     select_token_warp<32>(t, E, k, logits + (size_t)t * E, bias, idx, wout, sid[warp], ssc[warp], nullptr);
 }
 
-// One CTA per token (small T): every expert computes its rank in the order
-// (selection score descending, id ascending) against all others; the k experts
-// of rank < k are compacted in ascending id with a block-wide prefix count.
+// One CTA per token (small T): block_topk picks the k experts (order:
+// selection score descending, id ascending), which are then compacted in
+// ascending id with a block-wide prefix count; each pick's thread writes its
+// index and its weight s / sum(s), the sum taken in ascending id.
 __global__ void __launch_bounds__(1024) route_select_rank(int T, int E, int k, const float* __restrict__ logits,
                                                           const float* __restrict__ bias, int32_t* __restrict__ idx,
                                                           float* __restrict__ wout) {
-  __shared__ float sel_s[1024];
+  __shared__ unsigned long long offers[32 * 16];
+  __shared__ int flag[1024];
   __shared__ int wcount[32];
-  __shared__ int chosen[16];
   __shared__ float chosen_s[16];
   grid_dependency_wait();
   grid_dependents_launch();
   const int t = blockIdx.x, e = threadIdx.x, lane = e & 31, warp = e >> 5;
-  float sc = 0.f, my = -INFINITY;
+  float sc = 0.f;
+  unsigned long long key = 0ull;
   if (e < E) {
     sc = 1.0f / (1.0f + expf(-logits[(size_t)t * E + e]));
-    my = bias ? sc + bias[e] : sc;
-    sel_s[e] = my;
+    key = selection_key(bias ? sc + bias[e] : sc, e);
   }
-  __syncthreads();
-  int rank = 0;
-  if (e < E) {
-    for (int j = 0; j < E; ++j) {
-      const float v = sel_s[j];
-      rank += (v > my || (v == my && j < e)) ? 1 : 0;
-    }
-  }
-  const bool pick = e < E && rank < k;
+  const bool pick = block_topk(key, k, offers, flag);
   const unsigned bal = __ballot_sync(0xffffffffu, pick);
   if (lane == 0) wcount[warp] = __popc(bal);
   __syncthreads();
-  if (pick) {
-    int pos = __popc(bal & ((1u << lane) - 1u));
-    for (int w = 0; w < warp; ++w) pos += wcount[w];
-    if (pos < 16) {
-      chosen[pos] = e;
-      chosen_s[pos] = sc;
-    }
-  }
+  int pos = __popc(bal & ((1u << lane) - 1u));
+  for (int w = 0; w < warp; ++w) pos += wcount[w];
+  if (pick) chosen_s[pos] = sc;   // exactly k picks: pos < k
   __syncthreads();
-  if (e == 0) {
+  if (pick) {
     float tot = 0.f;
     for (int j = 0; j < k; ++j) tot += chosen_s[j];
-    for (int j = 0; j < k; ++j) {
-      idx[(size_t)t * k + j] = chosen[j];
-      wout[(size_t)t * k + j] = chosen_s[j] / tot;
-    }
+    idx[(size_t)t * k + pos] = e;
+    wout[(size_t)t * k + pos] = sc / tot;
   }
 }
 
 // One token: selection and dispatch in one CTA, one dependent launch less
-// between the router and the expert FFN.  It ranks the token's experts exactly
-// as route_select_rank does and dispatches the k picks with dispatch_block: the
-// same bits as route_select_rank followed by dispatch_single.  (For several
-// tokens, a version whose last CTA dispatched all picks measured slower than
-// the two kernels.)
+// between the router and the expert FFN.  The picks are those of
+// route_select_rank, and for one token the dispatch is direct: the picks are
+// distinct and already in ascending id, so pick j sits at position j (perm and
+// inv_perm are the identity on 0..k-1), expert e's count is whether it was
+// picked and its offset the number of picks below e -- the prefix count that
+// places the picks.  The same bits as route_select_rank then dispatch_single.
+// (For several tokens, a version whose last CTA dispatched all picks measured
+// slower than the two kernels.)
 __global__ void __launch_bounds__(1024) route_select_dispatch1(int E, int k, const float* __restrict__ logits,
                                                                const float* __restrict__ bias, int32_t* idx,
                                                                float* __restrict__ wout, int32_t* counts,
                                                                int32_t* offsets, int32_t* perm, int32_t* inv_perm,
                                                                int32_t* active, int32_t* n_active) {
-  __shared__ float sel_s[1024];
+  __shared__ unsigned long long offers[32 * 16];
+  __shared__ int flag[1024];
   __shared__ int wcount[32];
-  __shared__ int chosen[16];
   __shared__ float chosen_s[16];
-  __shared__ int s_cnt[1024];
-  __shared__ int total;
   grid_dependency_wait();
   grid_dependents_launch();
   const int e = threadIdx.x, lane = e & 31, warp = e >> 5;
-  float sc = 0.f, my = -INFINITY;
+  float sc = 0.f;
+  unsigned long long key = 0ull;
   if (e < E) {
     sc = 1.0f / (1.0f + expf(-logits[e]));
-    my = bias ? sc + bias[e] : sc;
-    sel_s[e] = my;
+    key = selection_key(bias ? sc + bias[e] : sc, e);
   }
-  __syncthreads();
-  int rank = 0;
-  if (e < E) {
-    for (int j = 0; j < E; ++j) {
-      const float v = sel_s[j];
-      rank += (v > my || (v == my && j < e)) ? 1 : 0;
-    }
-  }
-  const bool pick = e < E && rank < k;
+  const bool pick = block_topk(key, k, offers, flag);
   const unsigned bal = __ballot_sync(0xffffffffu, pick);
   if (lane == 0) wcount[warp] = __popc(bal);
   __syncthreads();
-  if (pick) {
-    int pos = __popc(bal & ((1u << lane) - 1u));
-    for (int w = 0; w < warp; ++w) pos += wcount[w];
-    if (pos < 16) {
-      chosen[pos] = e;
-      chosen_s[pos] = sc;
-    }
+  int pos = __popc(bal & ((1u << lane) - 1u));   // picks below e
+  for (int w = 0; w < warp; ++w) pos += wcount[w];
+  if (e < E) {
+    counts[e] = pick ? 1 : 0;
+    offsets[e] = pos;
+    if (e == E - 1) offsets[E] = pos + (pick ? 1 : 0);
   }
+  if (pick) {
+    chosen_s[pos] = sc;   // exactly k picks: pos < k
+    idx[pos] = e;
+    active[pos] = e;
+  }
+  if (e < k) {
+    perm[e] = e;
+    inv_perm[e] = e;
+  }
+  if (e == 0) n_active[0] = k;
   __syncthreads();
-  if (e == 0) {
+  if (pick) {
     float tot = 0.f;
     for (int j = 0; j < k; ++j) tot += chosen_s[j];
-    for (int j = 0; j < k; ++j) {
-      idx[j] = chosen[j];
-      wout[j] = chosen_s[j] / tot;
-    }
+    wout[pos] = sc / tot;
   }
-  __syncthreads();
-  dispatch_block(k, E, chosen, counts, offsets, perm, inv_perm, active, n_active, s_cnt, wcount, &total);
 }
 
 }  // namespace

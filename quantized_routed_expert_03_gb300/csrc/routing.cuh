@@ -179,6 +179,55 @@ __device__ __forceinline__ void select_token_warp(int t, int E, int k, const flo
   __syncwarp();
 }
 
+// ---------------------------------------------------------------- one-block top-k
+
+// Selection key of expert e with selection score v: a larger key comes earlier
+// in the selection order (score descending, id ascending).  The score's bits
+// are mapped so that unsigned order is float order; no selection score is -0
+// (a sigmoid in (0, 1] plus a bias rounds to +0 at most), so on finite scores
+// this is exactly the comparison `v > w || (v == w && e < f)`.  Every key of
+// an expert is above 0, the key of an empty thread.
+__device__ __forceinline__ unsigned long long selection_key(float v, int e) {
+  uint32_t b = __float_as_uint(v);
+  b = (b & 0x80000000u) ? ~b : (b | 0x80000000u);
+  return ((unsigned long long)b << 32) | (0xFFFFFFFFu - (uint32_t)e);
+}
+
+// Top k (k <= 16) of one token's experts, one expert per thread: key from
+// selection_key, or 0 for a thread without an expert.  Each warp sorts its 32
+// keys (bitonic, descending) and offers its first k; every expert of the top k
+// is offered (all experts before it are in the top k - 1, so no warp holds k
+// of them ahead of it), and its rank among the offers is its rank among all
+// experts.  The keys are distinct, so exactly k offers have rank < k.  Returns
+// whether the thread's expert is picked.  All threads of the block call it
+// (two barriers).  offers: shared, >= 32 * k keys; flag: shared, >= blockDim.x.
+__device__ __forceinline__ bool block_topk(unsigned long long key, int k, unsigned long long* offers, int* flag) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = (blockDim.x + 31) >> 5;
+  unsigned long long v = key;
+#pragma unroll
+  for (int size = 2; size <= 32; size <<= 1) {
+#pragma unroll
+    for (int stride = size >> 1; stride > 0; stride >>= 1) {
+      const unsigned long long o = __shfl_xor_sync(0xffffffffu, v, stride);
+      const bool keep_max = ((lane & stride) == 0) == ((lane & size) == 0);
+      v = keep_max ? (o > v ? o : v) : (o < v ? o : v);
+    }
+  }
+  if (lane < k) offers[warp * k + lane] = v;
+  flag[threadIdx.x] = 0;
+  __syncthreads();
+  const int n_off = nw * k;
+  if ((int)threadIdx.x < n_off) {
+    const unsigned long long mine = offers[threadIdx.x];
+    int rank = 0;
+    for (int j = 0; j < n_off; ++j) rank += offers[j] > mine ? 1 : 0;
+    const uint32_t id = 0xFFFFFFFFu - (uint32_t)(mine & 0xFFFFFFFFu);
+    if (rank < k && mine != 0ull && id < blockDim.x) flag[id] = 1;
+  }
+  __syncthreads();
+  return flag[threadIdx.x] != 0;
+}
+
 // ---------------------------------------------------------------- dispatch
 
 // Block-wide exclusive scan of one value per thread (blockDim.x <= 1024).

@@ -122,7 +122,9 @@ def test_empty_call_is_a_no_op():
 
 
 @pytest.mark.parametrize("H,E,k,T,bias", [(4096, 288, 8, 1, False), (4096, 288, 8, 8, True), (256, 16, 4, 4, False),
-                                          (512, 64, 6, 7, True), (768, 1024, 16, 8, False), (512, 64, 6, 40, False)])
+                                          (512, 64, 6, 7, True), (768, 1024, 16, 8, False), (512, 64, 6, 40, False),
+                                          (4096, 288, 8, 1, True), (256, 5, 5, 1, False), (256, 37, 16, 1, True),
+                                          (768, 1024, 16, 1, True), (512, 1000, 3, 1, False)])
 def test_route_dispatch_equals_route_then_dispatch(H, E, k, T, bias):
     """qre_route_dispatch (selection and dispatch in one CTA for T <= 8, the two
     calls' kernels above) writes the same bits as qre_route then qre_dispatch."""
@@ -151,3 +153,32 @@ def test_route_dispatch_equals_route_then_dispatch(H, E, k, T, bias):
         np.testing.assert_array_equal(f[name].cpu().numpy(), a[name].cpu().numpy(), err_msg=name)
     np.testing.assert_array_equal(f["active"][:n].cpu().numpy(), a["active"][:n].cpu().numpy())
     assert qre.qre_read_device_status() == 0
+
+
+@pytest.mark.parametrize("E,k", [(16, 4), (288, 8), (1024, 16)])
+def test_route_dispatch_one_token_exact_ties(E, k):
+    """One token whose experts all score the same: the one-CTA selection and
+    dispatch picks experts 0..k-1 (ties to the lower id), each with weight 1/k,
+    and dispatches them in place (perm and inv_perm the identity)."""
+    H = 256
+    shape = qre.make_shape(H, 128, E, k, 32)
+    x = bits_to_bf16_tensor(synthetic.activations_bits(1, H, seed=1), DEV)
+    wr = torch.from_numpy(np.tile(np.linspace(-0.1, 0.1, H, dtype=np.float32), (E, 1))).to(DEV)
+    ws = torch.empty(max(qre.qre_workspace_size(shape, 1), 256), dtype=torch.uint8, device=DEV)
+    i32 = dict(dtype=torch.int32, device=DEV)
+    o = {"idx": torch.full((1, k), -1, **i32), "w": torch.full((1, k), -1.0, device=DEV),
+         "counts": torch.full((E,), -1, **i32), "offsets": torch.full((E + 1,), -1, **i32),
+         "perm": torch.full((k,), -1, **i32), "inv_perm": torch.full((k,), -1, **i32),
+         "active": torch.full((E,), -1, **i32), "n_active": torch.full((4,), -1, **i32)}
+    qre.qre_route_dispatch(shape, 1, x, wr, None, o["idx"], o["w"], o["counts"], o["offsets"], o["perm"],
+                           o["inv_perm"], o["active"], o["n_active"], ws)
+    torch.cuda.synchronize()
+    g = {n: t.cpu().numpy() for n, t in o.items()}
+    np.testing.assert_array_equal(g["idx"][0], np.arange(k))
+    np.testing.assert_allclose(g["w"][0], 1.0 / k, rtol=1e-6, atol=0)
+    np.testing.assert_array_equal(g["counts"], (np.arange(E) < k).astype(np.int32))
+    np.testing.assert_array_equal(g["offsets"], np.minimum(np.arange(E + 1), k))
+    np.testing.assert_array_equal(g["perm"], np.arange(k))
+    np.testing.assert_array_equal(g["inv_perm"], np.arange(k))
+    np.testing.assert_array_equal(g["active"][:k], np.arange(k))
+    assert g["n_active"][0] == k

@@ -565,7 +565,10 @@ def measure_workload(name, args, K, W, rank, local_rank, world, device, log, cpu
                    **({"host_unit_cost": host_cost} if host_cost > 1 else {})},
         "gpu_launches": None, "roofline": roofline, "clocks": clocks, "e2e": None,
     }
-    launches_per_layer = (2 if T <= 8 else 2 + (1 if T * k <= 1024 else 3)) + (3 if prefill else 2) + 1
+    # route + dispatch: one token two kernels (logits GEMV, selection with the
+    # dispatch), else logits, selection and one (or three) dispatch kernels;
+    # expert FFN: gate/up + down (decode) or gather + two grouped GEMMs; combine
+    launches_per_layer = (2 if T == 1 else 2 + (1 if T * k <= 1024 else 3)) + (3 if prefill else 2) + 1
     if cfg.live_cache:
         launches_per_layer += 2
         rec["cache"] = cache_misses(wl, xs, T, first=warm + K + 1)

@@ -12,7 +12,8 @@ namespace {
 // KMAX > 0: top_k <= KMAX, and every weight, row index and expert row of the
 // thread is loaded before the first sum (one round of memory latency instead
 // of k dependent ones); KMAX == 0: any top_k, one pick at a time.  Same sums,
-// same order, same bits either way.
+// same order, same bits either way.  A pick whose row index is out of range
+// (one a dispatch that met a bad expert id left unset) adds nothing.
 template <int KMAX>
 __global__ void __launch_bounds__(256) combine_kernel(int T, int H, int k, const float* __restrict__ eo,
                                                       const float* __restrict__ w, const int32_t* __restrict__ inv_perm,
@@ -42,7 +43,9 @@ __global__ void __launch_bounds__(256) combine_kernel(int T, int H, int k, const
     float4 v[KMAX];
 #pragma unroll
     for (int j = 0; j < KMAX; ++j)
-      if (j < k) v[j] = __ldg(reinterpret_cast<const float4*>(eo + (size_t)qj[j] * H + h));
+      if (j < k)
+        v[j] = (unsigned)qj[j] < (unsigned)(T * k) ? __ldg(reinterpret_cast<const float4*>(eo + (size_t)qj[j] * H + h))
+                                                   : make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
     for (int j = 0; j < KMAX; ++j)
       if (j < k) add(wj[j], v[j]);
@@ -50,7 +53,8 @@ __global__ void __launch_bounds__(256) combine_kernel(int T, int H, int k, const
     for (int j = 0; j < k; ++j) {
       const float wj = __ldg(w + (size_t)t * k + j);
       const int q = __ldg(inv_perm + (size_t)t * k + j);
-      add(wj, __ldg(reinterpret_cast<const float4*>(eo + (size_t)q * H + h)));
+      add(wj, (unsigned)q < (unsigned)(T * k) ? __ldg(reinterpret_cast<const float4*>(eo + (size_t)q * H + h))
+                                              : make_float4(0.f, 0.f, 0.f, 0.f));
     }
   }
   acc.x += sh.x;

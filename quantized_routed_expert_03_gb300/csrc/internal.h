@@ -1,6 +1,7 @@
 // internal.h -- host-side declarations shared by the library's translation units.
 #pragma once
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <stddef.h>
 #include <stdint.h>
@@ -74,9 +75,10 @@ cudaError_t launch_dependent(void (*kernel)(Params...), dim3 grid, dim3 block, s
 cudaError_t launch_quantize(int n_rows, int k_dim, int group, const float* w, const float* w2, uint8_t* packed,
                             uint16_t* scales, int* status, cudaStream_t stream);
 
+// allow_tc: the workspace has route_ws_bytes (false: the logits only, the CUDA-core kernels).
 cudaError_t launch_route(const qre_layer_shape& s, int T, const uint16_t* x, const float* w_router,
                          const float* bias, int32_t* topk_idx, float* topk_w, void* ws,
-                         cudaStream_t stream);
+                         cudaStream_t stream, bool allow_tc = true);
 
 // Router + dispatch in two launches (GEMV, then selection and dispatch in one
 // CTA) when route_dispatch_fused(s, T) (one token); the outputs of launch_route
@@ -119,5 +121,20 @@ cudaError_t launch_read_probe(const void* src, size_t bytes, uint32_t* sink, cud
 
 cudaError_t launch_combine(const qre_layer_shape& s, int T, const float* expert_out, const float* topk_w,
                            const int32_t* inv_perm, float* y_f32, uint16_t* y_bf16, cudaStream_t stream);
+
+// 2-D bf16 row-major [rows][cols] tensor map: boxes of 64 columns x box_rows
+// rows, 128-byte swizzle, zero fill outside.  False when the driver refuses it
+// (e.g. a base that is not 16-byte aligned).
+bool make_tmap_bf16(CUtensorMap* m, const void* base, long long rows, int cols, int box_rows);
+
+// Router logits on the tensor cores (long token batches): whether a call of T
+// tokens takes them, the workspace they need beyond the logits (the router
+// weights split into three bf16 parts), and the launch (split, then GEMM).
+bool route_tc_wanted(const qre_layer_shape& s, int T);     // by shape (workspace sizing)
+bool route_tc_eligible(const qre_layer_shape& s, int T);   // and shared memory of this device
+size_t route_tc_split_bytes(const qre_layer_shape& s);
+// Returns false when the tensor maps cannot be made (nothing launched then).
+bool launch_route_logits_tc(const qre_layer_shape& s, int T, const uint16_t* x, const float* w_router,
+                            float* logits, void* split_ws, cudaStream_t stream, cudaError_t* err);
 
 }  // namespace qre

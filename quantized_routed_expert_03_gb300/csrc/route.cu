@@ -253,7 +253,16 @@ __global__ void __launch_bounds__(1024) route_select_dispatch1(int E, int k, con
 
 }  // namespace
 
-size_t route_ws_bytes(const qre_layer_shape& s, int T) { return (size_t)T * s.n_experts * sizeof(float); }
+// The logits, and for long batches the router weights split into three bf16
+// parts after them (route_tc.cu).
+size_t route_logits_bytes(const qre_layer_shape& s, int T) {
+  return ((size_t)T * s.n_experts * sizeof(float) + 255) & ~(size_t)255;
+}
+
+size_t route_ws_bytes(const qre_layer_shape& s, int T) {
+  return route_tc_wanted(s, T) ? route_logits_bytes(s, T) + route_tc_split_bytes(s)
+                               : (size_t)T * s.n_experts * sizeof(float);
+}
 
 bool route_dispatch_fused(const qre_layer_shape&, int T) { return T == 1; }
 
@@ -280,7 +289,8 @@ cudaError_t launch_route_dispatch(const qre_layer_shape& s, int T, const uint16_
 }
 
 cudaError_t launch_route(const qre_layer_shape& s, int T, const uint16_t* x, const float* w_router,
-                         const float* bias, int32_t* topk_idx, float* topk_w, void* ws, cudaStream_t stream) {
+                         const float* bias, int32_t* topk_idx, float* topk_w, void* ws, cudaStream_t stream,
+                         bool allow_tc) {
   float* logits = static_cast<float*>(ws);
   const int H = s.hidden, E = s.n_experts;
   cudaError_t err;
@@ -295,6 +305,10 @@ cudaError_t launch_route(const qre_layer_shape& s, int T, const uint16_t* x, con
       if (err != cudaSuccess) return err;
     }
     err = launch_dependent(kernel, dim3((E + 1) / 2), dim3(256), dyn, stream, T, H, E, x, w_router, logits, stage);
+  } else if (allow_tc && route_tc_eligible(s, T) &&
+             launch_route_logits_tc(s, T, x, w_router, logits, static_cast<char*>(ws) + route_logits_bytes(s, T),
+                                    stream, &err)) {
+    // tensor cores (long batches; the CUDA-core GEMM below when the tensor maps cannot be made)
   } else {
     dim3 grid((E + BN - 1) / BN, (T + BM - 1) / BM);
     err = launch_dependent(route_logits_gemm, grid, dim3(256), 0, stream, T, H, E, x, w_router, logits);

@@ -87,7 +87,7 @@ QRE_API qre_status qre_route_noalloc(const qre_layer_shape* shape, int32_t T, co
     scratch = g_scratch_ptr[dev];
   }
   e = qre::launch_route(*shape, T, x_bf16, w_router, bias, topk_idx, topk_w, scratch,
-                        reinterpret_cast<cudaStream_t>(stream));
+                        reinterpret_cast<cudaStream_t>(stream), /*allow_tc=*/false);   // the scratch holds logits only
   if (e != cudaSuccess) {
     qre::set_error_message("launch: %s (%s)", cudaGetErrorName(e), cudaGetErrorString(e));
     return QRE_ERR_CUDA;

@@ -182,3 +182,52 @@ def test_route_dispatch_one_token_exact_ties(E, k):
     np.testing.assert_array_equal(g["inv_perm"], np.arange(k))
     np.testing.assert_array_equal(g["active"][:k], np.arange(k))
     assert g["n_active"][0] == k
+
+
+def _route_with_logits(H, E, k, T, x_bits, wr):
+    """qre_route, plus the logits it leaves at the start of its workspace (the
+    router writes them there before the selection reads them)."""
+    shape = qre.make_shape(H, 128, E, k, 32)
+    ws = torch.zeros(max(qre.qre_workspace_size(shape, T), 256), dtype=torch.uint8, device=DEV)
+    idx = torch.empty((T, k), dtype=torch.int32, device=DEV)
+    w = torch.empty((T, k), dtype=torch.float32, device=DEV)
+    qre.qre_route(shape, T, bits_to_bf16_tensor(x_bits, DEV), torch.from_numpy(wr).to(DEV), None, idx, w, ws)
+    torch.cuda.synchronize()
+    logits = ws[:T * E * 4].view(torch.float32).reshape(T, E).cpu().numpy()
+    return idx.cpu().numpy(), w.cpu().numpy(), logits
+
+
+@pytest.mark.parametrize("H,E,T", [(4096, 288, 1024), (256, 16, 2048), (768, 1000, 1100), (512, 300, 1030)])
+def test_route_tensor_core_split_is_exact(H, E, T):
+    """Long batches take the tensor-core logits (the fp32 router weights as three
+    bf16 parts): with one-hot tokens every logit is a single weight, which the
+    three exact part products must give back bit for bit."""
+    rng = np.random.default_rng(E + T)
+    wr = (rng.standard_normal((E, H)) * 0.05).astype(np.float32)
+    cols = (np.arange(T) * 37) % H
+    x = np.zeros((T, H), np.float64)
+    x[np.arange(T), cols] = 1.0
+    x_bits = omoe.f32_to_bf16_bits(x.astype(np.float32))
+    _, _, logits = _route_with_logits(H, E, 4, T, x_bits, wr)
+    np.testing.assert_array_equal(logits, wr[:, cols].T)
+
+
+@pytest.mark.parametrize("H,E,k,T", [(4096, 288, 8, 1024), (4096, 288, 8, 1500), (256, 16, 4, 2048),
+                                     (768, 1000, 16, 1100), (512, 300, 6, 1030)])
+def test_route_tensor_core_logits_match_oracle(H, E, k, T):
+    """Tensor-core logits against the fp64 oracle.  Bound: the products are exact,
+    so the error is the tensor core's fp32 accumulation (3 H / 16 steps of 16
+    products; measured 1.7e-6 of sum |x w| at H 4096); 1e-5 of sum |x w| is about
+    6x that and ~200x below the error of a lost second weight part (2^-9 of each
+    weight); a lost third part is caught bit-exactly by the one-hot test."""
+    x_bits = synthetic.activations_bits(T, H, seed=5)
+    wr = synthetic.router_weights(E, H, seed=5)
+    idx, w, logits = _route_with_logits(H, E, k, T, x_bits, wr)
+    x = omoe.bf16_bits_to_f64(x_bits)
+    ref = x @ wr.astype(np.float64).T
+    scale = np.abs(x) @ np.abs(wr.astype(np.float64)).T
+    ratio = np.max(np.abs(logits - ref) / np.maximum(scale, 1e-30))
+    print(f"max |logit error| / sum|x w| = {ratio:.3e}")
+    assert ratio < 1e-5
+    near = check_routing(idx, w, omoe.route(x, wr, None, k))
+    assert near <= max(1, T // 500)

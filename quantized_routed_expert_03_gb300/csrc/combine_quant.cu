@@ -40,15 +40,20 @@ __global__ void __launch_bounds__(256) combine_kernel(int T, int H, int k, const
         wj[j] = __ldg(w + (size_t)t * k + j);
         qj[j] = __ldg(inv_perm + (size_t)t * k + j);
       }
+    // an out-of-range row index reads row 0 (the loads stay unconditional and in
+    // bounds, all k in flight together) and its term is skipped in the sums
     float4 v[KMAX];
+    uint32_t okm = 0;
 #pragma unroll
     for (int j = 0; j < KMAX; ++j)
-      if (j < k)
-        v[j] = (unsigned)qj[j] < (unsigned)(T * k) ? __ldg(reinterpret_cast<const float4*>(eo + (size_t)qj[j] * H + h))
-                                                   : make_float4(0.f, 0.f, 0.f, 0.f);
+      if (j < k) {
+        const bool ok = (unsigned)qj[j] < (unsigned)(T * k);
+        okm |= (ok ? 1u : 0u) << j;
+        v[j] = __ldg(reinterpret_cast<const float4*>(eo + (size_t)(ok ? qj[j] : 0) * H + h));
+      }
 #pragma unroll
     for (int j = 0; j < KMAX; ++j)
-      if (j < k) add(wj[j], v[j]);
+      if (j < k && ((okm >> j) & 1u)) add(wj[j], v[j]);
   } else {
     for (int j = 0; j < k; ++j) {
       const float wj = __ldg(w + (size_t)t * k + j);

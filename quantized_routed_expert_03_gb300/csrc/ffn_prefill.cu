@@ -99,35 +99,46 @@ struct SmemLayout {
 // ---------------------------------------------------------------- gather
 
 // Rows q in [q0, q1) of the pick order (q >= T*k: the shared expert's token q - T*k),
-// written at Xg row q - q0.
+// written at Xg row q - q0.  A thread converts kGatherChunks 16-byte pieces of
+// one row (columns c0 + j * H / kGatherChunks): one perm load and all
+// its token loads in flight together, every store coalesced across the warp.
+constexpr int kGatherChunks = 4;
 __global__ void __launch_bounds__(256) gather_x_kernel(int T, int H, int k, long long q0, long long q1,
                                                        const uint16_t* __restrict__ x,
                                                        const int32_t* __restrict__ perm, __half* __restrict__ xg,
                                                        int* status) {
+  grid_dependency_wait();   // perm, from the dispatch
+  grid_dependents_launch();
   const long long P = (long long)T * k;
-  const int per_row = H / 8;
+  const int tpr = H / (8 * kGatherChunks);   // threads per row
   const long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x;
-  if (i >= (q1 - q0) * per_row) return;
-  const long long qi = i / per_row;           // row within this launch's range
-  const int c = (int)(i - qi * per_row) * 8;  // first of the thread's 8 columns
+  if (i >= (q1 - q0) * tpr) return;
+  const long long qi = i / tpr;               // row within this launch's range
+  const int c0 = (int)(i - qi * tpr) * 8;     // first of the thread's columns
   const long long q = q0 + qi;
   const int t = q < P ? __ldg(perm + q) / k : (int)(q - P);
-  const uint4 v = __ldg(reinterpret_cast<const uint4*>(x + (size_t)t * H + c));
-  float f[8];
-  f[0] = bf16_bits_to_float(v.x & 0xFFFFu); f[1] = bf16_bits_to_float(v.x >> 16);
-  f[2] = bf16_bits_to_float(v.y & 0xFFFFu); f[3] = bf16_bits_to_float(v.y >> 16);
-  f[4] = bf16_bits_to_float(v.z & 0xFFFFu); f[5] = bf16_bits_to_float(v.z >> 16);
-  f[6] = bf16_bits_to_float(v.w & 0xFFFFu); f[7] = bf16_bits_to_float(v.w >> 16);
-  uint32_t o[4];
+  uint4 v[kGatherChunks];
+#pragma unroll
+  for (int j = 0; j < kGatherChunks; ++j)
+    v[j] = __ldg(reinterpret_cast<const uint4*>(x + (size_t)t * H + c0 + j * tpr * 8));
   bool bad = false;
 #pragma unroll
-  for (int j = 0; j < 4; ++j) {   // pair order (x_j, x_{j+4}), the order the weight decode produces
-    const __half2 h = __floats2half2_rn(f[j], f[j + 4]);
-    bad |= __hisinf(__low2half(h)) || __hisinf(__high2half(h));
-    o[j] = h2_as_u32(h);
+  for (int j = 0; j < kGatherChunks; ++j) {
+    float f[8];
+    f[0] = bf16_bits_to_float(v[j].x & 0xFFFFu); f[1] = bf16_bits_to_float(v[j].x >> 16);
+    f[2] = bf16_bits_to_float(v[j].y & 0xFFFFu); f[3] = bf16_bits_to_float(v[j].y >> 16);
+    f[4] = bf16_bits_to_float(v[j].z & 0xFFFFu); f[5] = bf16_bits_to_float(v[j].z >> 16);
+    f[6] = bf16_bits_to_float(v[j].w & 0xFFFFu); f[7] = bf16_bits_to_float(v[j].w >> 16);
+    uint32_t o[4];
+#pragma unroll
+    for (int m = 0; m < 4; ++m) {   // pair order (x_m, x_{m+4}), the order the weight decode produces
+      const __half2 h = __floats2half2_rn(f[m], f[m + 4]);
+      bad |= __hisinf(__low2half(h)) || __hisinf(__high2half(h));
+      o[m] = h2_as_u32(h);
+    }
+    *reinterpret_cast<uint4*>(xg + (size_t)(q - q0) * H + c0 + j * tpr * 8) = make_uint4(o[0], o[1], o[2], o[3]);
   }
   if (bad) set_status(status, QRE_DEV_FP16_RANGE);
-  *reinterpret_cast<uint4*>(xg + (size_t)(q - q0) * H + c) = make_uint4(o[0], o[1], o[2], o[3]);
 }
 
 // ---------------------------------------------------------------- GEMM
@@ -586,12 +597,12 @@ cudaError_t launch_ffn_prefill(const qre_layer_shape& s, int T, const uint16_t* 
   __half* h16 = reinterpret_cast<__half*>(static_cast<uint8_t*>(ws) + align256((size_t)rows * s.hidden * 2));
 
   {
-    const long long n = (q1 - q0) * (s.hidden / 8);
-    if (n > 0)
-      gather_x_kernel<<<(unsigned)((n + 255) / 256), 256, 0, stream>>>(T, s.hidden, s.top_k, q0, q1, x, perm, xg,
-                                                                       status);
-    cudaError_t e = cudaGetLastError();
-    if (e != cudaSuccess) return e;
+    const long long n = (q1 - q0) * (s.hidden / (8 * kGatherChunks));
+    if (n > 0) {
+      cudaError_t e = launch_dependent(gather_x_kernel, dim3((unsigned)((n + 255) / 256)), dim3(256), 0, stream, T,
+                                       s.hidden, s.top_k, q0, q1, x, perm, xg, status);
+      if (e != cudaSuccess) return e;
+    }
   }
   CUtensorMap tx, th;
   if (!make_tmap(&tx, xg, rows, s.hidden) || !make_tmap(&th, h16, rows, s.inter)) return cudaErrorInvalidValue;

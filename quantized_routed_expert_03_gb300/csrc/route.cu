@@ -28,6 +28,15 @@ __global__ void __launch_bounds__(256) route_logits_gemv(int T, int H, int E, co
                                                          int stage) {
   __shared__ float part[2][4][TMAX];
   extern __shared__ uint4 xs_dyn[];   // T * H bf16 when staged (dynamic size > 0)
+  // While the kernel before finishes: start this CTA's two weight rows on their
+  // way into L2 (a prefetch only warms the cache; the loads after the wait read
+  // whatever is current).
+  {
+    const int e0 = blockIdx.x * 2, rows = E - e0 < 2 ? E - e0 : 2;
+    const char* w0 = reinterpret_cast<const char*>(W + (size_t)e0 * H);
+    for (int l = threadIdx.x; l < rows * H / 32; l += blockDim.x)
+      asm volatile("prefetch.global.L2 [%0];" ::"l"(w0 + 128 * l));
+  }
   grid_dependency_wait();
   grid_dependents_launch();
   logits_gemv_pair<TMAX>(blockIdx.x * 2, T, H, E, x, W, logits, part, stage ? xs_dyn : nullptr);

@@ -5,14 +5,17 @@
 // this library reads it as sigmoid scores with an optional selection-only bias,
 // ties to the lower expert id, and weights s / sum(s) over the selection.
 //
-// Two logits kernels:
+// Three logits kernels:
 //   * T <= 16 (decode): a GEMV that streams W_r once; each CTA owns two expert
 //     rows and keeps all T tokens' partial sums in registers.
-//   * T > 16 (prefill): a tiled fp32 GEMM (64 tokens x 64 experts per CTA).
-// Both accumulate in a fixed order, so results are deterministic.  Selection:
-// for T <= 64 one CTA per token ranks every expert against all others in
-// parallel; for larger T one warp per token runs k rounds of arg-max.  Both
-// give the same bits (same fp32 scores, same exact order, same summation).
+//   * 16 < T < 1024: a tiled fp32 GEMM (64 tokens x 96 experts per CTA).
+//   * T >= 1024: the tensor cores with W_r split into three exact bf16 parts
+//     (route_tc.cu).
+// Each accumulates in a fixed order, so results are deterministic.  Selection:
+// for T <= 64 one CTA per token (block_topk: warp bitonic sorts, then ranks
+// among the warps' offers); for larger T one warp per token runs k rounds of
+// arg-max.  Both give the same bits (same fp32 scores, same exact order, same
+// summation).
 #include "common.cuh"
 #include "internal.h"
 #include "routing.cuh"

@@ -73,6 +73,8 @@ CONFIGS = {
                                    note="T4, Zipf(1.1), 16 layers; 40 static HBM experts + 148 HBM slots run as an "
                                         "LFU(0.995) cache (starting with ranks 41-188), misses copied from pinned "
                                         "host memory every step; the other experts read zero-copy until admitted"),
+    "decode8_zipf_x1": LayerConfig("decode8_zipf_x1", 4096, 2048, 288, 8, 128, 8, layers=1, zipf=True,
+                                   note="profiling case: one layer of decode8_zipf_x42 (3.7 GB of packed experts)"),
     "prefill2048_e64": LayerConfig("prefill2048_e64", 4096, 2048, 64, 8, 128, 2048,
                                    note="profiling case: the prefill8192 kernels on 64 experts and 2048 tokens "
                                         "(~256 tokens per expert, 0.84 GB of packed experts)"),

@@ -104,6 +104,20 @@ def test_mid_layers_match_oracle(cfg, T):
     _check_layer(built, got, ref)
 
 
+@pytest.mark.parametrize("H,I", [(512, 512), (256, 128)], ids=["fp8_kernels", "fp16_kernels"])
+def test_decode_largest_group_table_matches_oracle(H, I):
+    """1024 experts top-16 and eight tokens with distinct picks: 128 active
+    experts and the shared one, the decode kernels' largest group table (and a
+    grid with more groups than any full-size decode); H 512 runs the FP8
+    kernels, H 256 / I 128 (K slices of 64) the fp16 ones."""
+    cfg = synthetic.LayerConfig("maxgroups", H, I, 1024, 16, 128, 8)
+    built = BuiltLayer(cfg.hidden, cfg.inter, cfg.n_experts, cfg.top_k, cfg.group, 8, DEV, numpy_source(cfg))
+    x_bits, wr, _ = _inputs(cfg, 8, step=5)
+    got = _run(built, x_bits, wr, None)
+    assert got["n_active"] >= 120
+    _check_layer(built, got, built.oracle_layer(x_bits, wr, None))
+
+
 def test_wide_intermediate_layer_matches_oracle():
     """I = 4096: the down projection's h of one expert fills most of shared
     memory, so the down kernel holds one expert at a time and gives every CTA a

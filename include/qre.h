@@ -164,7 +164,10 @@ QRE_API qre_status qre_quantize_gate_up(int32_t inter, int32_t hidden, int32_t g
                                         qre_stream_t stream);
 
 /*
- * Router: logits l = x W_r^T (fp32 accumulation), scores s = sigmoid(l),
+ * Router: logits l = x W_r^T (fp32 accumulation: below 1024 tokens one fp32
+ * FMA chain over ascending h per logit; from 1024 tokens on the tensor cores,
+ * with W_r split into three bf16 parts whose sum is W_r exactly, so every
+ * product is exact and only the accumulation order differs), scores s = sigmoid(l),
  * selection score s + bias (bias is selection-only; NULL = 0), the top_k experts
  * by selection score with ties to the lower id, written in ascending id order,
  * and weights w = s / sum(s over the selection).  Top-8 of 288: GLM-5.3-Flash
@@ -184,8 +187,10 @@ QRE_API qre_status qre_route(const qre_layer_shape* shape, int32_t T, const uint
                      qre_stream_t stream);
 
 /*
- * qre_route without a workspace: the same router and the same results as
- * qre_route, for callers that cannot allocate device memory -- code that runs
+ * qre_route without a workspace: the same router as qre_route, with the same
+ * bits below 1024 tokens (its logits always come from the fp32 FMA chains,
+ * since the split weights of the tensor-core path need workspace), for callers
+ * that cannot allocate device memory -- code that runs
  * inside a host framework which owns every device allocation, loops that must
  * not allocate once they run, or callers that only hold the input and output
  * buffers someone else gave them.  The pages have no counterpart; it is an

@@ -668,7 +668,7 @@ struct Layout8 {
 __host__ __device__ inline Layout8 make_layout8(int MODE, int K, int nB, int TT) {
   Layout8 L;
   L.b_off = 0;                                          // nB x (bn8 rows x K bytes, swizzled; 1024-aligned)
-  L.ec_off = L.b_off + nB * bn8(MODE, TT) * K;          // nB x (E[TT][K/128], C[TT][K/128]) fp32
+  L.ec_off = L.b_off + nB * bn8(MODE, TT) * K;          // nB x 2 x TT x K/128 fp32 factors (see Et)
   L.ring_off = (L.ec_off + nB * 2 * TT * (K / SK8) * 4 + 127) & ~127;   // [stage][kWG] x 8 KB
   L.red_off = L.ring_off + ring8_stages(MODE, TT) * kWG * kStageBytes8;   // 2 x kWG x BM x TT fp32
   L.bar_off = L.red_off + 2 * kWG * BM * TT * 4;
@@ -744,8 +744,13 @@ __device__ __noinline__ void e4m3_b_job(int job, const uint4 raw, int T, int KG,
     *reinterpret_cast<uint32_t*>(Bs + jb * b_bytes + b8_offset(NT * n + j, g * SK8 + 4 * lane, BN8)) = t[j];
   if (lane == 0) {
     float* ec = Et + jb * 2 * TT * KG;
-    ec[n * KG + g] = 512.0f * down;   // the codes carry 2^-9
-    ec[TT * KG + n * KG + g] = 8.0f * back * down;
+    if constexpr (TT == 1) {
+      ec[n * KG + g] = 512.0f * down;   // the codes carry 2^-9
+      ec[TT * KG + n * KG + g] = 8.0f * back * down;
+    } else {   // [KG][TT] pairs: a stage's factors of all tokens in 16-byte pieces
+      ec[(g * TT + n) * 2] = 512.0f * down;
+      ec[(g * TT + n) * 2 + 1] = 8.0f * back * down;
+    }
   }
 }
 
@@ -801,8 +806,9 @@ __global__ void __launch_bounds__(kThreads, 1) ffn_e4m3_kernel(const FfnParams p
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
   const Layout8 L = make_layout8(MODE, p.K, p.nB, TT);
   uint8_t* Bs = smem + L.b_off;                                    // buffer j at j * b_bytes
-  float* Et = reinterpret_cast<float*>(smem + L.ec_off);          // buffer j at j * 2 * TT * KG: [TT][KG] 2^(9-e),
-                                                                   // then [TT][KG] 8 * sum of the represented values
+  float* Et = reinterpret_cast<float*>(smem + L.ec_off);          // buffer j at j * 2 * TT * KG: TT = 1 [KG] 2^(9-e)
+                                                                   // then [KG] 8 * sum of the represented values;
+                                                                   // TT = 8 [KG][TT] (2^(9-e), 8 * sum) pairs
   float* red = reinterpret_cast<float*>(smem + L.red_off);
   uint64_t* a_full = reinterpret_cast<uint64_t*>(smem + L.bar_off);
   uint64_t* done = a_full + kWG * 3;
@@ -1110,10 +1116,13 @@ __global__ void __launch_bounds__(kThreads, 1) ffn_e4m3_kernel(const FfnParams p
         else
           tmem_ld_32x32b_x16(tlane + tmem_wg + kD0 + BN8 * db, dv);
         tmem_ld_wait();
+        const float4* eg = reinterpret_cast<const float4*>(ec + g * 2 * TT);   // (2^(9-e), C) per token
 #pragma unroll
-        for (int n = 0; n < TT; ++n) {
-          const float d = add_terms<NT>(dv + NT * n);
-          acc[n] = fmaf(sc, fmaf(d, ec[n * KG + g], -ec[(TT + n) * KG + g]), acc[n]);
+        for (int n2 = 0; n2 < TT / 2; ++n2) {
+          const float4 q = eg[n2];
+          const float d0 = add_terms<NT>(dv + NT * (2 * n2)), d1 = add_terms<NT>(dv + NT * (2 * n2 + 1));
+          acc[2 * n2] = fmaf(sc, fmaf(d0, q.x, -q.y), acc[2 * n2]);
+          acc[2 * n2 + 1] = fmaf(sc, fmaf(d1, q.z, -q.w), acc[2 * n2 + 1]);
         }
       }
       if (est == nst - 1) {

@@ -18,6 +18,7 @@ import torch
 import synthetic
 import quantized_routed_expert_03_gb300 as qre
 from oracle import moe as omoe
+from oracle import quant as oquant
 
 from gpu_support import (BuiltLayer, bf16_tensor_to_bits, bits_to_bf16_tensor, check_routing, numpy_source,
                          rel_rms, torch_sources)
@@ -253,8 +254,9 @@ def test_full_size_decode_eight_tokens_zipf():
 def test_full_size_expert_cache_host_tier():
     """Expert-cache placement: popularity ranks > 188 read zero-copy from pinned host memory.
 
-    The FFN outputs are checked for the tokens that picked a host-resident expert
-    (at most two), plus routing and dispatch for all four."""
+    Routing, dispatch, every expert_out row and the layer output are checked for
+    all four tokens of a step in which at least one token picked a
+    host-resident expert."""
     cfg = synthetic.CONFIGS["cache4_x42"]
     layer = 3
     host_src, dev_src = torch_sources(cfg, layer, DEV)
@@ -265,11 +267,11 @@ def test_full_size_expert_cache_host_tier():
     for step in range(8):
         x_bits, wr, _ = _inputs(cfg, 4, layer=layer, step=step)
         got = _run(built, x_bits, wr, bias)
-        toks = [t for t in range(4) if host[got["idx"][t]].any()][:2]
-        if toks:
+        if any(host[got["idx"][t]].any() for t in range(4)):
             break
-    assert toks, "no token picked a host-resident expert in 8 steps"
-    _check_layer(built, got, built.oracle_layer(x_bits, wr, bias, tokens=toks), tokens=toks)
+    else:
+        raise AssertionError("no token picked a host-resident expert in 8 steps")
+    _check_layer(built, got, built.oracle_layer(x_bits, wr, bias))
 
 
 # ---------------------------------------------------------------- prefill (T > 8): tcgen05 grouped GEMM
@@ -326,7 +328,9 @@ def test_prefill_token_order_invariance_bit_exact():
 @pytest.mark.slow
 def test_full_size_prefill_8192_sampled():
     """Prefill chunk: 8192 tokens, uniform routing, full size.  Routing and dispatch
-    are checked for every token, the FFN outputs for three sampled tokens."""
+    are checked for every token; the layer output for three sampled tokens; and
+    every expert_out row of three whole experts (first, middle and last active
+    expert, ~230 tokens each: the grouped GEMM's full tiles and ragged tails)."""
     cfg = synthetic.CONFIGS["prefill8192"]
     host_src, dev_src = torch_sources(cfg, 0, DEV)
     built = BuiltLayer(cfg.hidden, cfg.inter, cfg.n_experts, cfg.top_k, cfg.group, cfg.tokens, DEV, host_src,
@@ -354,3 +358,14 @@ def test_full_size_prefill_8192_sampled():
     err = rel_rms(got["y"][toks], ref["y"][toks])
     assert err <= PREFILL_TOL, err
     np.testing.assert_array_equal(got["y_bf16"], omoe.f32_to_bf16_bits(got["y"]))
+    # whole experts: every row the GPU wrote for them (its own dispatch) against
+    # the oracle's expert FFN of those tokens
+    n_act = int(got["n_active"])
+    for e in (int(got["active"][0]), int(got["active"][n_act // 2]), int(got["active"][n_act - 1])):
+        lo, hi = int(got["offsets"][e]), int(got["offsets"][e + 1])
+        rows_tok = got["perm"][lo:hi] // k
+        Wg, Wu, Wd = oquant.dequantize_expert(built.oracle_experts[e], cfg.hidden, cfg.inter, cfg.group)
+        want = omoe.expert_ffn(ref["x"][rows_tok], Wg, Wu, Wd)
+        mine = got["expert_out"][lo:hi]
+        row_err = np.linalg.norm(mine - want, axis=1) / np.linalg.norm(want, axis=1)
+        assert hi - lo > 100 and row_err.max() <= PREFILL_TOL, (e, hi - lo, row_err.max())

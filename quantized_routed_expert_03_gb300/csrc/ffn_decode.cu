@@ -1093,6 +1093,9 @@ __global__ void __launch_bounds__(kThreads, 1) ffn_e4m3_kernel(const FfnParams p
     const uint32_t idesc = umma_idesc_e4m3(BM, BN8);
     const uint32_t bbase = smem_addr(Bs);
 
+    // down: the local units from u_split on belong to the range's second group
+    // (its h in the second B buffer; a range spans at most nB <= 2 groups)
+    const int u_split = (a_first + 1) * upe - ub;
     float acc[TT];
 #pragma unroll
     for (int n = 0; n < TT; ++n) acc[n] = 0.f;
@@ -1100,7 +1103,7 @@ __global__ void __launch_bounds__(kThreads, 1) ffn_e4m3_kernel(const FfnParams p
     auto readback = [&](int est, int eul, int db, uint32_t sp) {
       const float sc = __half2float(__ushort_as_half((unsigned short)sp));
       const int g = g0 + est;
-      const float* ec = MODE == 0 ? Et : Et + ((ub + eul) / upe - a_first) * 2 * TT * KG;
+      const float* ec = MODE == 0 ? Et : Et + (eul >= u_split ? 2 * TT * KG : 0);
       if constexpr (TT == 1) {
         uint32_t dv[4];
         asm volatile("tcgen05.ld.sync.aligned.32x32b.x4.b32 {%0,%1,%2,%3}, [%4];"
@@ -1147,7 +1150,7 @@ __global__ void __launch_bounds__(kThreads, 1) ffn_e4m3_kernel(const FfnParams p
       const int ib = i & 1;
       mbar_wait_bounded(&a_full[wg * 3 + ib], (i >> 1) & 1, abort_flag, p.status, p.wait_ns);
       tc_fence_after();
-      const uint32_t bbuf = MODE == 0 ? 0u : (uint32_t)((ub + iul) / upe - a_first) * b_bytes;
+      const uint32_t bbuf = MODE == 0 ? 0u : (iul >= u_split ? b_bytes : 0u);
       const uint32_t bstage = bbase + bbuf + (uint32_t)((g0 + ist) * (BN8 * 128));
 #pragma unroll
       for (int q = 0; q < 4; ++q)

@@ -985,12 +985,21 @@ __global__ void __launch_bounds__(kThreads, 1) ffn_e4m3_kernel(const FfnParams p
   const uint4* lptr = nullptr;
   const unsigned short* lsp = nullptr;
   bool lhost = false;
+  // Cursors advanced per stage and per unit instead of recomputed from the
+  // stage index (no division in the stage loop); the register-ring instance
+  // keeps the recomputation, whose registers it cannot spare.
+  constexpr bool kCursor = kStages != 0;
+  int la = lu / upe, lmb = lu - la * upe;   // the cursor's group and row block
   auto cursor_unit = [&](int u) {
-    const int a = u / upe, m0 = (u - a * upe) * BM;
+    int a = la, mb = lmb;
+    if constexpr (!kCursor) {
+      a = u / upe;
+      mb = u - a * upe;
+    }
     const Group& gr = groups[a];
     if (gr.flags & 1) {
-      lptr = reinterpret_cast<const uint4*>(gr.w + ((size_t)(m0 / BM) * KS + k0 / SK) * kChunk) + r;
-      lsp = reinterpret_cast<const unsigned short*>(gr.s) + ((size_t)(m0 / BM) * KG + g0) * BM + r;
+      lptr = reinterpret_cast<const uint4*>(gr.w + ((size_t)mb * KS + k0 / SK) * kChunk) + r;
+      lsp = reinterpret_cast<const unsigned short*>(gr.s) + ((size_t)mb * KG + g0) * BM + r;
       lhost = (gr.flags & 2) != 0;
     } else {
       lptr = nullptr;
@@ -1007,7 +1016,8 @@ __global__ void __launch_bounds__(kThreads, 1) ffn_e4m3_kernel(const FfnParams p
   // ring slot j <- the next stage of this warpgroup's slice
   auto load_next = [&](int j) {
     if (lptr) {
-      const uint4* c = lptr + (size_t)lst * (2 * kChunk / 16);   // chunks 2*lst and 2*lst + 1 of the slice
+      // chunks 2*lst and 2*lst + 1 of the slice
+      const uint4* c = kCursor ? lptr : lptr + (size_t)lst * (2 * kChunk / 16);
       if constexpr (kStages) {
         uint8_t* d = sbuf + j * (kWG * kStageBytes8);
         if (lhost) {
@@ -1021,7 +1031,11 @@ __global__ void __launch_bounds__(kThreads, 1) ffn_e4m3_kernel(const FfnParams p
 #pragma unroll
         for (int q = 0; q < 4; ++q) ring[j][q] = __ldg(c + q * (kQuarter / 16));
       }
-      sring[j] = __ldg(lsp + (size_t)lst * BM);
+      sring[j] = __ldg(kCursor ? lsp : lsp + (size_t)lst * BM);
+      if constexpr (kCursor) {
+        lptr += 2 * kChunk / 16;
+        lsp += BM;
+      }
     } else {
       const uint4 z = make_uint4(0x88888888u, 0x88888888u, 0x88888888u, 0x88888888u);
       if constexpr (kStages) {
@@ -1036,6 +1050,12 @@ __global__ void __launch_bounds__(kThreads, 1) ffn_e4m3_kernel(const FfnParams p
     if constexpr (kStages) cp_async_commit();
     if (++lst == nst) {
       lst = 0;
+      if constexpr (kCursor) {
+        if (++lmb == upe) {
+          lmb = 0;
+          ++la;
+        }
+      }
       if (++lu < ue) cursor_unit(lu);
     }
   };
@@ -1161,6 +1181,24 @@ __global__ void __launch_bounds__(kThreads, 1) ffn_e4m3_kernel(const FfnParams p
 
     uint32_t h1 = 0, h2 = 0;   // weight scales of stages gs-1, gs-2
     int st = 0, ul = 0;
+    int rst = 0, rul = 0;      // kCursor: the next stage to read back (gs - 2) and its local unit
+    // the stage `back` stages before the current one: its stage and local unit
+    auto readback_at = [&](int back, int db, uint32_t sp) {
+      if constexpr (kCursor) {
+        readback(rst, rul, db, sp);
+        if (++rst == nst) {
+          rst = 0;
+          ++rul;
+        }
+      } else {
+        int est = st - back, eul = ul;
+        while (est < 0) {
+          est += nst;
+          --eul;
+        }
+        readback(est, eul, db, sp);
+      }
+    };
     // test hook (outside the stage loop, whose code size matters): warp 1 of
     // warpgroup 0 of the CTA owning unit 0 publishes its first stage late
     if (p.stall_ns && ub == 0 && wg == 0 && wq == 1 && lane == 0) debug_stall(p.stall_ns);
@@ -1203,14 +1241,7 @@ __global__ void __launch_bounds__(kThreads, 1) ffn_e4m3_kernel(const FfnParams p
             cp_async_commit();   // keeps the group count in step with the stages
           }
           // (3) while the store drains: read back stage gs - 2
-          if (gs >= 2) {
-            int est = st - 2, eul = ul;
-            while (est < 0) {
-              est += nst;
-              --eul;
-            }
-            readback(est, eul, ab, h2);
-          }
+          if (gs >= 2) readback_at(2, ab, h2);
           h2 = h1;
           h1 = sp;
           // (4) publish the stored A
@@ -1239,12 +1270,7 @@ __global__ void __launch_bounds__(kThreads, 1) ffn_e4m3_kernel(const FfnParams p
       mbar_wait_bounded(&done[wg * 3 + (e & 1)], (e >> 1) & 1, abort_flag, p.status, p.wait_ns);
       __syncwarp();
       tc_fence_after();
-      int est = st - back, eul = ul;
-      while (est < 0) {
-        est += nst;
-        --eul;
-      }
-      readback(est, eul, e & 1, back == 1 ? h1 : h2);
+      readback_at(back, e & 1, back == 1 ? h1 : h2);
     }
     tc_fence_before();
     if (epi >= 0) epilogue(epi);

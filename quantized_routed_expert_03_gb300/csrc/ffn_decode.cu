@@ -743,14 +743,9 @@ __device__ __noinline__ void e4m3_b_job(int job, const uint4 raw, int T, int KG,
   for (int j = 0; j < NT; ++j)
     *reinterpret_cast<uint32_t*>(Bs + jb * b_bytes + b8_offset(NT * n + j, g * SK8 + 4 * lane, BN8)) = t[j];
   if (lane == 0) {
-    float* ec = Et + jb * 2 * TT * KG;
-    if constexpr (TT == 1) {
-      ec[n * KG + g] = 512.0f * down;   // the codes carry 2^-9
-      ec[TT * KG + n * KG + g] = 8.0f * back * down;
-    } else {   // [KG][TT] pairs: a stage's factors of all tokens in 16-byte pieces
-      ec[(g * TT + n) * 2] = 512.0f * down;
-      ec[(g * TT + n) * 2 + 1] = 8.0f * back * down;
-    }
+    float* ec = Et + jb * 2 * TT * KG;   // [KG][TT] pairs: a stage's factors of all tokens together
+    ec[(g * TT + n) * 2] = 512.0f * down;   // the codes carry 2^-9
+    ec[(g * TT + n) * 2 + 1] = 8.0f * back * down;
   }
 }
 
@@ -806,9 +801,8 @@ __global__ void __launch_bounds__(kThreads, 1) ffn_e4m3_kernel(const FfnParams p
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
   const Layout8 L = make_layout8(MODE, p.K, p.nB, TT);
   uint8_t* Bs = smem + L.b_off;                                    // buffer j at j * b_bytes
-  float* Et = reinterpret_cast<float*>(smem + L.ec_off);          // buffer j at j * 2 * TT * KG: TT = 1 [KG] 2^(9-e)
-                                                                   // then [KG] 8 * sum of the represented values;
-                                                                   // TT = 8 [KG][TT] (2^(9-e), 8 * sum) pairs
+  float* Et = reinterpret_cast<float*>(smem + L.ec_off);          // buffer j at j * 2 * TT * KG: [KG][TT] pairs
+                                                                   // (2^(9-e), 8 * sum of the represented values)
   float* red = reinterpret_cast<float*>(smem + L.red_off);
   uint64_t* a_full = reinterpret_cast<uint64_t*>(smem + L.bar_off);
   uint64_t* done = a_full + kWG * 3;
@@ -1131,7 +1125,8 @@ __global__ void __launch_bounds__(kThreads, 1) ffn_e4m3_kernel(const FfnParams p
                      : "r"(tlane + tmem_wg + kD0 + BN8 * db));
         tmem_ld_wait();
         const float d = add_terms<NT>(dv);
-        acc[0] = fmaf(sc, fmaf(d, ec[g], -ec[KG + g]), acc[0]);
+        const float2 q = *reinterpret_cast<const float2*>(ec + 2 * g);   // (2^(9-e), correction)
+        acc[0] = fmaf(sc, fmaf(d, q.x, -q.y), acc[0]);
       } else {
         uint32_t dv[BN8];
         if constexpr (BN8 == 32)
@@ -1172,9 +1167,10 @@ __global__ void __launch_bounds__(kThreads, 1) ffn_e4m3_kernel(const FfnParams p
       tc_fence_after();
       const uint32_t bbuf = MODE == 0 ? 0u : (iul >= u_split ? b_bytes : 0u);
       const uint32_t bstage = bbase + bbuf + (uint32_t)((g0 + ist) * (BN8 * 128));
+      const uint64_t bdesc = umma_desc_sw128(bstage);   // + 2 per 32 bytes inside the swizzle row
 #pragma unroll
       for (int q = 0; q < 4; ++q)
-        umma_e4m3_tmem_a(tmem_wg + kD0 + BN8 * ib, tmem_wg + ib * kA8 + 8 * q, umma_desc_sw128(bstage + 32 * q), idesc,
+        umma_e4m3_tmem_a(tmem_wg + kD0 + BN8 * ib, tmem_wg + ib * kA8 + 8 * q, bdesc + (uint64_t)(2 * q), idesc,
                          q ? 1u : 0u);
       umma_commit(&done[wg * 3 + ib]);
     };

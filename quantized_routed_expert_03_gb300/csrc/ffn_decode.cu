@@ -979,9 +979,10 @@ __global__ void __launch_bounds__(kThreads, 1) ffn_e4m3_kernel(const FfnParams p
   const uint4* lptr = nullptr;
   const unsigned short* lsp = nullptr;
   bool lhost = false;
-  // Cursors advanced per stage and per unit instead of recomputed from the
-  // stage index (no division in the stage loop); the register-ring instance
-  // keeps the recomputation, whose registers it cannot spare.
+  // Weight and scale cursors advanced per stage and per unit instead of
+  // recomputed from the stage index (no division in the stage loop); the
+  // register-ring instance keeps the recomputation, whose registers it cannot
+  // spare.  (The readback's cursor is advanced in every instance.)
   constexpr bool kCursor = kStages != 0;
   int la = lu / upe, lmb = lu - la * upe;   // the cursor's group and row block
   auto cursor_unit = [&](int u) {
@@ -1177,22 +1178,12 @@ __global__ void __launch_bounds__(kThreads, 1) ffn_e4m3_kernel(const FfnParams p
 
     uint32_t h1 = 0, h2 = 0;   // weight scales of stages gs-1, gs-2
     int st = 0, ul = 0;
-    int rst = 0, rul = 0;      // kCursor: the next stage to read back (gs - 2) and its local unit
-    // the stage `back` stages before the current one: its stage and local unit
-    auto readback_at = [&](int back, int db, uint32_t sp) {
-      if constexpr (kCursor) {
-        readback(rst, rul, db, sp);
-        if (++rst == nst) {
-          rst = 0;
-          ++rul;
-        }
-      } else {
-        int est = st - back, eul = ul;
-        while (est < 0) {
-          est += nst;
-          --eul;
-        }
-        readback(est, eul, db, sp);
+    int rst = 0, rul = 0;      // the next stage to read back (gs - 2) and its local unit
+    auto readback_next = [&](int db, uint32_t sp) {
+      readback(rst, rul, db, sp);
+      if (++rst == nst) {
+        rst = 0;
+        ++rul;
       }
     };
     // test hook (outside the stage loop, whose code size matters): warp 1 of
@@ -1237,7 +1228,7 @@ __global__ void __launch_bounds__(kThreads, 1) ffn_e4m3_kernel(const FfnParams p
             cp_async_commit();   // keeps the group count in step with the stages
           }
           // (3) while the store drains: read back stage gs - 2
-          if (gs >= 2) readback_at(2, ab, h2);
+          if (gs >= 2) readback_next(ab, h2);
           h2 = h1;
           h1 = sp;
           // (4) publish the stored A
@@ -1266,7 +1257,7 @@ __global__ void __launch_bounds__(kThreads, 1) ffn_e4m3_kernel(const FfnParams p
       mbar_wait_bounded(&done[wg * 3 + (e & 1)], (e >> 1) & 1, abort_flag, p.status, p.wait_ns);
       __syncwarp();
       tc_fence_after();
-      readback_at(back, e & 1, back == 1 ? h1 : h2);
+      readback_next(e & 1, back == 1 ? h1 : h2);
     }
     tc_fence_before();
     if (epi >= 0) epilogue(epi);

@@ -577,7 +577,11 @@ def measure_workload(name, args, K, W, rank, local_rank, world, device, log, cpu
             rec["cache"]["copy_bytes_per_layer_step"] * wl.layers_per_step / (ms / K / 1e3) / 1e9, 1)
     rec["gpu_launches"] = launches_per_layer * wl.layers_per_step * K
     if not args.no_e2e:
-        rec["e2e"] = run_e2e(wl, xs, stream, device, tokens_per_step, world, max(3, min(K, args.e2e_steps)))
+        # its own step count: at least ~0.25 s of device work (a few timed steps
+        # would mostly time the pipeline filling), at most --e2e-steps; the same
+        # on every rank (ms is the slowest rank's)
+        k_e2e = max(3, min(args.e2e_steps, max(K, int(0.25 / (ms / K / 1e3)))))
+        rec["e2e"] = run_e2e(wl, xs, stream, device, tokens_per_step, world, k_e2e)
     if rank == 0 and cpu_leg and not args.no_cpu_baseline:
         rec["cpu_baseline"] = cpu_baseline(name, wl, device)
     rec["build_s"] = round(wl.build_s, 1)
@@ -677,34 +681,66 @@ def run_e2e(wl, xs, stream, device, tokens_per_step, world, K):
             graphs.append(g)
     n_x = xs[0].shape[0]
     host_x = [xs[r].cpu().pin_memory() for r in range(len(sets))]
-    host_y = [torch.empty((T, H), dtype=torch.bfloat16).pin_memory() for _ in sets]
+    # two host output buffers per set: step j's output lands in buffer j % 2
+    host_y = [[torch.empty((T, H), dtype=torch.bfloat16).pin_memory() for _ in sets] for _ in range(2)]
+    done = [torch.cuda.Event(), torch.cuda.Event()]
     h2d = (len(sets) if stack else 1) * T * H * 2
     d2h = h2d
 
+    # single-layer workloads: the copies run on two copy streams, so that step
+    # j + 1's input copy overlaps step j's replay; per layer set, events keep
+    # the input from being overwritten before its last replay has read it, and
+    # the output from being overwritten before it has been copied out
+    cs_in, cs_out = torch.cuda.Stream(device), torch.cuda.Stream(device)
+    g_done = [torch.cuda.Event() for _ in sets]
+    in_done = [torch.cuda.Event() for _ in sets]
+    out_done = [torch.cuda.Event() for _ in sets]
+    used = [False] * len(sets)
+
     def one(j):
+        b = j % 2
         if stack:
             for r in range(len(sets)):
                 xin_dev[r].copy_(host_x[r][j % n_x], non_blocking=True)
             graphs[0].replay()
             for r in range(len(sets)):
-                host_y[r].copy_(sets[r]["layer"].y_bf16[:T], non_blocking=True)
+                host_y[b][r].copy_(sets[r]["layer"].y_bf16[:T], non_blocking=True)
+            done[b].record(stream)
+            if j >= 1:
+                done[1 - b].synchronize()   # step j - 1's output is on the host before step j + 1 is queued
         else:
             r = j % len(sets)
-            xin_dev[r].copy_(host_x[r][(j // len(sets)) % n_x], non_blocking=True)
+            if used[r]:
+                cs_in.wait_event(g_done[r])
+            with torch.cuda.stream(cs_in):
+                xin_dev[r].copy_(host_x[r][(j // len(sets)) % n_x], non_blocking=True)
+            in_done[r].record(cs_in)
+            stream.wait_event(in_done[r])
+            if used[r]:
+                stream.wait_event(out_done[r])
             graphs[r].replay()
-            host_y[r].copy_(sets[r]["layer"].y_bf16[:T], non_blocking=True)
-        stream.synchronize()
+            g_done[r].record(stream)
+            cs_out.wait_event(g_done[r])
+            with torch.cuda.stream(cs_out):
+                host_y[b][r].copy_(sets[r]["layer"].y_bf16[:T], non_blocking=True)
+            out_done[r].record(cs_out)
+            used[r] = True
+            if j >= 1:
+                out_done[(j - 1) % len(sets)].synchronize()   # step j - 1's output is on the host
 
     with torch.cuda.stream(stream):
-        for j in range(3):
+        for j in range(max(3, 2 * len(graphs))):   # every graph replayed (its first replay is slow) before timing
             one(j)
         torch.cuda.synchronize()
         if world > 1:
             torch.distributed.barrier()
         s0, s1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         s0.record(stream)
+        cs_in.wait_event(s0)   # no copy of the timed steps starts before the timed region
         for j in range(K):
             one(j)
+        if not stack:
+            stream.wait_event(out_done[(K - 1) % len(sets)])   # ends with the last output on the host
         s1.record(stream)
         torch.cuda.synchronize()
     ms = max_over_ranks(s0.elapsed_time(s1), world)
@@ -712,7 +748,10 @@ def run_e2e(wl, xs, stream, device, tokens_per_step, world, K):
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
             "api": "the layer's C-ABI calls (route, dispatch, [cache update + miss copy], expert FFN, combine) "
                    "through the binding, captured in a CUDA graph; per step: pinned H2D input copy, replay, "
-                   "pinned D2H of the bf16 output, stream synchronize"}
+                   "pinned D2H of the bf16 output into one of two host buffers; the host waits for step j-1's "
+                   "output before it queues step j+1 (at most two steps in flight); single-layer workloads "
+                   "copy on two copy streams ordered by events, so a step's input copy overlaps the replay "
+                   "before it; the timed region ends when the last output is on the host"}
 
 
 # ------------------------------------------------------------------ oracle (CPU) legs

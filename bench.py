@@ -710,13 +710,16 @@ def run_e2e(wl, xs, stream, device, tokens_per_step, world, K):
                 done[1 - b].synchronize()   # step j - 1's output is on the host before step j + 1 is queued
         else:
             r = j % len(sets)
-            if used[r]:
+            # set r's previous step is j - n; when the host queues step j it has
+            # step j - 2's output, so with two or more sets that step is done
+            # (its replay read the input, its output was copied) and needs no wait
+            if used[r] and len(sets) < 2:
                 cs_in.wait_event(g_done[r])
             with torch.cuda.stream(cs_in):
                 xin_dev[r].copy_(host_x[r][(j // len(sets)) % n_x], non_blocking=True)
             in_done[r].record(cs_in)
             stream.wait_event(in_done[r])
-            if used[r]:
+            if used[r] and len(sets) < 2:
                 stream.wait_event(out_done[r])
             graphs[r].replay()
             g_done[r].record(stream)

@@ -373,7 +373,7 @@ def measure_workload(name, args, K, W, rank, local_rank, world, device, log, cpu
     wl = Workload(name, device, n_sets=args.sets if name == args.workload else None, log=log)
     cfg, T, H, k = wl.cfg, wl.T, wl.cfg.hidden, wl.cfg.top_k
     # host-mapped experts in the tables: cut the decode work at equal cost
-    host_cost = args.host_unit_cost if args.host_unit_cost is not None else (4 if cfg.host_tier else 0)
+    host_cost = args.host_unit_cost if args.host_unit_cost is not None else (3 if cfg.host_tier else 0)
     qre.qre_set_host_unit_cost(host_cost)
     stream = torch.cuda.Stream(device)
 
@@ -893,7 +893,7 @@ def main():
     ap.add_argument("--side-stream", action="store_true",
                     help="run the shared expert on a second stream beside the router and dispatch")
     ap.add_argument("--host-unit-cost", type=int, default=None,
-                    help="decode work cut: cost of a host-mapped unit (default 4 with host-resident experts, else 0)")
+                    help="decode work cut: cost of a host-mapped unit (default 3 with host-resident experts, else 0)")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-clocks", action="store_true")

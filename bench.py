@@ -877,7 +877,7 @@ def run_reference(args):
             "e2e": {"value": round(value, 6), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
 
 
-def main():
+def make_parser() -> argparse.ArgumentParser:
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=20000)
@@ -899,6 +899,11 @@ def main():
     ap.add_argument("--no-clocks", action="store_true")
     ap.add_argument("--traffic", type=float, default=None,
                     help="ncu dram bytes per FFN launch, when a capture of the current kernels exists")
+    return ap
+
+
+def main():
+    ap = make_parser()
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")

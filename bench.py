@@ -68,7 +68,7 @@ def dist_env():
 # DRAM bytes per expert-FFN call (both kernels) measured with ncu on a workload,
 # for the FFN kernel code with the given hash (ffn_source_hash).  Reported only
 # while the sources still hash to that value; a changed kernel reports null.
-MEASURED_TRAFFIC = {"decode1": (117426432, "dc2e76bf8e8cb0c3")}
+MEASURED_TRAFFIC = {"decode1": (117420416, "a0f8835ccb0da49a")}
 FFN_SOURCES = ("ffn_decode.cu", "common.cuh", "tc.cuh", "internal.h")
 
 

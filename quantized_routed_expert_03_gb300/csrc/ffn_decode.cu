@@ -152,7 +152,7 @@ template <int MODE, int TT, bool H32 = false>
 __device__ __noinline__ void finish_unit(int v, int ub, int upe, const Group* groups, const float* red,
                                          uint64_t* red_full, uint64_t* red_empty, int kq, int T, int I, int H,
                                          __half* hbuf, float* expert_out, volatile int* abort_flag, int* status,
-                                         uint64_t wait_ns) {
+                                         uint64_t wait_ns, float own0 = 0.f, float own1 = 0.f) {
   const int tid = threadIdx.x, lane = tid & 31, wg = tid >> 7, r = tid & 127;
   const int u = ub + v, a = u / upe, m0 = (u - a * upe) * BM;
   const Group& gr = groups[a];
@@ -163,8 +163,17 @@ __device__ __noinline__ void finish_unit(int v, int ub, int upe, const Group* gr
     float vv[NT];
 #pragma unroll
     for (int t = 0; t < NT; ++t) vv[t] = 0.f;
+    // FP8 down kernel, eight tokens: warpgroup w stores every token but its own
+    // two (2w, 2w + 1), which it passes in own0/own1; same terms, same order
+    constexpr bool kOwn = H32 && MODE == 1 && TT == 8;
+    constexpr int RT = kOwn ? TT - 2 : TT;
     for (int w = 0; w < kq; ++w) {
-      const float* rr = red + ((size_t)((v & 1) * kWG + w) * BM + r) * TT + n0;
+      if (kOwn && w == wg) {
+        vv[0] += own0;
+        vv[NT - 1] += own1;
+        continue;
+      }
+      const float* rr = red + ((size_t)((v & 1) * kWG + w) * BM + r) * RT + (kOwn && n0 > 2 * w ? n0 - 2 : n0);
 #pragma unroll
       for (int t = 0; t < NT; ++t) vv[t] += rr[t];
     }
@@ -654,11 +663,14 @@ __host__ __device__ constexpr int bn8(int MODE, int TT) { return n_terms(MODE) *
 // Where shared memory allows, the weights stream through a ring of stages
 // that every thread fills with cp.async (its own 4 x 16 bytes per stage, read
 // back by itself, so only cp.async groups order them): kStages8 stages in
-// flight without holding registers.  The down kernel for eight tokens keeps a
-// register ring (two experts' h take 128 KB).
+// flight without holding registers.  The down kernel for eight tokens fits
+// its ring beside two experts' h (128 KB) because each warpgroup keeps the
+// partial sums of the two tokens it finishes in registers instead of the
+// reduction area (red_tt).
 constexpr int kStages8 = 2;
 constexpr int kStageBytes8 = BM * SK8 / 2;   // one warpgroup's stage: 128 rows x 128 nibbles
-__host__ __device__ constexpr int ring8_stages(int MODE, int TT) { return (TT == 1 || MODE == 0) ? kStages8 : 0; }
+// fp32 partials per (warpgroup, row) in the reduction area
+__host__ __device__ constexpr int red_tt(int MODE, int TT) { return (MODE == 1 && TT == 8) ? TT - 2 : TT; }
 
 struct Layout8 {
   int b_off, ec_off, ring_off, red_off, bar_off, grp_off, misc_off;
@@ -670,8 +682,8 @@ __host__ __device__ inline Layout8 make_layout8(int MODE, int K, int nB, int TT)
   L.b_off = 0;                                          // nB x (bn8 rows x K bytes, swizzled; 1024-aligned)
   L.ec_off = L.b_off + nB * bn8(MODE, TT) * K;          // nB x 2 x TT x K/128 fp32 factors (see Et)
   L.ring_off = (L.ec_off + nB * 2 * TT * (K / SK8) * 4 + 127) & ~127;   // [stage][kWG] x 8 KB
-  L.red_off = L.ring_off + ring8_stages(MODE, TT) * kWG * kStageBytes8;   // 2 x kWG x BM x TT fp32
-  L.bar_off = L.red_off + 2 * kWG * BM * TT * 4;
+  L.red_off = L.ring_off + kStages8 * kWG * kStageBytes8;   // 2 x kWG x BM x red_tt fp32
+  L.bar_off = L.red_off + 2 * kWG * BM * red_tt(MODE, TT) * 4;
   L.grp_off = L.bar_off + (kWG * 6 + 4 + kThreads / 32) * 8;
   L.misc_off = L.grp_off + kMaxGroups * (int)sizeof(Group);
   L.bytes = (size_t)L.misc_off + 16 + 1024;
@@ -790,8 +802,8 @@ __device__ __noinline__ int2 unit_range(const Group* groups, int ngroups, int up
 
 template <int MODE, int TT, bool HC = false>
 __global__ void __launch_bounds__(kThreads, 1) ffn_e4m3_kernel(const FfnParams p) {
-  constexpr int kStages = ring8_stages(MODE, TT);   // shared-memory ring depth (0: register ring)
-  constexpr int R = kStages ? kStages : 2;          // ring depth = unroll
+  constexpr int kStages = kStages8;                 // shared-memory ring depth
+  constexpr int R = kStages;                        // ring depth = unroll
   constexpr int NA = 2;                    // A buffers (and D buffers) per warpgroup
   constexpr int NT = n_terms(MODE);
   constexpr int BN8 = bn8(MODE, TT);       // MMA N
@@ -980,17 +992,10 @@ __global__ void __launch_bounds__(kThreads, 1) ffn_e4m3_kernel(const FfnParams p
   const unsigned short* lsp = nullptr;
   bool lhost = false;
   // Weight and scale cursors advanced per stage and per unit instead of
-  // recomputed from the stage index (no division in the stage loop); the
-  // register-ring instance keeps the recomputation, whose registers it cannot
-  // spare.  (The readback's cursor is advanced in every instance.)
-  constexpr bool kCursor = kStages != 0;
+  // recomputed from the stage index (no division in the stage loop).
   int la = lu / upe, lmb = lu - la * upe;   // the cursor's group and row block
-  auto cursor_unit = [&](int u) {
-    int a = la, mb = lmb;
-    if constexpr (!kCursor) {
-      a = u / upe;
-      mb = u - a * upe;
-    }
+  auto cursor_unit = [&]() {
+    const int a = la, mb = lmb;
     const Group& gr = groups[a];
     if (gr.flags & 1) {
       lptr = reinterpret_cast<const uint4*>(gr.w + ((size_t)mb * KS + k0 / SK) * kChunk) + r;
@@ -1001,8 +1006,7 @@ __global__ void __launch_bounds__(kThreads, 1) ffn_e4m3_kernel(const FfnParams p
       lsp = nullptr;
     }
   };
-  cursor_unit(lu);
-  uint4 ring[kStages ? 1 : R][4];   // register ring (no shared-memory ring)
+  cursor_unit();
   uint32_t sring[R];                // weight scales of the stages in flight
   // shared-memory ring: this thread's 16 bytes of each quarter
   // of slot 0; slot j, quarter c at + j * kWG * kStageBytes8 + c * 2048
@@ -1012,46 +1016,32 @@ __global__ void __launch_bounds__(kThreads, 1) ffn_e4m3_kernel(const FfnParams p
   auto load_next = [&](int j) {
     if (lptr) {
       // chunks 2*lst and 2*lst + 1 of the slice
-      const uint4* c = kCursor ? lptr : lptr + (size_t)lst * (2 * kChunk / 16);
-      if constexpr (kStages) {
-        uint8_t* d = sbuf + j * (kWG * kStageBytes8);
-        if (lhost) {
+      const uint4* c = lptr;
+      uint8_t* d = sbuf + j * (kWG * kStageBytes8);
+      if (lhost) {
 #pragma unroll
-          for (int q = 0; q < 4; ++q) *reinterpret_cast<uint4*>(d + q * kQuarter) = __ldg(c + q * (kQuarter / 16));
-        } else {
-#pragma unroll
-          for (int q = 0; q < 4; ++q) cp_async_16(d + q * kQuarter, c + q * (kQuarter / 16));
-        }
+        for (int q = 0; q < 4; ++q) *reinterpret_cast<uint4*>(d + q * kQuarter) = __ldg(c + q * (kQuarter / 16));
       } else {
 #pragma unroll
-        for (int q = 0; q < 4; ++q) ring[j][q] = __ldg(c + q * (kQuarter / 16));
+        for (int q = 0; q < 4; ++q) cp_async_16(d + q * kQuarter, c + q * (kQuarter / 16));
       }
-      sring[j] = __ldg(kCursor ? lsp : lsp + (size_t)lst * BM);
-      if constexpr (kCursor) {
-        lptr += 2 * kChunk / 16;
-        lsp += BM;
-      }
+      sring[j] = __ldg(lsp);
+      lptr += 2 * kChunk / 16;
+      lsp += BM;
     } else {
       const uint4 z = make_uint4(0x88888888u, 0x88888888u, 0x88888888u, 0x88888888u);
-      if constexpr (kStages) {
 #pragma unroll
-        for (int q = 0; q < 4; ++q) *reinterpret_cast<uint4*>(sbuf + j * (kWG * kStageBytes8) + q * kQuarter) = z;
-      } else {
-#pragma unroll
-        for (int q = 0; q < 4; ++q) ring[j][q] = z;
-      }
+      for (int q = 0; q < 4; ++q) *reinterpret_cast<uint4*>(sbuf + j * (kWG * kStageBytes8) + q * kQuarter) = z;
       sring[j] = 0;
     }
-    if constexpr (kStages) cp_async_commit();
+    cp_async_commit();
     if (++lst == nst) {
       lst = 0;
-      if constexpr (kCursor) {
-        if (++lmb == upe) {
-          lmb = 0;
-          ++la;
-        }
+      if (++lmb == upe) {
+        lmb = 0;
+        ++la;
       }
-      if (++lu < ue) cursor_unit(lu);
+      if (++lu < ue) cursor_unit();
     }
   };
   if (wg < p.kq) {
@@ -1059,7 +1049,7 @@ __global__ void __launch_bounds__(kThreads, 1) ffn_e4m3_kernel(const FfnParams p
     for (int j = 0; j < R; ++j) {
       if (j < NS) {
         load_next(j);
-      } else if constexpr (kStages) {
+      } else {
         cp_async_commit();   // one group per ring slot, loaded or not
       }
     }
@@ -1096,9 +1086,12 @@ __global__ void __launch_bounds__(kThreads, 1) ffn_e4m3_kernel(const FfnParams p
   tc_fence_after();
 
 
+  // eight-token down kernel: this thread's partials of its own two tokens, by unit parity
+  float own[2][2] = {{0.f, 0.f}, {0.f, 0.f}};
   auto epilogue = [&](int v) {
     finish_unit<MODE, TT, true>(v, ub, upe, groups, red, red_full, red_empty, p.kq, p.T, p.I, p.H, p.hbuf,
-                                p.expert_out, abort_flag, p.status, p.wait_ns);
+                                p.expert_out, abort_flag, p.status, p.wait_ns, (v & 1) ? own[1][0] : own[0][0],
+                                (v & 1) ? own[1][1] : own[0][1]);
   };
   int epi = -1;
 
@@ -1150,11 +1143,30 @@ __global__ void __launch_bounds__(kThreads, 1) ffn_e4m3_kernel(const FfnParams p
           epi = -1;
         }
         if (eul >= 2) mbar_wait_bounded(&red_empty[eul & 1], ((eul >> 1) - 1) & 1, abort_flag, p.status, p.wait_ns);
-        float* rw = red + ((size_t)((eul & 1) * kWG + wg) * BM + r) * TT;
+        constexpr int RT = red_tt(MODE, TT);
+        float* rw = red + ((size_t)((eul & 1) * kWG + wg) * BM + r) * RT;
+        if constexpr (RT == TT) {
 #pragma unroll
-        for (int n = 0; n < TT; ++n) {
-          rw[n] = acc[n];
-          acc[n] = 0.f;
+          for (int n = 0; n < TT; ++n) {
+            rw[n] = acc[n];
+            acc[n] = 0.f;
+          }
+        } else {
+          // tokens 2wg, 2wg + 1 stay in registers for this warpgroup's own epilogue
+          const float m0 = wg == 0 ? acc[0] : (wg == 1 ? acc[2] : (wg == 2 ? acc[4] : acc[6]));
+          const float m1 = wg == 0 ? acc[1] : (wg == 1 ? acc[3] : (wg == 2 ? acc[5] : acc[7]));
+          if (eul & 1) {
+            own[1][0] = m0;
+            own[1][1] = m1;
+          } else {
+            own[0][0] = m0;
+            own[0][1] = m1;
+          }
+#pragma unroll
+          for (int n = 0; n < TT; ++n) {
+            if ((n >> 1) != wg) rw[n < 2 * wg ? n : n - 2] = acc[n];
+            acc[n] = 0.f;
+          }
         }
         mbar_arrive(&red_full[eul & 1]);
         if (eul >= 1) epi = eul - 1;
@@ -1203,15 +1215,10 @@ __global__ void __launch_bounds__(kThreads, 1) ffn_e4m3_kernel(const FfnParams p
           // (2) split 128 nibbles of this row into 128 E4M3 codes, store them in TMEM
           {
             uint4 cur[4];
-            if constexpr (kStages) {
-              cp_async_wait_group<kStages - 1>();   // slot j's group (the oldest in flight) has landed
+            cp_async_wait_group<kStages - 1>();   // slot j's group (the oldest in flight) has landed
 #pragma unroll
-              for (int q = 0; q < 4; ++q)
-                cur[q] = *reinterpret_cast<const uint4*>(sbuf + j * (kWG * kStageBytes8) + q * kQuarter);
-            } else {
-#pragma unroll
-              for (int q = 0; q < 4; ++q) cur[q] = ring[j][q];
-            }
+            for (int q = 0; q < 4; ++q)
+              cur[q] = *reinterpret_cast<const uint4*>(sbuf + j * (kWG * kStageBytes8) + q * kQuarter);
             uint32_t av[32];
 #pragma unroll
             for (int c = 0; c < 4; ++c) {
@@ -1224,7 +1231,7 @@ __global__ void __launch_bounds__(kThreads, 1) ffn_e4m3_kernel(const FfnParams p
           const uint32_t sp = sring[j];
           if (gs + R < NS) {
             load_next(j);
-          } else if constexpr (kStages) {
+          } else {
             cp_async_commit();   // keeps the group count in step with the stages
           }
           // (3) while the store drains: read back stage gs - 2

@@ -35,3 +35,14 @@ def test_profile_bench_commands_parse():
             assert w in synthetic.CONFIGS, (name, w)
         n += 1
     assert n >= 6
+
+
+def test_profile_ncu_commands_leave_the_clocks_alone():
+    n = 0
+    for path in sorted(PROFILES.glob("*.md")):
+        text = re.sub(r"\\\n\s*", " ", path.read_text())
+        for line in text.splitlines():
+            if re.match(r"\s*ncu\s+-", line):
+                assert "--clock-control none" in line, (path.name, line.strip()[:80])
+                n += 1
+    assert n >= 6
